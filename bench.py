@@ -1,0 +1,390 @@
+"""Benchmark: KDA training forward + backward throughput (token*heads/s) on GB300.
+
+One step = kda_fwd + kda_bwd (every kernel of the path) over the packed
+8 x 1024-token, 96-head workload (K = V = 128), synthetic seeded inputs
+(kda_inputs.py), already resident in HBM. Each input tensor is larger than the
+129 MB L2, so no flush is needed between steps. Timing: CUDA events on the
+launching stream, W untimed warm-up steps, then exactly K timed steps between
+a barrier + synchronize on both sides; the max over ranks is reported.
+
+Also reported on the same JSON line:
+  roofline      the dominant kernel's achieved algorithmic HBM bytes/s against
+                the measured copy bandwidth (MEASURED_PEAKS.json);
+  e2e           the same metric with inputs in pinned host memory, copied in and
+                all results copied out inside the timed region;
+  cpu_baseline  the FP64 oracle timed on this host on a bounded sample;
+  clocks        nvidia-smi SM clocks and throttle reasons sampled while timing.
+
+``--impl reference`` times the oracle itself (the only reference implementation
+of this method available here) as the reference arm.
+Multi-GPU (torchrun, N > 1): every rank runs its own copy of the workload on its
+own GPU with no collective on the data path (weak scaling, replicas).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "packed_8x1024_h96"
+METRIC = "KDA fwd+bwd token·heads/s (1 GB300) and fraction of roofline"
+UNIT = "token·heads/s"
+DIM = 128
+
+
+def algorithmic_bytes(total_tokens, hqk, hv, units):
+    """Compulsory HBM bytes of one forward and one backward (each tensor read or
+    written once): per token 1536 Hqk + 2054 Hv, per unit 4 states of 64 KiB."""
+    fwd_tok = 512 * hqk + 512 * hv + 2 * hv + 256 * hv
+    bwd_tok = (512 * hqk + 512 * hv + 2 * hv + 256 * hv) + 512 * hqk + 512 * hv + 2 * hv
+    state = DIM * DIM * 4
+    return {"fwd": total_tokens * fwd_tok + units * 2 * state,
+            "bwd": total_tokens * bwd_tok + units * 2 * state}
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def kernel_source_sha(name):
+    path = os.path.join(ROOT, "linear_attention_gated_gb300", "csrc", name)
+    if not os.path.exists(path):
+        return None
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, or None if absent or
+    taken on a different version of the kernel's source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel)
+    if not d or d.get("source_sha") != kernel_source_sha(d.get("source", "")):
+        return None
+    return d.get("bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world, device=None):
+    """Largest value over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, world, max_seconds):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def oracle_sample_run(x, heads, r):
+    """Time the FP64 oracle's forward + backward on the given query/key heads."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from kda_test_utils import FWD_KEYS, slice_heads
+    y = slice_heads(x, heads, r)
+    f = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in y.items()}
+    t0 = time.perf_counter()
+    oracle.forward(*[f[k] for k in FWD_KEYS], cu_seqlens=f.get("cu_seqlens"))
+    oracle.backward(*[f[k] for k in FWD_KEYS], f["do"], f["dfinal_state"], cu_seqlens=f.get("cu_seqlens"))
+    return time.perf_counter() - t0, oracle.num_threads()
+
+
+def cpu_baseline(x, w, target_s=12.0):
+    """Oracle on a bounded sample: query/key heads in order, grown until about target_s."""
+    r = w.hv // w.hqk
+    token_heads_per_qk = x["q"].shape[0] * x["q"].shape[1] * r
+    nh = 1
+    dt, cores = oracle_sample_run(x, list(range(nh)), r)
+    while dt < target_s / 4 and nh < w.hqk:
+        nh = min(w.hqk, max(nh + 1, int(nh * target_s / max(dt, 1e-3) * 0.5)))
+        dt, cores = oracle_sample_run(x, list(range(nh)), r)
+    th = nh * token_heads_per_qk
+    return {"value": th / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{WORKLOAD}: query/key heads 0..{nh - 1} of {w.hqk} (all sequences), "
+                      f"{th} token·heads, FP64 forward + backward, {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    import kda_inputs as ki
+    if rank != 0:
+        return
+    w = ki.WORKLOADS[WORKLOAD]
+    x = ki.workload_inputs(WORKLOAD)
+    r = w.hv // w.hqk
+    heads = list(range(2))
+    th = len(heads) * x["q"].shape[1] * r
+    for _ in range(args.warmup):
+        oracle_sample_run(x, heads, r)
+    times = []
+    cores = 0
+    for _ in range(args.steps):
+        dt, cores = oracle_sample_run(x, heads, r)
+        times.append(dt)
+    total = sum(times)
+    value = th * args.steps / total
+    sample = (f"{WORKLOAD}: query/key heads {heads} of {w.hqk} (all sequences) per step, "
+              f"{th} token·heads, FP64 forward + backward")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+
+    import kda_inputs as ki
+    from linear_attention_gated_gb300 import kda_bwd, kda_fwd, load_library
+    from linear_attention_gated_gb300 import build as cuda_build
+
+    cuda_build.build()
+    load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = ki.WORKLOADS[WORKLOAD]
+    x = ki.workload_inputs(WORKLOAD)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cu_cpu = x["cu_seqlens"]
+    N = cu_cpu.numel() - 1
+    Ttot = int(cu_cpu[-1])
+    units = N * w.hv
+    token_heads = Ttot * w.hv
+    stream = torch.cuda.current_stream(dev)
+
+    o = torch.empty_like(d["v"])
+    hT = torch.empty_like(d["h0"])
+    grads = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+             torch.empty_like(d["g"]), torch.empty_like(d["beta"]), torch.empty_like(d["A_log"]),
+             torch.empty_like(d["dt_bias"]), torch.empty_like(d["h0"]))
+    ctx = None
+
+    def step(evs=None):
+        nonlocal ctx
+        if evs:
+            evs[0].record(stream)
+        _, _, ctx = kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"],
+                            d["h0"], cu_seqlens=d["cu_seqlens"], out=o, final_state_out=hT,
+                            context_out=ctx, cu_seqlens_cpu=cu_cpu)
+        if evs:
+            evs[1].record(stream)
+        kda_bwd(ctx, d["do"], d["dfinal_state"], out=grads)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed = max_over_ranks(elapsed, world, dev)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    value = job_value(token_heads, world, elapsed)
+
+    ab = algorithmic_bytes(Ttot, w.hqk, w.hv, units)
+    peaks = read_peaks()
+    fwd_avg, bwd_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dom, dom_ms = ("kda_bwd_kernel", bwd_avg) if bwd_avg >= fwd_avg else ("kda_fwd_kernel", fwd_avg)
+    dom_bytes = ab["bwd"] if dom == "kda_bwd_kernel" else ab["fwd"]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom),
+                "kernel": dom, "peak_src": peaks["src"],
+                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                "step_frac": (ab["fwd"] + ab["bwd"]) / (elapsed / args.steps) / 1e9 / peaks["hbm_gbs"],
+                "fwd_ms": fwd_avg, "bwd_ms": bwd_avg}
+    launches_per_step = 2 + (1 if w.hv != w.hqk else 0) + 1  # fwd, bwd, param reduce, GQA reduce
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sequences": N, "tokens": Ttot, "Hqk": w.hqk, "Hv": w.hv,
+                       "head_dim": DIM, "token_heads_per_gpu": token_heads, "io_dtype": "bf16",
+                       "state_dtype": "fp32", "l2": "inputs larger than L2 (each token tensor "
+                       f"{d['q'].numel() * 2 / 1e6:.0f} MB > 129 MB), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+            "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=5):
+    """Inputs in pinned host memory; each step copies them in, runs the C-ABI
+    forward and backward, and copies every result out, all inside the timing."""
+    import torch
+    names_in = ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "h0", "cu_seqlens", "do", "dfinal_state"]
+    host_in = {k: x[k].pin_memory() for k in names_in}
+    dev_in = {k: torch.empty_like(d[k]) for k in names_in}
+    cu_cpu = x["cu_seqlens"]
+    outs_dev = None
+    host_out = None
+    ctx = None
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+
+    def one():
+        nonlocal ctx, outs_dev, host_out
+        for k in names_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        o, hT, ctx = kda_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
+                             dev_in["A_log"], dev_in["dt_bias"], dev_in["h0"],
+                             cu_seqlens=dev_in["cu_seqlens"], context_out=ctx, cu_seqlens_cpu=cu_cpu)
+        grads = kda_bwd(ctx, dev_in["do"], dev_in["dfinal_state"])
+        outs_dev = (o, hT) + tuple(grads)
+        if host_out is None:
+            host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
+        for h_, t in zip(host_out, outs_dev):
+            h_.copy_(t, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    el = max_over_ranks(a.elapsed_time(b) / 1e3, world, dev)
+    return {"value": job_value(token_heads, world, el / steps), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) recurrent KDA training forward/backward.
+ *
+ * The method: Kimi Delta Attention, a gated delta rule with a per-key-dimension
+ * decay and a value-first FP32 state S[V, K] per (sequence, value head),
+ * K = V = 128. Per token (flashinfer.kda_backward.recurrent_kda_backward,
+ * description; flashinfer.kda.recurrent_kda, parameter lower_bound):
+ *   q^ = q / sqrt(|q|^2 + 1e-6),   k^ = k / sqrt(|k|^2 + 1e-6)
+ *   d  = exp(lower_bound * sigmoid(exp(A_log[h]) * (g + dt_bias[h])))   (per key dim)
+ *   beta = sigmoid(beta_logit)
+ *   S' = S diag(d);  u = v - S' k^;  S = S' + beta u k^T;  o = scale S q^
+ * The pages give the gate, norm, beta, scale and shape contracts; the order of
+ * the update (decay, delta correction, rank-1 write, output from the updated
+ * state) is the plain reading this library adopts.
+ *
+ * Two entry points form one training pair (flashinfer.kda_training, module
+ * description): kda_fwd returns the output, the final state and a saved
+ * context; kda_bwd consumes that context (it never reruns the forward) and
+ * returns the eight gradients in the documented order
+ * (dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dinitial_state).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensor pointers are DEVICE pointers to contiguous row-major storage, owned
+ *    by the caller, on the current CUDA device. The only host pointer is the
+ *    trusted cu_seqlens mirror (flashinfer.kda_training.recurrent_kda_training_forward,
+ *    parameter cu_seqlens_cpu).
+ *  - BF16 tensors are passed as kda_bf16 (raw bfloat16 bits).
+ *  - `stream` is a cudaStream_t (struct CUstream_st*); NULL is the legacy
+ *    default stream. All work is enqueued asynchronously on it.
+ *  - Argument errors are detected on the host before any launch; nothing is
+ *    enqueued and the call returns a non-zero kda_status. A message describing
+ *    the last failure on the calling thread is available from
+ *    kda_last_error_message().
+ *  - Outputs are overwritten, never accumulated into.
+ *  - Thread safety: distinct contexts may be used from different threads;
+ *    calls sharing one context must be serialised by the caller.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef uint16_t kda_bf16;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARGUMENT = 1,    /* null pointer, bad shape, bad cu_seqlens, empty sequence */
+  KDA_ERR_UNSUPPORTED = 2,         /* head dim != 128, scale != 1/sqrt(128), lower_bound != -5,
+                                      device not compute capability 10.3 */
+  KDA_ERR_ALIASING = 3,            /* an output overlaps an input, another output or the context */
+  KDA_ERR_CONTEXT = 4,             /* context shape/device/stream mismatch, or context busy */
+  KDA_ERR_CUDA = 5,                /* a CUDA runtime call failed */
+  KDA_ERR_DEVICE_TIMEOUT = 6,      /* a bounded device-side wait gave up (see kda_ctx_status) */
+  KDA_ERR_WORKSPACE_TOO_SMALL = 7  /* ctx_bytes below kda_ctx_workspace_bytes() */
+} kda_status;
+
+/* Opaque saved-forward context: host metadata (shapes, the launch plan), the
+ * borrowed input pointers and offsets into the caller's workspace, which holds
+ * the state checkpoints and the backward's scratch. */
+typedef struct kda_ctx kda_ctx;
+
+/*
+ * Bytes of device workspace one context needs for this problem.
+ *   Fixed layout  (flashinfer.kda_training, module description): cu_seqlens_host = NULL,
+ *                 num_seqs ignored; B >= 1 sequences of T >= 1 tokens each.
+ *   Packed layout: B == 1, cu_seqlens_host[num_seqs + 1] with cu[0] = 0,
+ *                 cu[num_seqs] = T and every sequence non-empty.
+ * Writes the size to *bytes. Returns KDA_ERR_INVALID_ARGUMENT on a bad shape.
+ */
+kda_status kda_ctx_workspace_bytes(int64_t B, int64_t T, int64_t Hqk, int64_t Hv,
+                                   const int64_t* cu_seqlens_host, int64_t num_seqs,
+                                   size_t* bytes);
+
+/*
+ * Training forward (flashinfer.kda_training.recurrent_kda_training_forward).
+ * Inputs (device, contiguous):
+ *   q, k     BF16 [B, T, Hqk, 128]      v, g  BF16 [B, T, Hv, 128]
+ *   beta     BF16 [B, T, Hv]  raw logits       A_log FP32 [Hv]   dt_bias FP32 [Hv, 128]
+ *   h0       FP32 [N, Hv, 128, 128] value-first initial state (N = B fixed, num_seqs packed)
+ *   cu_seqlens_dev  INT64 [num_seqs + 1] for packed input, NULL for fixed input
+ *   cu_seqlens_host its trusted host mirror (NULL for fixed input); the launch plan
+ *                   (longest sequence first) is built from it and must match the device copy
+ *   head_dim must be 128; Hv % Hqk == 0 (value head h reads query/key head h / (Hv/Hqk)).
+ *   scale: NaN selects 1/sqrt(128); any other value must equal it.
+ *   lower_bound must be -5.
+ * Outputs (device, caller-owned, must not overlap any input, each other or the workspace):
+ *   o    BF16 [B, T, Hv, 128]         h_T  FP32 [N, Hv, 128, 128]
+ * Context:
+ *   ctx_workspace / ctx_bytes: device memory of at least kda_ctx_workspace_bytes(),
+ *   256-byte aligned, owned by the caller and bound to the context until it is
+ *   destroyed. *ctx == NULL creates a context; a non-NULL *ctx is reused, which
+ *   requires identical shapes, device, stream and workspace, and overwrites its
+ *   saved checkpoints. The inputs are borrowed by the context: they must stay
+ *   allocated and unmodified until kda_bwd has been enqueued.
+ */
+kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                   const kda_bf16* beta, const float* A_log, const float* dt_bias,
+                   const float* h0, const int64_t* cu_seqlens_dev,
+                   const int64_t* cu_seqlens_host, int64_t num_seqs, int64_t B, int64_t T,
+                   int64_t Hqk, int64_t Hv, int64_t head_dim, float scale, float lower_bound,
+                   kda_bf16* o, float* h_T, void* ctx_workspace, size_t ctx_bytes,
+                   kda_ctx** ctx, struct CUstream_st* stream);
+
+/*
+ * Training backward (flashinfer.kda_training, recurrent_kda_training_backward;
+ * gradient list of flashinfer.kda_backward.recurrent_kda_backward).
+ * Inputs: the context of the last kda_fwd, the output adjoint d_o BF16 [B, T, Hv, 128]
+ * and the final-state adjoint d_hT FP32 [N, Hv, 128, 128].
+ * Outputs (device, caller-owned, all written, none may overlap an input, the
+ * context workspace or each other):
+ *   dq, dk BF16 [B, T, Hqk, 128]   dv, dg BF16 [B, T, Hv, 128]   dbeta BF16 [B, T, Hv]
+ *   dA_log FP32 [Hv]   ddt_bias FP32 [Hv, 128]   dh0 FP32 [N, Hv, 128, 128]
+ * dg and dbeta are gradients with respect to the raw gate and raw beta logits.
+ * dA_log and ddt_bias are summed over all sequences and tokens in a fixed order
+ * (bitwise reproducible). Must be called on the stream and device that created
+ * the context.
+ */
+kda_status kda_bwd(kda_ctx* ctx, const kda_bf16* d_o, const float* d_hT, kda_bf16* dq,
+                   kda_bf16* dk, kda_bf16* dv, kda_bf16* dg, kda_bf16* dbeta, float* dA_log,
+                   float* ddt_bias, float* dh0, struct CUstream_st* stream);
+
+/* Synchronises the context's stream and reports the first device-side error
+ * (KDA_ERR_DEVICE_TIMEOUT if a bounded wait gave up, KDA_ERR_CUDA on a CUDA
+ * error), else KDA_OK. */
+kda_status kda_ctx_status(kda_ctx* ctx);
+
+/* Frees the host-side context. The workspace stays owned by the caller. Safe on NULL. */
+void kda_ctx_destroy(kda_ctx* ctx);
+
+/* Static description of a status code. */
+const char* kda_status_string(kda_status status);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* kda_last_error_message(void);
+
+/* Internal tiling, for tooling and tests: sub-chunk length in tokens and the
+ * checkpoint interval in tokens. */
+int32_t kda_chunk_tokens(void);
+int32_t kda_checkpoint_tokens(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

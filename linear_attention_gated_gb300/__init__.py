@@ -1,0 +1,18 @@
+"""GB300 (sm_103a) recurrent KDA training forward + backward behind a C ABI.
+
+``kda_fwd`` / ``kda_bwd`` (and the aliases ``recurrent_kda_training_forward`` /
+``recurrent_kda_training_backward``) call libkda.so; see include/kda.h.
+"""
+
+from .kda import (  # noqa: F401
+    EXPORTED,
+    GRAD_NAMES,
+    KdaContext,
+    KdaError,
+    kda_bwd,
+    kda_fwd,
+    load_library,
+    recurrent_kda_training_backward,
+    recurrent_kda_training_forward,
+    workspace_bytes,
+)

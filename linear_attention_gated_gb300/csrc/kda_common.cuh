@@ -1,0 +1,101 @@
+// kda_common.cuh -- constants, launch parameters and small device helpers
+// shared by the KDA forward and backward kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kDim = 128;      // K = V = 128 (flashinfer.kda_training, module description)
+constexpr int kChunk = 16;     // tokens per sub-chunk of the chunked (WY / UT) form
+constexpr int kCkTokens = 16;  // tokens between saved state checkpoints (multiple of kChunk)
+constexpr int kLds = 132;      // padded shared-memory row stride (floats) of 128-wide tiles
+constexpr float kNormEps = 1e-6f;  // L2-norm epsilon (recurrent_kda_backward, description)
+
+// One (sequence, value head) pair is a "unit"; it owns one 128x128 state.
+struct SeqInfo {
+  int64_t t0;       // first token of the sequence on the packed token axis
+  int64_t len;      // tokens in the sequence (>= 1)
+  int64_t ck_base;  // first checkpoint slot of the sequence
+  int64_t pad;
+};
+
+struct Problem {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* g;
+  const __nv_bfloat16* beta;
+  const float* A_log;
+  const float* dt_bias;
+  const float* h0;
+  const int32_t* order;   // launch slot -> unit id (n * Hv + h), longest sequence first
+  const SeqInfo* seq;     // [N]
+  float* ckpt;            // [n_ck, Hv, 128, 128] state at the start of every checkpoint interval
+  int64_t N, Hqk, Hv;
+  int32_t r;              // Hv / Hqk
+  float scale, lb;
+};
+
+struct FwdOut {
+  __nv_bfloat16* o;
+  float* hT;
+};
+
+struct BwdArgs {
+  const __nv_bfloat16* d_o;
+  const float* d_hT;
+  __nv_bfloat16* dq;     // written directly when r == 1
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  __nv_bfloat16* dg;
+  __nv_bfloat16* dbeta;
+  float* dh0;
+  float* dqk_part;       // r > 1: [Ttot, Hv, 2, 128] per-value-head d(q^), d(k^)
+  float* par_part;       // [N * Hv, kParStride]: per-unit ddt_bias (128) and dA_log (1)
+};
+
+constexpr int kParStride = 132;
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float* out) {
+  uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h2[i]);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* p, const float* in) {
+  uint4 raw;
+  __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = raw;
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+
+// Sum over the 16 lanes that share a token row (lanes 0-15 or 16-31 of a warp).
+__device__ __forceinline__ float row16_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 8);
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x;
+}
+
+// Launchers (defined in kda_fwd.cu / kda_bwd.cu).
+cudaError_t launch_forward(const Problem& P, const FwdOut& out, int64_t units, cudaStream_t s);
+cudaError_t launch_backward(const Problem& P, const BwdArgs& a, int64_t units, int64_t Ttot,
+                            float* dA_log, float* ddt_bias, cudaStream_t s);
+
+}  // namespace kda

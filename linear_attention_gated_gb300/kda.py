@@ -1,0 +1,248 @@
+"""Python binding of the KDA training C ABI (include/kda.h).
+
+Argument marshalling only: torch provides device memory and the current CUDA
+stream; every step of the forward and backward runs in libkda.so's kernels.
+There is no CPU fallback: if the library cannot be loaded the calls raise.
+
+Names follow the C ABI (``kda_fwd``, ``kda_bwd``); the documented training pair
+(flashinfer.kda_training.recurrent_kda_training_forward / _backward) is exposed
+under those names too.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+DIM = 128
+SCALE = 1.0 / math.sqrt(DIM)
+
+_STATUS = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIASING",
+    4: "KDA_ERR_CONTEXT", 5: "KDA_ERR_CUDA", 6: "KDA_ERR_DEVICE_TIMEOUT",
+    7: "KDA_ERR_WORKSPACE_TOO_SMALL",
+}
+
+EXPORTED = ("kda_ctx_workspace_bytes", "kda_fwd", "kda_bwd", "kda_ctx_status", "kda_ctx_destroy",
+            "kda_status_string", "kda_last_error_message", "kda_chunk_tokens",
+            "kda_checkpoint_tokens")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.name = _STATUS.get(status, str(status))
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libkda.so and declare the C signatures. Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run __graft_entry__.build() "
+                           "(or python linear_attention_gated_gb300/build.py)")
+    lib = ctypes.CDLL(path)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.kda_ctx_workspace_bytes.argtypes = [I, I, I, I, P, I, ctypes.POINTER(S)]
+    lib.kda_ctx_workspace_bytes.restype = ctypes.c_int
+    lib.kda_fwd.argtypes = [P] * 8 + [P, P, I, I, I, I, I, I, F, F, P, P, P, S, ctypes.POINTER(P), P]
+    lib.kda_fwd.restype = ctypes.c_int
+    lib.kda_bwd.argtypes = [P] * 12
+    lib.kda_bwd.restype = ctypes.c_int
+    lib.kda_ctx_status.argtypes = [P]
+    lib.kda_ctx_status.restype = ctypes.c_int
+    lib.kda_ctx_destroy.argtypes = [P]
+    lib.kda_ctx_destroy.restype = None
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_last_error_message.argtypes = []
+    lib.kda_last_error_message.restype = ctypes.c_char_p
+    lib.kda_chunk_tokens.argtypes = []
+    lib.kda_chunk_tokens.restype = ctypes.c_int32
+    lib.kda_checkpoint_tokens.argtypes = []
+    lib.kda_checkpoint_tokens.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = load_library().kda_last_error_message().decode()
+        raise KdaError(rc, msg)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _want(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
+
+
+def workspace_bytes(B, T, Hqk, Hv, cu_seqlens_cpu=None) -> int:
+    lib = load_library()
+    out = ctypes.c_size_t(0)
+    if cu_seqlens_cpu is not None:
+        cu = cu_seqlens_cpu.to(torch.int64).contiguous()
+        rc = lib.kda_ctx_workspace_bytes(B, T, Hqk, Hv, _ptr(cu), cu.numel() - 1, ctypes.byref(out))
+    else:
+        rc = lib.kda_ctx_workspace_bytes(B, T, Hqk, Hv, None, 0, ctypes.byref(out))
+    _check(rc)
+    return int(out.value)
+
+
+class KdaContext:
+    """Saved forward context: the C handle, the device workspace it owns and the
+    borrowed inputs with their tensor versions (inputs must not change between
+    the forward and the backward)."""
+
+    def __init__(self):
+        self.handle = ctypes.c_void_p(None)
+        self.workspace = None
+        self.inputs = ()
+        self.versions = ()
+        self.shape_key = None
+        self.device = None
+        self.stream = None
+
+    def _snapshot(self, inputs):
+        self.inputs = tuple(inputs)
+        self.versions = tuple(t._version for t in inputs)
+        self.ws_version = self.workspace._version
+
+    def check_unchanged(self):
+        for t, v in zip(self.inputs, self.versions):
+            if t._version != v:
+                raise KdaError(4, "an input of the forward was modified before the backward")
+        if self.workspace._version != self.ws_version:
+            raise KdaError(4, "the context workspace was modified before the backward")
+
+    def status(self):
+        _check(load_library().kda_ctx_status(self.handle))
+
+    def __del__(self):
+        try:
+            if self.handle and self.handle.value:
+                load_library().kda_ctx_destroy(self.handle)
+                self.handle = ctypes.c_void_p(None)
+        except Exception:
+            pass
+
+
+def kda_fwd(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens=None, scale=None,
+            lower_bound=-5.0, out=None, final_state_out=None, context_out=None, *,
+            cu_seqlens_cpu=None):
+    """Training forward. Returns (o BF16 [B,T,Hv,128], final_state FP32 [N,Hv,128,128], ctx)."""
+    lib = load_library()
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v, g must be [B, T, H, 128]")
+    B, T, Hqk, D = q.shape
+    Hv = v.shape[2]
+    bf, f32 = torch.bfloat16, torch.float32
+    _want(q, "q", bf); _want(k, "k", bf, q.shape); _want(v, "v", bf, (B, T, Hv, D))
+    _want(g, "g", bf, (B, T, Hv, D)); _want(beta, "beta", bf, (B, T, Hv))
+    _want(A_log, "A_log", f32, (Hv,)); _want(dt_bias, "dt_bias", f32, (Hv, D))
+    if q.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if cu_seqlens is not None:
+        if cu_seqlens_cpu is None:
+            raise ValueError("packed input requires cu_seqlens_cpu, a trusted CPU mirror of cu_seqlens")
+        _want(cu_seqlens, "cu_seqlens", torch.int64)
+        _want(cu_seqlens_cpu, "cu_seqlens_cpu", torch.int64, cu_seqlens.shape)
+        if cu_seqlens_cpu.device.type != "cpu":
+            raise ValueError("cu_seqlens_cpu must be a CPU tensor")
+        N = cu_seqlens.numel() - 1
+    else:
+        if cu_seqlens_cpu is not None:
+            raise ValueError("cu_seqlens_cpu must be omitted for fixed-length input")
+        N = B
+    _want(initial_state, "initial_state", f32, (N, Hv, D, D))
+    dev = q.device
+    o = out if out is not None else torch.empty((B, T, Hv, D), dtype=bf, device=dev)
+    hT = final_state_out if final_state_out is not None else torch.empty((N, Hv, D, D), dtype=f32, device=dev)
+    _want(o, "out", bf, (B, T, Hv, D)); _want(hT, "final_state_out", f32, (N, Hv, D, D))
+    key = (B, T, Hqk, Hv, None if cu_seqlens_cpu is None else tuple(cu_seqlens_cpu.tolist()))
+    stream = torch.cuda.current_stream(dev)
+    ctx = context_out
+    if ctx is None:
+        ctx = KdaContext()
+        nbytes = workspace_bytes(B, T, Hqk, Hv, cu_seqlens_cpu)
+        ctx.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ctx.shape_key, ctx.device, ctx.stream = key, dev, stream.cuda_stream
+    elif ctx.shape_key != key or ctx.device != dev or ctx.stream != stream.cuda_stream:
+        raise KdaError(4, "context reuse needs the same shapes, device and stream")
+    ws = ctx.workspace
+    rc = lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                     _ptr(initial_state), _ptr(cu_seqlens),
+                     _ptr(cu_seqlens_cpu) if cu_seqlens_cpu is not None else None,
+                     N if cu_seqlens is not None else 0, B, T, Hqk, Hv, D,
+                     float("nan") if scale is None else float(scale), float(lower_bound),
+                     _ptr(o), _ptr(hT), _ptr(ws), ws.numel(), ctypes.byref(ctx.handle),
+                     ctypes.c_void_p(stream.cuda_stream))
+    _check(rc)
+    ctx._snapshot((q, k, v, g, beta, A_log, dt_bias, initial_state)
+                  + ((cu_seqlens,) if cu_seqlens is not None else ()))
+    ctx.out_shapes = dict(q=tuple(q.shape), v=tuple(v.shape), beta=tuple(beta.shape),
+                          A_log=tuple(A_log.shape), dt_bias=tuple(dt_bias.shape),
+                          h0=tuple(initial_state.shape))
+    return o, hT, ctx
+
+
+GRAD_NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias", "dinitial_state")
+
+
+def kda_bwd(ctx: KdaContext, do, dfinal_state, out=None):
+    """Training backward. Returns (dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dinitial_state)."""
+    lib = load_library()
+    if not isinstance(ctx, KdaContext) or not ctx.handle.value:
+        raise KdaError(4, "not a forward context")
+    ctx.check_unchanged()
+    s = ctx.out_shapes
+    _want(do, "do", torch.bfloat16, s["v"])
+    _want(dfinal_state, "dfinal_state", torch.float32, s["h0"])
+    dev = ctx.device
+    if out is None:
+        bf, f32 = torch.bfloat16, torch.float32
+        out = (torch.empty(s["q"], dtype=bf, device=dev), torch.empty(s["q"], dtype=bf, device=dev),
+               torch.empty(s["v"], dtype=bf, device=dev), torch.empty(s["v"], dtype=bf, device=dev),
+               torch.empty(s["beta"], dtype=bf, device=dev), torch.empty(s["A_log"], dtype=f32, device=dev),
+               torch.empty(s["dt_bias"], dtype=f32, device=dev), torch.empty(s["h0"], dtype=f32, device=dev))
+    if len(out) != 8:
+        raise ValueError("out must hold eight gradient tensors in return order")
+    shapes = (s["q"], s["q"], s["v"], s["v"], s["beta"], s["A_log"], s["dt_bias"], s["h0"])
+    dtypes = (torch.bfloat16,) * 5 + (torch.float32,) * 3
+    for t, name, shp, dt in zip(out, GRAD_NAMES, shapes, dtypes):
+        _want(t, name, dt, shp)
+    stream = torch.cuda.current_stream(dev)
+    rc = lib.kda_bwd(ctx.handle, _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out],
+                     ctypes.c_void_p(stream.cuda_stream))
+    _check(rc)
+    return tuple(out)
+
+
+recurrent_kda_training_forward = kda_fwd
+
+
+def recurrent_kda_training_backward(context, do, dfinal_state, out=None):
+    return kda_bwd(context, do, dfinal_state, out=out)

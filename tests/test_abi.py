@@ -1,0 +1,179 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/kda.h declares, sizes workspaces, and rejects bad arguments on the host
+before any CUDA call (pointers below are fake addresses that are never read)."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_gated_gb300 import build as b
+    b.build()
+    from linear_attention_gated_gb300 import kda
+    return kda.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(kda_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9, names
+    for name in names:
+        assert hasattr(lib, name), name
+    from linear_attention_gated_gb300 import kda
+    assert set(kda.EXPORTED) <= set(names)
+
+
+def test_status_strings(lib):
+    for st in range(8):
+        assert lib.kda_status_string(st)
+    assert lib.kda_last_error_message() == b""
+
+
+def test_tiling_constants(lib):
+    assert lib.kda_chunk_tokens() == 16
+    assert lib.kda_checkpoint_tokens() % lib.kda_chunk_tokens() == 0
+
+
+def ws_bytes(lib, B, T, hqk, hv, cu=None):
+    out = ctypes.c_size_t()
+    if cu is None:
+        rc = lib.kda_ctx_workspace_bytes(B, T, hqk, hv, None, 0, ctypes.byref(out))
+    else:
+        arr = (ctypes.c_int64 * len(cu))(*cu)
+        rc = lib.kda_ctx_workspace_bytes(B, T, hqk, hv, ctypes.cast(arr, ctypes.c_void_p),
+                                         len(cu) - 1, ctypes.byref(out))
+    return rc, out.value
+
+
+def test_workspace_bytes_grows_with_problem(lib):
+    rc, a = ws_bytes(lib, 1, 64, 2, 2)
+    assert rc == 0 and a > 0 and a % 256 == 0
+    rc, b = ws_bytes(lib, 2, 1024, 32, 32)
+    assert rc == 0 and b > a
+    # checkpoint storage: one 64 KiB state per (interval, head)
+    ck = lib.kda_checkpoint_tokens()
+    rc, c = ws_bytes(lib, 1, 8192, 96, 96, list(range(0, 8193, 1024)))
+    assert rc == 0 and c >= 8 * math.ceil(1024 / ck) * 96 * 65536
+    # GQA adds per-value-head scratch for the group sums
+    rc, d1 = ws_bytes(lib, 4, 2048, 32, 32)
+    rc, d2 = ws_bytes(lib, 4, 2048, 16, 32)
+    assert d2 > d1
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 64, 2, 2, None), 1),           # B = 0
+    ((1, 64, 3, 4, None), 1),           # Hv not a multiple of Hqk
+    ((2, 64, 2, 2, [0, 32, 64]), 1),    # packed with B != 1
+    ((1, 64, 2, 2, [0, 32, 32, 64]), 1),  # empty sequence
+    ((1, 64, 2, 2, [1, 32, 64]), 1),    # does not start at 0
+    ((1, 64, 2, 2, [0, 32, 60]), 1),    # does not end at T
+])
+def test_workspace_bytes_rejects(lib, args, status):
+    rc, _ = ws_bytes(lib, *args)
+    assert rc == status
+
+
+class FakeCall:
+    """kda_fwd with fake, well-separated, aligned device addresses."""
+
+    def __init__(self, lib, B=1, T=64, hqk=2, hv=2, cu=None):
+        self.lib = lib
+        self.B, self.T, self.hqk, self.hv, self.cu = B, T, hqk, hv, cu
+        base = 1 << 40
+        names = ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "h0", "cu_dev", "o", "hT", "ws"]
+        self.addr = {n: base + i * (1 << 34) for i, n in enumerate(names)}
+        rc, self.ws_bytes = ws_bytes(lib, B, T, hqk, hv, cu)
+        assert rc == 0
+
+    def __call__(self, head_dim=128, scale=float("nan"), lb=-5.0, ws_bytes=None, **override):
+        a = dict(self.addr)
+        a.update(override)
+        P = ctypes.c_void_p
+        cu_host = None
+        nseq = 0
+        if self.cu is not None:
+            self._cu_arr = (ctypes.c_int64 * len(self.cu))(*self.cu)
+            cu_host = ctypes.cast(self._cu_arr, P)
+            nseq = len(self.cu) - 1
+        else:
+            a["cu_dev"] = None
+        ctx = P(None)
+        rc = self.lib.kda_fwd(*[P(a[n]) if a[n] is not None else None for n in
+                                ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "h0"]],
+                              P(a["cu_dev"]) if a["cu_dev"] is not None else None, cu_host, nseq,
+                              self.B, self.T, self.hqk, self.hv, head_dim, scale, lb,
+                              P(a["o"]) if a["o"] else None, P(a["hT"]), P(a["ws"]),
+                              self.ws_bytes if ws_bytes is None else ws_bytes,
+                              ctypes.byref(ctx), None)
+        return rc, self.lib.kda_last_error_message().decode()
+
+
+def test_fwd_rejects_unsupported_head_dim(lib):
+    rc, msg = FakeCall(lib)(head_dim=64)
+    assert rc == 2 and "128" in msg
+
+
+def test_fwd_rejects_wrong_scale_and_lower_bound(lib):
+    call = FakeCall(lib)
+    assert call(scale=0.5)[0] == 2
+    assert call(lb=-4.0)[0] == 2
+
+
+def test_fwd_rejects_null_pointer(lib):
+    rc, msg = FakeCall(lib)(o=None)
+    assert rc == 1 and "NULL" in msg
+
+
+def test_fwd_rejects_small_workspace(lib):
+    call = FakeCall(lib)
+    assert call(ws_bytes=call.ws_bytes - 256)[0] == 7
+
+
+def test_fwd_rejects_unaligned_workspace_and_tensors(lib):
+    call = FakeCall(lib)
+    assert call(ws=call.addr["ws"] + 16)[0] == 1
+    assert call(q=call.addr["q"] + 2)[0] == 1
+
+
+def test_fwd_rejects_aliasing(lib):
+    call = FakeCall(lib)
+    rc, msg = call(o=call.addr["v"] + 1024)
+    assert rc == 3 and "o" in msg
+    rc, msg = call(hT=call.addr["ws"] + 4096)
+    assert rc == 3
+    rc, _ = call(ws=call.addr["h0"])
+    assert rc == 3
+
+
+def test_fwd_packed_rejects_missing_device_offsets(lib):
+    call = FakeCall(lib, cu=[0, 10, 64])
+    rc, msg = call(cu_dev=None)
+    assert rc == 1
+
+
+def test_fwd_reaches_device_check_when_arguments_are_valid(lib):
+    """With valid arguments the only remaining failure here (no GPU) is the device query."""
+    rc, msg = FakeCall(lib, cu=[0, 10, 64])()
+    assert rc in (2, 5), msg
+
+
+def test_bwd_rejects_null_context(lib):
+    P = ctypes.c_void_p
+    rc = lib.kda_bwd(None, *[P(1 << 40)] * 10, None)
+    assert rc == 1
+
+
+def test_ctx_destroy_accepts_null(lib):
+    lib.kda_ctx_destroy(None)
