@@ -231,6 +231,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="named workload of kda_inputs.WORKLOADS (default: the packed 8 x 1024, 96-head one)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -249,8 +251,8 @@ def main():
     load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = ki.WORKLOADS[WORKLOAD]
-    x = ki.workload_inputs(WORKLOAD)
+    w = ki.WORKLOADS[args.workload]
+    x = ki.workload_inputs(args.workload)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     cu_cpu = x["cu_seqlens"]
     N = cu_cpu.numel() - 1
@@ -304,7 +306,7 @@ def main():
     elapsed = max_over_ranks(elapsed, world, dev)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    value = job_value(token_heads, world, elapsed)
+    value = job_value(token_heads * args.steps, world, elapsed)
 
     ab = algorithmic_bytes(Ttot, w.hqk, w.hv, units)
     peaks = read_peaks()
@@ -327,7 +329,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sequences": N, "tokens": Ttot, "Hqk": w.hqk, "Hv": w.hv,
+            "config": {"workload": args.workload, "sequences": N, "tokens": Ttot, "Hqk": w.hqk, "Hv": w.hv,
                        "head_dim": DIM, "token_heads_per_gpu": token_heads, "io_dtype": "bf16",
                        "state_dtype": "fp32", "l2": "inputs larger than L2 (each token tensor "
                        f"{d['q'].numel() * 2 / 1e6:.0f} MB > 129 MB), no flush",

@@ -62,6 +62,8 @@ WORKLOADS = {
                                   lengths=(1024,) * 8),
     "packed_24mixed_hqk8_hv64": Workload("packed_24mixed_hqk8_hv64", 1, 0, 8, 64, 4, True,
                                          mixed_n=24, mixed_max=4000),
+    # half of the packed 8 x 1024 workload, for profiler captures (a few GB on the device)
+    "packed_4x1024_h96": Workload("packed_4x1024_h96", 1, 4096, 96, 96, 5, True, lengths=(1024,) * 4),
 }
 
 

@@ -2,7 +2,7 @@
 //
 // One CTA owns one (sequence, value head) unit. It walks the unit's sub-chunks
 // from last to first, carrying the state adjoint G = dL/dS (value-first,
-// 128x128 FP32, on chip) and a key-dim vector rho used for the decay gradient.
+// 128x128 FP32, on chip).
 // Per sub-chunk it reloads the chunk-start state S0 saved by the forward and
 // recomputes the chunk's WY quantities (never the whole forward):
 //   Y  = V - (k^ gamma) S0^T,     W = T diag(beta) Y,     U = Y - A W  (u_i)
@@ -16,9 +16,13 @@
 // The decay gradient uses the gauge identity of the per-key-dim decay: scaling
 // the decay of token t in key dim j by e^eps equals scaling, for every later
 // token, the query and the read key by e^eps and the written key by e^-eps, and
-// the final state's column j by e^eps. Hence
-//   da_t = sum_{s >= t} (q^ dq^ + k^ (dk^_read - dk^_write))_s + sum_v dS_T * S_T,
-// a reverse cumulative sum that needs no per-token elementwise state product.
+// the final state's column j by e^eps. Applied at the end of each sub-chunk,
+// where scaling column j of the state S_C has the direct effect
+// sum_v G[v,j] S_C[v,j], it gives for the tokens t of the sub-chunk
+//   da_t = sum_{s >= t in chunk} (q^ dq^ + k^ (dk^_read - dk^_write))_s + rho,
+//   rho  = gamma_C * sum_v (G * S0) + sum_i (k^ gamma_C/gamma)_i * (W G)_i,
+// so no per-token elementwise state product is needed and no sum runs across
+// sub-chunks (a running sum over the whole sequence drifts in FP32).
 // The gate, sigmoid and L2-norm backward are applied in the epilogue
 // (flashinfer.kda_backward.recurrent_kda_backward, description: gradients with
 // respect to the raw gate and raw beta logits, Q/K normalised with eps 1e-6).
@@ -52,7 +56,7 @@ struct BwdSmem {
   float bs[kChunk];
   float dba[kChunk]; // dbeta before the sigmoid derivative
   float gC[kDim];
-  float rho[kDim];
+  float rho[3][kDim]; // sum_v G*S0, and the two halves of sum_i Kb (W G)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -251,25 +255,11 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
     }
     __syncthreads();
-    // ---- last sub-chunk only: rho = sum_v dS_T * S_T with S_T = S0 diag(gC) + W^T Kb
-    if (c == nchunks - 1) {
-      const int kc = tid & 127, vh = tid >> 7;
-      float acc = 0.f;
-      for (int vv = vh * 64; vv < vh * 64 + 64; ++vv) {
-        float st = sm.S0[vv * kLds + kc] * sm.gC[kc];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) st += sm.Ws[i * kLds + vv] * sm.Kb[i * kLds + kc];
-        acc += sm.G[vv * kLds + kc] * st;
-      }
-      if (vh == 1) sm.rho[kc] = acc;
-      __syncthreads();
-      if (vh == 0) sm.rho[kc] += acc;
-      __syncthreads();
-    }
-    // ---- P5: reductions over v: dO S0, dV S0, W G; dO W^T, dV W^T; dbeta rows
+    // ---- P5: reductions over v: dO S0, dV S0, W G, sum G*S0; dO W^T, dV W^T; dbeta rows
     float accq[8], accr[8], accw[8];
     const int kc = tid & 127, i0 = (tid >> 7) * 8;
     {
+      float gs = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) { accq[i] = 0.f; accr[i] = 0.f; accw[i] = 0.f; }
 #pragma unroll 2
@@ -279,6 +269,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         for (int x = 0; x < 4; ++x) {
           s0[x] = sm.S0[(vv + x) * kLds + kc];
           g0[x] = sm.G[(vv + x) * kLds + kc];
+          gs += s0[x] * g0[x];
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -290,6 +281,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           accw[i] += w4.x * g0[0] + w4.y * g0[1] + w4.z * g0[2] + w4.w * g0[3];
         }
       }
+      if (tid < kDim) sm.rho[0][kc] = gs;
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
         const int e = tid + rep * kThreads;
@@ -319,9 +311,11 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       float* dKh = sm.S0 + kTile;
       float* tv = sm.S0 + 2 * kTile;
       const float gck = sm.gC[kc];
+      float rp = 0.f;
 #pragma unroll
       for (int ii = 0; ii < 8; ++ii) {
         const int i = i0 + ii;
+        rp += sm.Kb[i * kLds + kc] * accw[ii];
         const float gam = sm.Gm[i * kLds + kc];
         const float inv = 1.0f / gam;
         float pq = accq[ii], pr = accr[ii], pw = gck * accw[ii];
@@ -342,6 +336,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         dKh[i * kLds + kc] = dkr + dkw;
         tv[i * kLds + kc] = qh_ * dq_ + kh_ * (dkr - dkw);
       }
+      sm.rho[1 + (tid >> 7)][kc] = rp;
       // G <- G diag(gC) + (scale dO)^T Qt - dV^T Kt
       const int gv = tid >> 1, half = tid & 1;
 #pragma unroll 4
@@ -365,16 +360,15 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
     }
     __syncthreads();
-    // ---- P7: da = rho + reverse cumulative sum of the gauge term
+    // ---- P7: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
     if (tid < kDim) {
       float* tv = sm.S0 + 2 * kTile;
-      float run = sm.rho[tid];
+      float run = sm.gC[tid] * sm.rho[0][tid] + sm.rho[1][tid] + sm.rho[2][tid];
 #pragma unroll
       for (int i = kChunk - 1; i >= 0; --i) {
         run += tv[i * kLds + tid];
         tv[i * kLds + tid] = run;
       }
-      sm.rho[tid] = run;
     }
     __syncthreads();
     // ---- P8: epilogue: gate / sigmoid / L2-norm backward and stores
@@ -388,8 +382,10 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       float pq = 0.f, pk = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
+        // sigmoid'(z) = sigmoid(z) sigmoid(-z), both evaluated directly (no 1 - s cancellation)
         const float sg = 1.0f / (1.0f + expf(-zz[e]));
-        const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * sg * (1.0f - sg) : 0.f;
+        const float sn = 1.0f / (1.0f + expf(zz[e]));
+        const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * sg * sn : 0.f;
         dg8[e] = dz * ea;
         ddt_acc[e] += dg8[e];
         dA_acc += dz * zz[e];
@@ -423,8 +419,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         }
       }
       if (tid < nt) {
-        const float b = sm.bs[tid];
-        a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * b * (1.0f - b));
+        const float bl = __bfloat162float(P.beta[(tc0 + tid) * P.Hv + h]);
+        const float bn = 1.0f / (1.0f + expf(bl));  // sigmoid(-logit)
+        a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
       }
     }
     __syncthreads();
