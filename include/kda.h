@@ -139,6 +139,45 @@ const char* kda_status_string(kda_status status);
 /* Message of the last failed call on this thread ("" if none). */
 const char* kda_last_error_message(void);
 
+/*
+ * Standalone backward that allocates nothing. The documentation pages have no
+ * counterpart for this entry point; it exists for callers that cannot call
+ * cudaMalloc: code running while another component owns all device memory
+ * through its own pool (a framework caching allocator, a server that carves
+ * the GPU up front), hosts that forbid allocation inside a plug-in call, and
+ * loops that cannot afford the device-wide synchronisation cudaMalloc/cudaFree
+ * may imply. Such callers own their inputs and outputs but cannot provide the
+ * context workspace kda_fwd/kda_bwd need.
+ *
+ * Inputs and outputs are those of kda_fwd (inputs, same layouts and rules) plus
+ * those of kda_bwd (d_o, d_hT and the eight gradients); the function recomputes
+ * the forward's checkpoints itself and returns the same eight gradients.
+ * Scratch: one fixed array of KDA_NOALLOC_SCRATCH_BYTES compiled into the
+ * library (a static __device__ array), resident on every GPU where the library's
+ * module is loaded until the process exits. A problem whose checkpoints and
+ * intermediates exceed it is rejected with KDA_ERR_WORKSPACE_TOO_SMALL (use
+ * kda_fwd + kda_bwd for it). With a checkpoint every kda_checkpoint_tokens()
+ * = 16 tokens about 4.3 KiB per token-head (5.3 KiB when Hv > Hqk) plus 65 KiB
+ * per (sequence, head) are needed: e.g. 1024 tokens x 12 heads with Hv = Hqk fit.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture. Every call shares the one array and leaves its contents
+ * behind; nothing in it needs to start at zero. Calls whose work overlaps on the
+ * GPU (different streams, or several host threads) race on the array: serialise
+ * them. Units run in index order. Nothing is allocated: no cudaMalloc, cudaFree
+ * or allocating library routine is called.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                           const kda_bf16* g, const kda_bf16* beta, const float* A_log,
+                           const float* dt_bias, const float* h0, const int64_t* cu_seqlens_dev,
+                           const int64_t* cu_seqlens_host, int64_t num_seqs, int64_t B, int64_t T,
+                           int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
+                           float lower_bound, const kda_bf16* d_o, const float* d_hT,
+                           kda_bf16* dq, kda_bf16* dk, kda_bf16* dv, kda_bf16* dg,
+                           kda_bf16* dbeta, float* dA_log, float* ddt_bias, float* dh0,
+                           struct CUstream_st* stream);
+
 /* Internal tiling, for tooling and tests: sub-chunk length in tokens and the
  * checkpoint interval in tokens. */
 int32_t kda_chunk_tokens(void);

@@ -10,6 +10,7 @@ from .kda import (  # noqa: F401
     KdaContext,
     KdaError,
     kda_bwd,
+    kda_bwd_noalloc,
     kda_fwd,
     load_library,
     recurrent_kda_training_backward,

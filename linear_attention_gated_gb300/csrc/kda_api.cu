@@ -148,6 +148,8 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
+void kda::set_last_error(const char* msg) { g_last_error = msg; }
+
 struct kda_ctx {
   Shape shape;
   Layout layout;

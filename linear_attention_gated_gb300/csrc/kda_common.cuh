@@ -93,6 +93,9 @@ __device__ __forceinline__ float row16_sum(float x) {
   return x;
 }
 
+// Sets the message kda_last_error_message() returns on this thread (kda_api.cu).
+void set_last_error(const char* msg);
+
 // Launchers (defined in kda_fwd.cu / kda_bwd.cu).
 cudaError_t launch_forward(const Problem& P, const FwdOut& out, int64_t units, cudaStream_t s);
 cudaError_t launch_backward(const Problem& P, const BwdArgs& a, int64_t units, int64_t Ttot,

@@ -30,7 +30,7 @@ _STATUS = {
 
 EXPORTED = ("kda_ctx_workspace_bytes", "kda_fwd", "kda_bwd", "kda_ctx_status", "kda_ctx_destroy",
             "kda_status_string", "kda_last_error_message", "kda_chunk_tokens",
-            "kda_checkpoint_tokens")
+            "kda_checkpoint_tokens", "kda_bwd_noalloc")
 
 
 class KdaError(RuntimeError):
@@ -67,6 +67,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_last_error_message.argtypes = []
     lib.kda_last_error_message.restype = ctypes.c_char_p
+    lib.kda_bwd_noalloc.argtypes = [P] * 8 + [P, P, I, I, I, I, I, I, F, F] + [P] * 10 + [P]
+    lib.kda_bwd_noalloc.restype = ctypes.c_int
     lib.kda_chunk_tokens.argtypes = []
     lib.kda_chunk_tokens.restype = ctypes.c_int32
     lib.kda_checkpoint_tokens.argtypes = []
@@ -237,6 +239,38 @@ def kda_bwd(ctx: KdaContext, do, dfinal_state, out=None):
     stream = torch.cuda.current_stream(dev)
     rc = lib.kda_bwd(ctx.handle, _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out],
                      ctypes.c_void_p(stream.cuda_stream))
+    _check(rc)
+    return tuple(out)
+
+
+def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_state,
+                    cu_seqlens=None, scale=None, lower_bound=-5.0, out=None, *, cu_seqlens_cpu=None):
+    """Standalone backward that allocates no device memory in the library (for
+    callers that cannot call cudaMalloc; scratch is a fixed array compiled into
+    libkda.so). Returns the eight gradients of kda_bwd. ``out`` (eight tensors in
+    return order) lets the caller own every output buffer as well."""
+    lib = load_library()
+    B, T, Hqk, D = q.shape
+    Hv = v.shape[2]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None and cu_seqlens_cpu is None:
+        raise ValueError("packed input requires cu_seqlens_cpu, a trusted CPU mirror of cu_seqlens")
+    dev = q.device
+    shapes = ((B, T, Hqk, D), (B, T, Hqk, D), (B, T, Hv, D), (B, T, Hv, D), (B, T, Hv), (Hv,), (Hv, D),
+              (N, Hv, D, D))
+    dtypes = (torch.bfloat16,) * 5 + (torch.float32,) * 3
+    if out is None:
+        out = tuple(torch.empty(s_, dtype=dt, device=dev) for s_, dt in zip(shapes, dtypes))
+    for t, name, s_, dt in zip(out, GRAD_NAMES, shapes, dtypes):
+        _want(t, name, dt, s_)
+    stream = torch.cuda.current_stream(dev)
+    rc = lib.kda_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                             _ptr(initial_state), _ptr(cu_seqlens),
+                             _ptr(cu_seqlens_cpu) if cu_seqlens_cpu is not None else None,
+                             N if cu_seqlens is not None else 0, B, T, Hqk, Hv, D,
+                             float("nan") if scale is None else float(scale), float(lower_bound),
+                             _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out],
+                             ctypes.c_void_p(stream.cuda_stream))
     _check(rc)
     return tuple(out)
 
