@@ -47,7 +47,7 @@ struct Shape {
 };
 
 struct Layout {
-  size_t order = 0, seq = 0, ckpt = 0, dqk = 0, par = 0, status = 0, total = 0;
+  size_t order = 0, seq = 0, ckpt = 0, utape = 0, dqk = 0, par = 0, status = 0, total = 0;
 };
 
 Layout make_layout(const Shape& s) {
@@ -56,6 +56,7 @@ Layout make_layout(const Shape& s) {
   L.order = off; off = align_up(off + sizeof(int32_t) * s.units);
   L.seq = off;   off = align_up(off + sizeof(SeqInfo) * s.N);
   L.ckpt = off;  off = align_up(off + sizeof(float) * (size_t)s.n_ck * s.Hv * kda::kDim * kda::kDim);
+  L.utape = off; off = align_up(off + sizeof(float) * (size_t)s.Ttot * s.Hv * kda::kDim);
   L.dqk = off;
   if (s.Hv != s.Hqk) off = align_up(off + sizeof(float) * (size_t)s.Ttot * s.Hv * 2 * kda::kDim);
   L.par = off;   off = align_up(off + sizeof(float) * (size_t)s.units * kda::kParStride);
@@ -299,6 +300,8 @@ kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, cons
   P.order = reinterpret_cast<const int32_t*>(c->ws + L.order);
   P.seq = reinterpret_cast<const SeqInfo*>(c->ws + L.seq);
   P.ckpt = reinterpret_cast<float*>(c->ws + L.ckpt);
+  P.status = reinterpret_cast<int32_t*>(c->ws + L.status);
+  P.utape = reinterpret_cast<float*>(c->ws + L.utape);
   P.N = s.N;
   P.Hqk = Hqk;
   P.Hv = Hv;

@@ -1,70 +1,100 @@
-// kda_bwd.cu -- reverse-time chunked backward of the recurrent KDA recurrence.
+// kda_bwd.cu -- reverse-time chunked backward of the recurrent KDA recurrence
+// on sm_103a tensor cores.
 //
 // One CTA owns one (sequence, value head) unit. It walks the unit's sub-chunks
-// from last to first, carrying the state adjoint G = dL/dS (value-first,
-// 128x128 FP32, on chip).
-// Per sub-chunk it reloads the chunk-start state S0 saved by the forward and
-// recomputes the chunk's WY quantities (never the whole forward):
-//   Y  = V - (k^ gamma) S0^T,     W = T diag(beta) Y,     U = Y - A W  (u_i)
-//   dW = (k^ gamma_C/gamma) G^T + scale B^T dO,   E = T^T dW,   dV = diag(beta) E
+// from last to first, carrying the state adjoint G = dL/dS as an FP32
+// accumulator in tensor memory, stored transposed (lane = key dim k, column =
+// value dim v). Per sub-chunk it reads the chunk-start state S0 saved by the
+// forward and the forward's per-token u = v - S' k^ (so W = diag(beta) U is
+// never recomputed), and with Gd = G diag(gamma_C) (the adjoint moved to the
+// decayed end state):
+//   dW = (k^/gamma) Gd^T + scale B^T dO,   E = T^T dW,   dV = diag(beta) E
 //   dbeta_i = E_i . U_i  (before the sigmoid derivative)
 //   dq^ = scale gamma * (dO S0 + tril(dO W^T) (k^/gamma))
-//   dk^ = -gamma * (dV S0 + stril(dV W^T) (k^/gamma))                 (read key)
-//       + (1/gamma) * (gamma_C * (W G) + triu(scale W dO^T) (q^ gamma)
-//                      - striu(W dV^T) (k^ gamma))                     (write key)
-//   G  <- G diag(gamma_C) + (scale dO)^T (q^ gamma) - dV^T (k^ gamma)
-// The decay gradient uses the gauge identity of the per-key-dim decay: scaling
-// the decay of token t in key dim j by e^eps equals scaling, for every later
-// token, the query and the read key by e^eps and the written key by e^-eps, and
-// the final state's column j by e^eps. Applied at the end of each sub-chunk,
-// where scaling column j of the state S_C has the direct effect
-// sum_v G[v,j] S_C[v,j], it gives for the tokens t of the sub-chunk
+//   dk^ = -gamma * (dV S0 + stril(dV W^T) (k^/gamma))                  (read key)
+//       + (1/gamma) * (W Gd + triu(scale W dO^T) (q^ gamma)
+//                      - striu(W dV^T) (k^ gamma))                      (write key)
+//   G  <- Gd + (scale dO)^T (q^ gamma) - dV^T (k^ gamma)
+// with T = (I + diag(beta) A)^-1 applied by substitution. The decay gradient
+// uses the gauge identity of the per-key-dim decay: scaling the decay of token
+// t in key dim j by e^eps equals scaling, for every later token, the query and
+// the read key by e^eps and the written key by e^-eps, and the final state's
+// column j by e^eps. Applied at the end of each sub-chunk, where scaling column
+// j of the state S_C has the direct effect sum_v G[v,j] S_C[v,j], it gives for
+// the tokens t of the sub-chunk
 //   da_t = sum_{s >= t in chunk} (q^ dq^ + k^ (dk^_read - dk^_write))_s + rho,
-//   rho  = gamma_C * sum_v (G * S0) + sum_i (k^ gamma_C/gamma)_i * (W G)_i,
+//   rho  = sum_v (Gd * S0) + sum_i (k^/gamma)_i * (W Gd)_i,
 // so no per-token elementwise state product is needed and no sum runs across
 // sub-chunks (a running sum over the whole sequence drifts in FP32).
-// The gate, sigmoid and L2-norm backward are applied in the epilogue
-// (flashinfer.kda_backward.recurrent_kda_backward, description: gradients with
-// respect to the raw gate and raw beta logits, Q/K normalised with eps 1e-6).
+//
+// Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
+// state-sized contractions: [k^g; q^g] (k^/g)^T (A and B), S0^T [dO; dV]^T,
+// Gd (k^/g)^T, Gd^T W^T (W split into TF32 hi + lo) and the rank-32 adjoint
+// update (dV split into hi + lo; dO is exact in TF32). The 16x16 intra-chunk
+// products, the substitutions and the combination run in FP32 on CUDA cores:
+// the decay gradient is a difference of nearly equal terms and needs them at
+// full single precision. The gate, sigmoid and L2-norm backward are applied in
+// the epilogue (flashinfer.kda_backward.recurrent_kda_backward, description:
+// gradients with respect to the raw gate and raw beta logits, Q/K normalised
+// with eps 1e-6).
 #include "kda_common.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTile = kChunk * kLds;
-constexpr int kSq = kChunk * (kChunk + 1);
-constexpr int kState = kDim * kLds;
+constexpr int kTileF = kChunk * kLds;
+constexpr int kSq = kChunk + 1;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColG = 0;     // G^T, FP32 accumulator (lanes k, columns v)
+constexpr uint32_t kColGr = 128;  // Gd^T rounded to TF32 (A operand of Gd^T W^T)
+constexpr uint32_t kColS = 256;   // S0^T rounded to TF32 (A operand of S0^T [dO; dV]^T)
+constexpr uint32_t kColDW = 384;  // Gd (k^/g)^T : lanes v, 16 columns
+constexpr uint32_t kColAB = 400;  // [k^g; q^g] (k^/g)^T : lanes 0..31, 16 columns
+constexpr uint32_t kColQ = 416;   // S0^T dO^T : lanes k, 16 columns
+constexpr uint32_t kColR = 432;   // S0^T dV^T : lanes k, 16 columns
+constexpr uint32_t kColWG = 448;  // Gd^T W^T  : lanes k, 16 columns
 
 struct BwdSmem {
-  float S0[kState];  // chunk-start state; later reused for dq^, dk^, da tiles
-  float G[kState];   // adjoint of the state at the end of the current sub-chunk
-  float Qt[kTile];   // q^ gamma
-  float Kt[kTile];   // k^ gamma
-  float Ki[kTile];   // k^ / gamma
-  float Kb[kTile];   // k^ gamma_C / gamma
-  float Gm[kTile];   // gamma
-  float Vs[kTile];   // v, then Y, then E*U
-  float Ws[kTile];   // W
-  float dO[kTile];   // do
-  float DU[kTile];   // dW (k-part), then dV = beta E
-  float Am[kSq];
-  float Bm[kSq];
-  float Tm[kSq];
-  float M1[kSq];     // dO W^T
-  float M2[kSq];     // dV W^T
+  // KQ must directly precede Gdv: the A operand of the A/B product is 128 rows
+  // starting at KQ (rows 32..127 read Gdv and are unused).
+  unsigned char KQ[32 * kDim * 4];        // rows 0..15 k^ gamma, 16..31 q^ gamma (K-major, K = 128)
+  unsigned char Gdv[kDim * kDim * 4];     // Gd rows v, TF32                     (K-major, K = 128)
+  unsigned char Ki[kChunk * kDim * 4];    // k^ / gamma rows t                  (K-major, K = 128)
+  // Wt and dOU are contiguous: after the second MMA group they hold the
+  // combination tiles (d q^, d k^, gauge term).
+  unsigned char Wt[2][kChunk * kDim * 4]; // W rows t, TF32 hi / lo              (K-major, K = 128)
+  unsigned char dOU[32 * kDim * 4];       // rows 0..15 dO, 16..31 dV           (K-major, K = 128)
+  unsigned char dOUv[kDim * 32 * 4];      // rows v: cols 0..15 dO, 16..31 dV (hi) (K-major, K = 32)
+  unsigned char dUlo[kDim * kChunk * 4];  // rows v: dV lo part                 (K-major, K = 16)
+  unsigned char QKT[kDim * 32 * 4];       // rows k: cols 0..15 scale q^g, 16..31 -k^g (K-major, K = 32)
+  float Pa[kTileF];                       // log decay, then gamma
+  float Qtp[kTileF];                      // q^ gamma (FP32)
+  float Ktp[kTileF];                      // k^ gamma (FP32)
+  float Kip[kTileF];                      // k^ / gamma (FP32)
+  float Up[kTileF];                       // u from the forward
+  float DUp[kTileF];                      // dV
+  __nv_bfloat16 dOp[kChunk * kDim];       // do
+  float As[kChunk][kSq];
+  float Bs[kChunk][kSq];
+  float M1[kChunk][kSq];                  // dO W^T
+  float M2[kChunk][kSq];                  // dV W^T
   float bs[kChunk];
-  float dba[kChunk]; // dbeta before the sigmoid derivative
+  float dba[kChunk];
   float gC[kDim];
-  float rho[3][kDim]; // sum_v G*S0, and the two halves of sum_i Kb (W G)
+  float rho0[2][kDim];                    // halves of sum_v Gd * S0
+  float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
+  float dbp[4][kChunk];                   // per-warp partial dbeta
+  unsigned long long mbar;
+  uint32_t tmem_base;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 kda_bwd_kernel(const Problem P, const BwdArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = P.order[blockIdx.x];
   const int64_t n = unit / P.Hv;
   const int64_t h = unit % P.Hv;
@@ -72,15 +102,35 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   const SeqInfo si = P.seq[n];
   const float s = P.scale;
 
-  // G <- dfinal_state
+  const int kl = 32 * (warp & 3) + lane;  // TMEM lane of this thread (key dim k, or value dim v)
+  const int hv = warp >> 2;               // column half handled by this thread
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
+  if (tid == 0) tc::mbar_init(tc::smem_u32(&sm.mbar), 1);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = sm.tmem_base;
+  const uint32_t tl = tbase + lane_off;
+  const uint32_t mbar = tc::smem_u32(&sm.mbar);
+  uint32_t parity = 0;
+  bool ok = true;
+  bool aborted = false;
+
+  // G^T <- dfinal_state^T
   {
     const float* src = a.d_hT + (n * P.Hv + h) * kDim * kDim;
-    for (int f = tid; f < kDim * kDim / 4; f += kThreads) {
-      const int row = f >> 5, c4 = (f & 31) * 4;
-      *reinterpret_cast<float4*>(sm.G + row * kLds + c4) =
-          *reinterpret_cast<const float4*>(src + row * kDim + c4);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int v0 = 64 * hv + 16 * q;
+      float x[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[j] = src[(v0 + j) * kDim + kl];
+      tc::tmem_st16(tl + kColG + v0, x);
     }
+    tc::tmem_wait_st();
   }
+
   const int ti = tid >> 4;
   const int c8 = (tid & 15) * 8;
   const float ea = expf(P.A_log[h]);
@@ -91,35 +141,42 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) ddt_acc[e] = 0.f;
   float dA_acc = 0.f;
+  float* cmb = reinterpret_cast<float*>(sm.Wt[0]);  // d q^, d k^, gauge / da tiles (after the MMAs)
 
   const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
   const int ck_every = kCkTokens / kChunk;
   for (int64_t c = nchunks - 1; c >= 0; --c) {
     const int64_t tc0 = si.t0 + c * kChunk;
     const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
-    // ---- P0: chunk-start state, token tiles and prologue
+    // ---- P0: token tiles and prologue (token row ti, columns c8..c8+7)
+    float qhat[8], khat[8], zz[8], uu[8], rq, rk;
     {
-      const float* src = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
-      for (int f = tid; f < kDim * kDim / 4; f += kThreads) {
-        const int row = f >> 5, c4 = (f & 31) * 4;
-        *reinterpret_cast<float4*>(sm.S0 + row * kLds + c4) =
-            *reinterpret_cast<const float4*>(src + row * kDim + c4);
-      }
-    }
-    float qhat[8], khat[8], zz[8], rq, rk;
-    {
-      float qv[8], kv[8], gv[8], vv[8], dv8[8];
+      float qv[8], kv[8], gv[8];
+      uint4 draw = make_uint4(0u, 0u, 0u, 0u);
       const bool valid = ti < nt;
       const int64_t t = tc0 + ti;
       if (valid) {
         load_bf16x8(P.q + (t * P.Hqk + qh) * kDim + c8, qv);
         load_bf16x8(P.k + (t * P.Hqk + qh) * kDim + c8, kv);
         load_bf16x8(P.g + (t * P.Hv + h) * kDim + c8, gv);
-        load_bf16x8(P.v + (t * P.Hv + h) * kDim + c8, vv);
-        load_bf16x8(a.d_o + (t * P.Hv + h) * kDim + c8, dv8);
+        draw = *reinterpret_cast<const uint4*>(a.d_o + (t * P.Hv + h) * kDim + c8);
+        const float4 u0 = *reinterpret_cast<const float4*>(P.utape + (t * P.Hv + h) * kDim + c8);
+        const float4 u1 = *reinterpret_cast<const float4*>(P.utape + (t * P.Hv + h) * kDim + c8 + 4);
+        uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
+        uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] = kv[e] = gv[e] = vv[e] = dv8[e] = 0.f;
+        for (int e = 0; e < 8; ++e) qv[e] = kv[e] = gv[e] = uu[e] = 0.f;
+      }
+      float dv8[8];
+      {
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&draw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          dv8[2 * e] = f.x;
+          dv8[2 * e + 1] = f.y;
+        }
       }
       float sq = 0.f, sk = 0.f;
 #pragma unroll
@@ -133,237 +190,261 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         qhat[e] = qv[e] * rq;
         khat[e] = kv[e] * rk;
         zz[e] = ea * (gv[e] + dtb[e]);
-        const float la = valid ? P.lb / (1.0f + expf(-zz[e])) : 0.f;
-        sm.Qt[ti * kLds + c8 + e] = qhat[e];
-        sm.Kt[ti * kLds + c8 + e] = khat[e];
-        sm.Ki[ti * kLds + c8 + e] = la;
-        sm.Vs[ti * kLds + c8 + e] = vv[e];
-        sm.dO[ti * kLds + c8 + e] = dv8[e];
+        sm.Pa[ti * kLds + c8 + e] = valid ? P.lb / (1.0f + expf(-zz[e])) : 0.f;
+        sm.Up[ti * kLds + c8 + e] = uu[e];
+        // dO is exact in TF32: it goes straight into both operand layouts
+        *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(c8 + e, ti, 32)) = dv8[e];
       }
+      *reinterpret_cast<uint4*>(sm.dOp + ti * kDim + c8) = draw;
+      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ti, c8, kDim)) = make_float4(dv8[0], dv8[1], dv8[2], dv8[3]);
+      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ti, c8 + 4, kDim)) = make_float4(dv8[4], dv8[5], dv8[6], dv8[7]);
       if (tid < kChunk)
-        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-__bfloat162float(P.beta[(tc0 + tid) * P.Hv + h])))
-                                : 0.f;
+        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-__bfloat162float(P.beta[(tc0 + tid) * P.Hv + h]))) : 0.f;
     }
     __syncthreads();
     // ---- P1: cumulative decay (one key column per thread)
     if (tid < kDim) {
-      const int kc = tid;
-      float Gc = 0.f;
+      float G = 0.f;
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        Gc += sm.Ki[i * kLds + kc];
-        sm.Ki[i * kLds + kc] = Gc;
+        G += sm.Pa[i * kLds + tid];
+        sm.Pa[i * kLds + tid] = expf(G);
       }
-      const float GC = Gc;
-      sm.gC[kc] = expf(GC);
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const float Gi = sm.Ki[i * kLds + kc];
-        const float kh = sm.Kt[i * kLds + kc];
-        const float gam = expf(Gi);
-        sm.Gm[i * kLds + kc] = gam;
-        sm.Qt[i * kLds + kc] *= gam;
-        sm.Kt[i * kLds + kc] = kh * gam;
-        sm.Ki[i * kLds + kc] = kh * expf(-Gi);
-        sm.Kb[i * kLds + kc] = kh * expf(GC - Gi);
-      }
+      sm.gC[tid] = expf(G);
     }
     __syncthreads();
-    // ---- P2: A, B; Y = V - Kt S0^T and dWk = Kb G^T (reductions over k)
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int e = tid + rep * kThreads;
-      const int mat = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const float* X = mat ? sm.Qt : sm.Kt;
-      float acc = 0.f;
-      if (j < i || (mat && j == i)) {
-#pragma unroll 8
-        for (int kk = 0; kk < kDim; kk += 4)
-          acc += dot4(*reinterpret_cast<const float4*>(X + i * kLds + kk),
-                      *reinterpret_cast<const float4*>(sm.Ki + j * kLds + kk));
-      }
-      (mat ? sm.Bm : sm.Am)[i * (kChunk + 1) + j] = acc;
-    }
+    // ---- P2a: operand tiles from q^, k^, gamma, u
     {
-      const int vv = tid & 127, i0 = (tid >> 7) * 8;
-      float y[8], dw[8];
+      const float bt = sm.bs[ti];
+      float kt[8], qt[8], ki[8], w[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { y[i] = 0.f; dw[i] = 0.f; }
-#pragma unroll 4
-      for (int kk = 0; kk < kDim; kk += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sm.S0 + vv * kLds + kk);
-        const float4 g4 = *reinterpret_cast<const float4*>(sm.G + vv * kLds + kk);
+      for (int e = 0; e < 8; ++e) {
+        const float gam = sm.Pa[ti * kLds + c8 + e];
+        kt[e] = khat[e] * gam;
+        qt[e] = qhat[e] * gam;
+        ki[e] = khat[e] / gam;
+        w[e] = bt * uu[e];
+        sm.Ktp[ti * kLds + c8 + e] = kt[e];
+        sm.Qtp[ti * kLds + c8 + e] = qt[e];
+        sm.Kip[ti * kLds + c8 + e] = ki[e];
+        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(c8 + e, ti, 32)) = tc::round_tf32(s * qt[e]);
+        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(c8 + e, 16 + ti, 32)) = tc::round_tf32(-kt[e]);
+      }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          y[i] += dot4(*reinterpret_cast<const float4*>(sm.Kt + (i0 + i) * kLds + kk), s4);
-          dw[i] += dot4(*reinterpret_cast<const float4*>(sm.Kb + (i0 + i) * kLds + kk), g4);
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int o = 4 * hlf;
+        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(ti, c8 + o, kDim)) =
+            make_float4(tc::round_tf32(kt[o]), tc::round_tf32(kt[o + 1]), tc::round_tf32(kt[o + 2]),
+                        tc::round_tf32(kt[o + 3]));
+        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(16 + ti, c8 + o, kDim)) =
+            make_float4(tc::round_tf32(qt[o]), tc::round_tf32(qt[o + 1]), tc::round_tf32(qt[o + 2]),
+                        tc::round_tf32(qt[o + 3]));
+        *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ti, c8 + o, kDim)) =
+            make_float4(tc::round_tf32(ki[o]), tc::round_tf32(ki[o + 1]), tc::round_tf32(ki[o + 2]),
+                        tc::round_tf32(ki[o + 3]));
+        float whi[4], wlo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          whi[e] = tc::round_tf32(w[o + e]);
+          wlo[e] = tc::round_tf32(w[o + e] - whi[e]);
+        }
+        *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ti, c8 + o, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
+        *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ti, c8 + o, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
+      }
+    }
+    // ---- P2b: decay the adjoint (Gd = G diag(gamma_C)); S0 and Gd as TF32 operands
+    {
+      const float gck = sm.gC[kl];
+      const float* s0 = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
+      float racc = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int v0 = 64 * hv + 16 * q;
+        float g16[16], sv16[16], r16[16];
+        tc::tmem_ld16(tl + kColG + v0, g16);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          sv16[j] = s0[(v0 + j) * kDim + kl];  // S0[v][k], coalesced over k
+          g16[j] *= gck;
+          racc = fmaf(g16[j], sv16[j], racc);
+        }
+        tc::tmem_st16(tl + kColG + v0, g16);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r16[j] = tc::round_tf32(g16[j]);
+        tc::tmem_st16(tl + kColGr + v0, r16);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sv16[j] = tc::round_tf32(sv16[j]);
+        tc::tmem_st16(tl + kColS + v0, sv16);
+        // Gd rows v for the A operand of Gd (k^/g)^T: transpose 4x4 blocks across lane quads
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float x[4] = {r16[4 * b], r16[4 * b + 1], r16[4 * b + 2], r16[4 * b + 3]};
+          tc::quad_transpose(x, lane);
+          *reinterpret_cast<float4*>(sm.Gdv + tc::kmaj(v0 + 4 * b + (lane & 3), kl & ~3, kDim)) =
+              make_float4(x[0], x[1], x[2], x[3]);
         }
       }
+      sm.rho0[hv][kl] = racc;
+      tc::tmem_wait_st();
+    }
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    // ---- MMA group 1: A/B, S0^T dO^T, Gd (k^/g)^T, Gd^T W^T
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t kq = tc::smem_u32(sm.KQ), ki = tc::smem_u32(sm.Ki), gdv = tc::smem_u32(sm.Gdv);
+      const uint32_t dou = tc::smem_u32(sm.dOU);
+      const uint32_t wt0 = tc::smem_u32(sm.Wt[0]), wt1 = tc::smem_u32(sm.Wt[1]);
+      const uint32_t i16 = tc::idesc_tf32(128, 16);
+#pragma unroll 1
+      for (int st = 0; st < kDim / 8; ++st) {
+        tc::mma_ss(tbase + kColAB, tc::kdesc(kq, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
+        tc::mma_ts(tbase + kColQ, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
+        tc::mma_ss(tbase + kColDW, tc::kdesc(gdv, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
+        tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt0, st, kDim), i16, st > 0);
+        tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt1, st, kDim), i16, 1);
+      }
+      tc::mma_commit(mbar);
+    }
+    ok = ok && tc::mbar_wait(mbar, parity);
+    parity ^= 1;
+    tc::fence_after();
+    float dwk[16];
+    if (warp < 4) tc::tmem_ld16(tl + kColDW, dwk);
+    if (warp == 0) {
+      float r[16];
+      tc::tmem_ld16(tl + kColAB, r);
+      if (lane < 16) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        sm.Vs[(i0 + i) * kLds + vv] -= y[i];
-        sm.DU[(i0 + i) * kLds + vv] = dw[i];
+        for (int j = 0; j < kChunk; ++j) sm.As[lane][j] = (j < lane) ? r[j] : 0.f;
+      } else {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) sm.Bs[lane - 16][j] = (j <= lane - 16) ? r[j] : 0.f;
       }
     }
-    __syncthreads();
-    // ---- P3: T = (I + diag(beta) A)^-1
-    if (tid < kChunk) {
-      const int j = tid;
-      float tc[kChunk];
+    tc::fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials; warps 4-7: dO W^T
+    if (warp < 4) {
+      const int vv = kl;
+      float dw[kChunk], e[kChunk];
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        float acc = 0.f;
+        float acc = dwk[i];
 #pragma unroll
-        for (int m = 0; m < i; ++m)
-          if (m >= j) acc += sm.Am[i * (kChunk + 1) + m] * tc[m];
-        tc[i] = (i < j) ? 0.f : (i == j ? 1.f : -sm.bs[i] * acc);
-        sm.Tm[i * (kChunk + 1) + j] = tc[i];
-      }
-    }
-    __syncthreads();
-    // ---- P4: per value column: W, U, dW, E, dV, E*U
-    if (tid < kDim) {
-      const int vv = tid;
-      float y[kChunk], w[kChunk], dw[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) y[i] = sm.Vs[i * kLds + vv];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j <= i; ++j) acc += sm.Tm[i * (kChunk + 1) + j] * sm.bs[j] * y[j];
-        w[i] = acc;
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        float acc = sm.DU[i * kLds + vv];
-#pragma unroll
-        for (int j = i; j < kChunk; ++j) acc += s * sm.Bm[j * (kChunk + 1) + i] * sm.dO[j * kLds + vv];
+        for (int j = i; j < kChunk; ++j) acc += s * sm.Bs[j][i] * __bfloat162float(sm.dOp[j * kDim + vv]);
         dw[i] = acc;
       }
 #pragma unroll
+      for (int i = kChunk - 1; i >= 0; --i) {
+        float acc = dw[i];
+#pragma unroll
+        for (int j = i + 1; j < kChunk; ++j) acc -= sm.As[j][i] * sm.bs[j] * e[j];
+        e[i] = acc;
+      }
+#pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        float e = 0.f;
+        const float du = sm.bs[i] * e[i];
+        if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(du);
+        sm.DUp[i * kLds + vv] = du;
+        const float dhi = tc::round_tf32(du);
+        *reinterpret_cast<float*>(sm.dOU + tc::kmaj(16 + i, vv, kDim)) = dhi;
+        *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(vv, 16 + i, 32)) = dhi;
+        *reinterpret_cast<float*>(sm.dUlo + tc::kmaj(vv, i, kChunk)) = tc::round_tf32(du - dhi);
+        float pb = e[i] * sm.Up[i * kLds + vv];
 #pragma unroll
-        for (int j = i; j < kChunk; ++j) e += sm.Tm[j * (kChunk + 1) + i] * dw[j];
-        float u = y[i];
-#pragma unroll
-        for (int j = 0; j < i; ++j) u -= sm.Am[i * (kChunk + 1) + j] * w[j];
-        sm.Ws[i * kLds + vv] = w[i];
-        sm.DU[i * kLds + vv] = sm.bs[i] * e;
-        sm.Vs[i * kLds + vv] = e * u;
+        for (int off = 16; off > 0; off >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, off);
+        if (lane == 0) sm.dbp[warp][i] = pb;
       }
-    }
-    __syncthreads();
-    // ---- P5: reductions over v: dO S0, dV S0, W G, sum G*S0; dO W^T, dV W^T; dbeta rows
-    float accq[8], accr[8], accw[8];
-    const int kc = tid & 127, i0 = (tid >> 7) * 8;
-    {
-      float gs = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { accq[i] = 0.f; accr[i] = 0.f; accw[i] = 0.f; }
-#pragma unroll 2
-      for (int vv = 0; vv < kDim; vv += 4) {
-        float s0[4], g0[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          s0[x] = sm.S0[(vv + x) * kLds + kc];
-          g0[x] = sm.G[(vv + x) * kLds + kc];
-          gs += s0[x] * g0[x];
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 o4 = *reinterpret_cast<const float4*>(sm.dO + (i0 + i) * kLds + vv);
-          const float4 u4 = *reinterpret_cast<const float4*>(sm.DU + (i0 + i) * kLds + vv);
-          const float4 w4 = *reinterpret_cast<const float4*>(sm.Ws + (i0 + i) * kLds + vv);
-          accq[i] += o4.x * s0[0] + o4.y * s0[1] + o4.z * s0[2] + o4.w * s0[3];
-          accr[i] += u4.x * s0[0] + u4.y * s0[1] + u4.z * s0[2] + u4.w * s0[3];
-          accw[i] += w4.x * g0[0] + w4.y * g0[1] + w4.z * g0[2] + w4.w * g0[3];
-        }
-      }
-      if (tid < kDim) sm.rho[0][kc] = gs;
+    } else {
+      const int t2 = tid - 128;
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
-        const int e = tid + rep * kThreads;
-        const int mat = e >> 8, i = (e >> 4) & 15, j = e & 15;
-        const float* X = mat ? sm.DU : sm.dO;
+        const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
         float acc = 0.f;
 #pragma unroll 8
-        for (int vv = 0; vv < kDim; vv += 4)
-          acc += dot4(*reinterpret_cast<const float4*>(X + i * kLds + vv),
-                      *reinterpret_cast<const float4*>(sm.Ws + j * kLds + vv));
-        (mat ? sm.M2 : sm.M1)[i * (kChunk + 1) + j] = acc;
-      }
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int i = warp * 2 + rr;
-        const float4 x = *reinterpret_cast<const float4*>(sm.Vs + i * kLds + lane * 4);
-        float acc = x.x + x.y + x.z + x.w;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) sm.dba[i] = acc;
+        for (int vv = 0; vv < kDim; ++vv)
+          acc = fmaf(__bfloat162float(sm.dOp[i * kDim + vv]), sm.Up[j * kLds + vv], acc);
+        sm.M1[i][j] = acc * sm.bs[j];
       }
     }
+    tc::fence_async_smem();
     __syncthreads();
-    // ---- P6: assemble dq^, dk^ and the gauge term; update G
+    // ---- MMA group 2: S0^T dV^T and the adjoint update
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
+      const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
+      const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
+#pragma unroll 1
+      for (int st = 0; st < kDim / 8; ++st)
+        tc::mma_ts(tbase + kColR, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        tc::mma_ss(tbase + kColG, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
+#pragma unroll
+      for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) times the dV lo part
+        tc::mma_ss(tbase + kColG, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
+      tc::mma_commit(mbar);
+    }
+    if (warp >= 4) {
+      const int t2 = tid - 128;
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int vv = 0; vv < kDim; ++vv) acc = fmaf(sm.DUp[i * kLds + vv], sm.Up[j * kLds + vv], acc);
+        sm.M2[i][j] = acc * sm.bs[j];
+      }
+    } else if (tid < kChunk) {
+      sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
+    }
+    ok = ok && tc::mbar_wait(mbar, parity);
+    parity ^= 1;
+    tc::fence_after();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows 8 hv .. 8 hv + 7)
     {
-      float* dQh = sm.S0;              // tiles reuse the (no longer needed) S0 storage
-      float* dKh = sm.S0 + kTile;
-      float* tv = sm.S0 + 2 * kTile;
-      const float gck = sm.gC[kc];
+      float* dQh = cmb;
+      float* dKh = cmb + kTileF;
+      float* tv = cmb + 2 * kTileF;
+      float qd[16], rd[16], wg[16];
+      tc::tmem_ld16(tl + kColQ, qd);
+      tc::tmem_ld16(tl + kColR, rd);
+      tc::tmem_ld16(tl + kColWG, wg);
+      const int k = kl, i0 = 8 * hv;
       float rp = 0.f;
 #pragma unroll
       for (int ii = 0; ii < 8; ++ii) {
         const int i = i0 + ii;
-        rp += sm.Kb[i * kLds + kc] * accw[ii];
-        const float gam = sm.Gm[i * kLds + kc];
+        const float gam = sm.Pa[i * kLds + k];
         const float inv = 1.0f / gam;
-        float pq = accq[ii], pr = accr[ii], pw = gck * accw[ii];
+        float pq = qd[i], pr = rd[i], pw = wg[i];
+        rp = fmaf(sm.Kip[i * kLds + k], wg[i], rp);
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          const float kij = sm.Ki[j * kLds + kc];
-          if (j <= i) pq += sm.M1[i * (kChunk + 1) + j] * kij;
-          if (j < i) pr += sm.M2[i * (kChunk + 1) + j] * kij;
-          if (j >= i) pw += s * sm.M1[j * (kChunk + 1) + i] * sm.Qt[j * kLds + kc];
-          if (j > i) pw -= sm.M2[j * (kChunk + 1) + i] * sm.Kt[j * kLds + kc];
+          const float kij = sm.Kip[j * kLds + k];
+          if (j <= i) pq = fmaf(sm.M1[i][j], kij, pq);
+          if (j < i) pr = fmaf(sm.M2[i][j], kij, pr);
+          if (j >= i) pw = fmaf(s * sm.M1[j][i], sm.Qtp[j * kLds + k], pw);
+          if (j > i) pw = fmaf(-sm.M2[j][i], sm.Ktp[j * kLds + k], pw);
         }
         const float dq_ = s * gam * pq;
         const float dkr = -gam * pr;
         const float dkw = inv * pw;
-        const float qh_ = sm.Qt[i * kLds + kc] * inv;
-        const float kh_ = sm.Kt[i * kLds + kc] * inv;
-        dQh[i * kLds + kc] = dq_;
-        dKh[i * kLds + kc] = dkr + dkw;
-        tv[i * kLds + kc] = qh_ * dq_ + kh_ * (dkr - dkw);
+        dQh[i * kLds + k] = dq_;
+        dKh[i * kLds + k] = dkr + dkw;
+        tv[i * kLds + k] = sm.Qtp[i * kLds + k] * inv * dq_ + sm.Ktp[i * kLds + k] * inv * (dkr - dkw);
       }
-      sm.rho[1 + (tid >> 7)][kc] = rp;
-      // G <- G diag(gC) + (scale dO)^T Qt - dV^T Kt
-      const int gv = tid >> 1, half = tid & 1;
-#pragma unroll 4
-      for (int m = 0; m < 16; ++m) {
-        const int kk = m * 8 + half * 4;
-        float4 g4 = *reinterpret_cast<const float4*>(sm.G + gv * kLds + kk);
-        const float4 c4 = *reinterpret_cast<const float4*>(sm.gC + kk);
-        g4.x *= c4.x; g4.y *= c4.y; g4.z *= c4.z; g4.w *= c4.w;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-          const float od = s * sm.dO[i * kLds + gv];
-          const float ud = sm.DU[i * kLds + gv];
-          const float4 q4 = *reinterpret_cast<const float4*>(sm.Qt + i * kLds + kk);
-          const float4 k4 = *reinterpret_cast<const float4*>(sm.Kt + i * kLds + kk);
-          g4.x += od * q4.x - ud * k4.x;
-          g4.y += od * q4.y - ud * k4.y;
-          g4.z += od * q4.z - ud * k4.z;
-          g4.w += od * q4.w - ud * k4.w;
-        }
-        *reinterpret_cast<float4*>(sm.G + gv * kLds + kk) = g4;
-      }
+      sm.rho2[hv][k] = rp;
     }
     __syncthreads();
-    // ---- P7: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
+    // ---- P8: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
     if (tid < kDim) {
-      float* tv = sm.S0 + 2 * kTile;
-      float run = sm.gC[tid] * sm.rho[0][tid] + sm.rho[1][tid] + sm.rho[2][tid];
+      float* tv = cmb + 2 * kTileF;
+      float run = sm.rho0[0][tid] + sm.rho0[1][tid] + sm.rho2[0][tid] + sm.rho2[1][tid];
 #pragma unroll
       for (int i = kChunk - 1; i >= 0; --i) {
         run += tv[i * kLds + tid];
@@ -371,14 +452,14 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
     }
     __syncthreads();
-    // ---- P8: epilogue: gate / sigmoid / L2-norm backward and stores
+    // ---- P9: epilogue: gate / sigmoid / L2-norm backward and stores
     {
-      const float* dQh = sm.S0;
-      const float* dKh = sm.S0 + kTile;
-      const float* da = sm.S0 + 2 * kTile;
+      const float* dQh = cmb;
+      const float* dKh = cmb + kTileF;
+      const float* da = cmb + 2 * kTileF;
       const bool valid = ti < nt;
       const int64_t t = tc0 + ti;
-      float dg8[8], dq8[8], dk8[8], dv8[8];
+      float dg8[8], dq8[8], dk8[8];
       float pq = 0.f, pk = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -391,7 +472,6 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         dA_acc += dz * zz[e];
         dq8[e] = dQh[ti * kLds + c8 + e];
         dk8[e] = dKh[ti * kLds + c8 + e];
-        dv8[e] = sm.DU[ti * kLds + c8 + e];
         pq += qhat[e] * dq8[e];
         pk += khat[e] * dk8[e];
       }
@@ -406,7 +486,6 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
       if (valid) {
         store_bf16x8(a.dg + (t * P.Hv + h) * kDim + c8, dg8);
-        store_bf16x8(a.dv + (t * P.Hv + h) * kDim + c8, dv8);
         if (P.r == 1) {
           store_bf16x8(a.dq + (t * P.Hqk + qh) * kDim + c8, dq8);
           store_bf16x8(a.dk + (t * P.Hqk + qh) * kDim + c8, dk8);
@@ -424,35 +503,47 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
       }
     }
+    tc::fence_before();
     __syncthreads();
   }
-  // dinitial_state = G
-  {
+  if (!aborted) {
+    // dinitial_state = G (stored transposed in TMEM)
     float* dst = a.dh0 + (n * P.Hv + h) * kDim * kDim;
-    for (int f = tid; f < kDim * kDim / 4; f += kThreads) {
-      const int row = f >> 5, c4 = (f & 31) * 4;
-      *reinterpret_cast<float4*>(dst + row * kDim + c4) =
-          *reinterpret_cast<const float4*>(sm.G + row * kLds + c4);
+    tc::fence_after();
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int v0 = 64 * hv + 16 * q;
+      float x[16];
+      tc::tmem_ld16(tl + kColG + v0, x);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dst[(v0 + j) * kDim + kl] = x[j];
     }
-  }
-  // per-unit parameter-gradient partials, reduced in a fixed order
-  {
-    float* red = sm.S0;  // [16 rows][128] + [256]
+    // per-unit parameter-gradient partials, reduced in a fixed order
+    float* red = sm.Qtp;  // [16 rows][128] + [256]: spans Qtp and Ktp
+    __syncthreads();
 #pragma unroll
     for (int e = 0; e < 8; ++e) red[ti * kDim + c8 + e] = ddt_acc[e];
     red[kChunk * kDim + tid] = dA_acc;
     __syncthreads();
-    float* dst = a.par_part + (int64_t)unit * kParStride;
+    float* pp = a.par_part + (int64_t)unit * kParStride;
     if (tid < kDim) {
       float acc = 0.f;
       for (int i = 0; i < kChunk; ++i) acc += red[i * kDim + tid];
-      dst[tid] = acc;
+      pp[tid] = acc;
     }
     if (tid == 0) {
       float acc = 0.f;
       for (int i = 0; i < kThreads; ++i) acc += red[kChunk * kDim + i];
-      dst[kDim] = acc;
+      pp[kDim] = acc;
     }
+  } else if (tid == 0) {
+    atomicExch(P.status, 1);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tbase, kTmemCols);
   }
 }
 

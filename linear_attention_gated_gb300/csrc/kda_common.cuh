@@ -34,6 +34,8 @@ struct Problem {
   const int32_t* order;   // launch slot -> unit id (n * Hv + h), longest sequence first
   const SeqInfo* seq;     // [N]
   float* ckpt;            // [n_ck, Hv, 128, 128] state at the start of every checkpoint interval
+  float* utape;           // [Ttot, Hv, 128]: u_t = v_t - S'_t k^_t of every token (forward -> backward)
+  int32_t* status;        // device status word: non-zero when a bounded device wait gave up
   int64_t N, Hqk, Hv;
   int32_t r;              // Hv / Hqk
   float scale, lb;

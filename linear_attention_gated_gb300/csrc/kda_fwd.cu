@@ -1,66 +1,96 @@
-// kda_fwd.cu -- chunked forward of the recurrent KDA training recurrence.
+// kda_fwd.cu -- chunked forward of the recurrent KDA training recurrence on
+// sm_103a tensor cores.
 //
 // One CTA owns one (sequence, value head) unit and walks its tokens in
-// sub-chunks of kChunk = 16, keeping the 128x128 FP32 value-first state on
-// chip. Within a sub-chunk starting from state S0, with Gam_i the cumulative
-// log-decay of tokens 1..i (per key dim) and gamma_i = exp(Gam_i):
-//   A_ij = k^_i . (k^_j * gamma_i / gamma_j)   (j < i)
-//   B_ij = q^_i . (k^_j * gamma_i / gamma_j)   (j <= i)
-//   T    = (I + diag(beta) A)^-1
-//   Y    = V - (k^ * gamma) S0^T,   W = T diag(beta) Y      (rows: beta_i u_i)
-//   O    = scale ((q^ * gamma) S0^T + B W)
-//   S_C  = S0 diag(gamma_C) + W^T (k^ * gamma_C / gamma)
+// sub-chunks of kChunk = 16, keeping the 128x128 FP32 value-first state in
+// registers (thread (warp w, lane l) owns row 32 (w % 4) + l, columns
+// [64 (w / 4), +64)). Within a sub-chunk starting from state S0, with Gam_i the
+// cumulative log-decay of tokens 1..i (per key dim) and gamma_i = exp(Gam_i):
+//   A_ij = k^_i . (k^_j gamma_i / gamma_j)   (j < i)      B_ij likewise with q^_i (j <= i)
+//   Y    = V - (k^ gamma) S0^T
+//   W    solves (I + diag(beta) A) W = diag(beta) Y      (rows: beta_i u_i)
+//   O    = scale ((q^ gamma) S0^T + B W)
+//   S_C  = S0 diag(gamma_C) + W^T (k^ gamma_C / gamma)
 // which equals the token-by-token rule S' = S diag(d); u = v - S' k^;
 // S = S' + beta u k^T; o = scale S q^ (flashinfer.kda_backward.recurrent_kda_backward,
-// description: gate, norm and sigmoid contracts). The gate, L2 norm and sigmoid
-// of each token are computed on chip (the fused prologue). The state at the
-// start of every checkpoint interval is stored for the backward.
+// description: gate, norm and sigmoid contracts; the update order is the plain
+// reading the library adopts).
+//
+// Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
+// three contractions: [k^ gamma; q^ gamma] (k^/gamma)^T (A and B, 16x16 each),
+// S0 [k^ gamma; q^ gamma]^T (128x32) and W^T (k^ gamma_C/gamma) (128x128).
+// Operands are rounded to TF32 when written to shared memory; the state update
+// uses split TF32 (x = hi + lo, three products) so that the carried state keeps
+// FP32-level accuracy. Accumulation, the triangular solve, the output and the
+// state stay FP32. Each token's u = v - S' k^ is saved for the backward. The gate, L2 norm
+// and sigmoid of each token are computed on chip (the fused prologue). The
+// state at the start of every checkpoint interval is stored for the backward.
 #include "kda_common.cuh"
+#include "tc.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTile = kChunk * kLds;
-constexpr int kSq = kChunk * (kChunk + 1);
+constexpr int kTileF = kChunk * kLds;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColAB = 0;    // [k^g; q^g] (k^/g)^T   : 16 columns, lanes 0..31 used
+constexpr uint32_t kColYO = 32;   // S0 [k^g; q^g]^T       : 32 columns
+constexpr uint32_t kColU = 128;   // W^T (k^ gC / g)       : 128 columns
 
 struct FwdSmem {
-  float Qt[kTile];   // q^ * gamma
-  float Kt[kTile];   // k^ * gamma
-  float Ki[kTile];   // k^ / gamma
-  float Kb[kTile];   // k^ * gamma_C / gamma
-  float Vs[kTile];   // v
-  float Am[kSq];
-  float Bm[kSq];
-  float Tm[kSq];
-  float bs[kChunk];  // beta = sigmoid(logit)
-  float gC[kDim];    // gamma at the end of the sub-chunk
+  // Tensor-core operands. KQ must directly precede Sa: the A operand of the
+  // A/B product is 128 rows starting at KQ (rows 32..127 read Sa and are unused).
+  unsigned char KQ[32 * kDim * 4];      // rows 0..15 k^ gamma, rows 16..31 q^ gamma   (K-major, K = 128)
+  unsigned char Sa[kDim * kDim * 4];    // chunk-start state, rows v                  (K-major, K = 128)
+  unsigned char Ki[kChunk * kDim * 4];  // k^ / gamma, rows t                          (K-major, K = 128)
+  unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo parts (K = 16)
+  unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo parts                     (K = 16)
+  float Pq[kTileF];                     // q^
+  float Pk[kTileF];                     // k^
+  float Pa[kTileF];                     // log decay, then gamma
+  float Vs[kTileF];                     // v
+  float As[kChunk][kChunk + 1];
+  float Bs[kChunk][kChunk + 1];
+  float bs[kChunk];
+  float gC[kDim];
+  unsigned long long mbar;
+  uint32_t tmem_base;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fwd_kernel(const Problem P, const FwdOut out) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(smem_raw);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = P.order[blockIdx.x];
   const int64_t n = unit / P.Hv;
   const int64_t h = unit % P.Hv;
   const int64_t qh = h / P.r;
   const SeqInfo si = P.seq[n];
 
-  // state ownership: row sv, key quads kq(m) = m*8 + half*4, m = 0..15
-  const int sv = tid >> 1;
-  const int half = tid & 1;
+  const int sv = 32 * (warp & 3) + lane;  // state row owned by this thread
+  const int ch = warp >> 2;               // column half [64 ch, 64 ch + 64)
   float S[64];
   {
-    const float* src = P.h0 + ((n * P.Hv + h) * kDim + sv) * kDim;
+    const float* src = P.h0 + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-      const float4 x = *reinterpret_cast<const float4*>(src + m * 8 + half * 4);
+      const float4 x = *reinterpret_cast<const float4*>(src + 4 * m);
       S[4 * m] = x.x; S[4 * m + 1] = x.y; S[4 * m + 2] = x.z; S[4 * m + 3] = x.w;
     }
   }
-  // tile mapping: token row ti, 8 columns from c8
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
+  if (tid == 0) tc::mbar_init(tc::smem_u32(&sm.mbar), 1);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = sm.tmem_base;
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t mbar = tc::smem_u32(&sm.mbar);
+  uint32_t parity = 0;
+  bool ok = true;
+
   const int ti = tid >> 4;
   const int c8 = (tid & 15) * 8;
   const float ea = expf(P.A_log[h]);
@@ -70,17 +100,17 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 
   const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
   const int ck_every = kCkTokens / kChunk;
+  bool aborted = false;
   for (int64_t c = 0; c < nchunks; ++c) {
     const int64_t tc0 = si.t0 + c * kChunk;
     const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
     if (c % ck_every == 0) {
-      float* dst = P.ckpt + (((si.ck_base + c / ck_every) * P.Hv + h) * kDim + sv) * kDim;
+      float* dst = P.ckpt + (((si.ck_base + c / ck_every) * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        *reinterpret_cast<float4*>(dst + m * 8 + half * 4) =
-            make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+        *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
     }
-    // ---- load the sub-chunk and run the prologue (L2 norm, gate, sigmoid beta)
+    // ---- prologue: L2 norm, gate, sigmoid beta (token row ti, columns c8..c8+7)
     {
       float qv[8], kv[8], gv[8], vv[8];
       const bool valid = ti < nt;
@@ -104,135 +134,180 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float z = ea * (gv[e] + dtb[e]);
-        const float a = valid ? P.lb / (1.0f + expf(-z)) : 0.f;  // log decay
-        sm.Qt[ti * kLds + c8 + e] = qv[e] * rq;
-        sm.Kt[ti * kLds + c8 + e] = kv[e] * rk;
-        sm.Ki[ti * kLds + c8 + e] = a;
+        sm.Pq[ti * kLds + c8 + e] = qv[e] * rq;
+        sm.Pk[ti * kLds + c8 + e] = kv[e] * rk;
+        sm.Pa[ti * kLds + c8 + e] = valid ? P.lb / (1.0f + expf(-z)) : 0.f;
         sm.Vs[ti * kLds + c8 + e] = vv[e];
       }
       if (tid < kChunk)
-        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-__bfloat162float(P.beta[(tc0 + tid) * P.Hv + h])))
-                                : 0.f;
+        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-__bfloat162float(P.beta[(tc0 + tid) * P.Hv + h]))) : 0.f;
+    }
+    // ---- chunk-start state as a TF32 operand
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const int k = 64 * ch + 4 * m;
+      *reinterpret_cast<float4*>(sm.Sa + tc::kmaj(sv, k, kDim)) =
+          make_float4(tc::round_tf32(S[4 * m]), tc::round_tf32(S[4 * m + 1]), tc::round_tf32(S[4 * m + 2]),
+                      tc::round_tf32(S[4 * m + 3]));
     }
     __syncthreads();
     // ---- cumulative decay along the sub-chunk (one key column per thread)
     if (tid < kDim) {
-      const int kc = tid;
       float G = 0.f;
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        G += sm.Ki[i * kLds + kc];
-        sm.Ki[i * kLds + kc] = G;  // keep Gam_i for the second pass
+        G += sm.Pa[i * kLds + tid];
+        sm.Pa[i * kLds + tid] = expf(G);
       }
-      const float GC = G;
-      sm.gC[kc] = expf(GC);
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const float Gi = sm.Ki[i * kLds + kc];
-        const float kh = sm.Kt[i * kLds + kc];
-        const float gam = expf(Gi);
-        sm.Qt[i * kLds + kc] *= gam;
-        sm.Kt[i * kLds + kc] = kh * gam;
-        sm.Ki[i * kLds + kc] = kh * expf(-Gi);
-        sm.Kb[i * kLds + kc] = kh * expf(GC - Gi);
-      }
+      sm.gC[tid] = expf(G);
     }
     __syncthreads();
-    // ---- A (strictly lower) and B (lower with diagonal)
+    // ---- operand tiles: token t, key quads q4 and q4 + 16
+    {
+      const int t = tid & 15;
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int e = tid + rep * kThreads;
-      const int mat = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const float* X = mat ? sm.Qt : sm.Kt;
-      float acc = 0.f;
-      if (j < i || (mat && j == i)) {
-#pragma unroll 8
-        for (int kk = 0; kk < kDim; kk += 4)
-          acc += dot4(*reinterpret_cast<const float4*>(X + i * kLds + kk),
-                      *reinterpret_cast<const float4*>(sm.Ki + j * kLds + kk));
+      for (int rep = 0; rep < 2; ++rep) {
+        const int k0 = 4 * ((tid >> 4) + 16 * rep);
+        const float4 qh4 = *reinterpret_cast<const float4*>(sm.Pq + t * kLds + k0);
+        const float4 kh4 = *reinterpret_cast<const float4*>(sm.Pk + t * kLds + k0);
+        const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + t * kLds + k0);
+        const float4 c4 = *reinterpret_cast<const float4*>(sm.gC + k0);
+        const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
+        const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ca[4] = {c4.x, c4.y, c4.z, c4.w};
+        float kt[4], qt[4], ki[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float inv = 1.0f / ga[e];
+          kt[e] = tc::round_tf32(ka[e] * ga[e]);
+          qt[e] = tc::round_tf32(qa[e] * ga[e]);
+          ki[e] = tc::round_tf32(ka[e] * inv);
+          const float kb = ka[e] * (ca[e] * inv);
+          const float kb_hi = tc::round_tf32(kb);
+          *reinterpret_cast<float*>(sm.KbT[0] + tc::kmaj(k0 + e, t, kChunk)) = kb_hi;
+          *reinterpret_cast<float*>(sm.KbT[1] + tc::kmaj(k0 + e, t, kChunk)) = tc::round_tf32(kb - kb_hi);
+        }
+        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(t, k0, kDim)) = make_float4(kt[0], kt[1], kt[2], kt[3]);
+        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(16 + t, k0, kDim)) = make_float4(qt[0], qt[1], qt[2], qt[3]);
+        *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(t, k0, kDim)) = make_float4(ki[0], ki[1], ki[2], ki[3]);
       }
-      (mat ? sm.Bm : sm.Am)[i * (kChunk + 1) + j] = acc;
     }
+    tc::fence_async_smem();
+    tc::fence_before();
     __syncthreads();
-    // ---- T = (I + diag(beta) A)^-1 by forward substitution, one column per lane
-    if (tid < kChunk) {
-      const int j = tid;
-      float tc[kChunk];
+    // ---- tensor cores: A/B matrices and S0 [k^g; q^g]^T
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t kq = tc::smem_u32(sm.KQ), sa = tc::smem_u32(sm.Sa), ki = tc::smem_u32(sm.Ki);
+#pragma unroll 1
+      for (int s = 0; s < kDim / 8; ++s)
+        tc::mma_ss(tbase + kColAB, tc::kdesc(kq, s, kDim), tc::kdesc(ki, s, kDim), tc::idesc_tf32(128, 16), s > 0);
+#pragma unroll 1
+      for (int s = 0; s < kDim / 8; ++s)
+        tc::mma_ss(tbase + kColYO, tc::kdesc(sa, s, kDim), tc::kdesc(kq, s, kDim), tc::idesc_tf32(128, 32), s > 0);
+      tc::mma_commit(mbar);
+    }
+    ok = ok && tc::mbar_wait(mbar, parity);
+    parity ^= 1;
+    tc::fence_after();
+    float yp[16], op[16];
+    if (warp < 4) {
+      tc::tmem_ld16(tbase + lane_off + kColYO, yp);
+      tc::tmem_ld16(tbase + lane_off + kColYO + 16, op);
+    }
+    if (warp == 0) {
+      float r[16];
+      tc::tmem_ld16(tbase + lane_off + kColAB, r);
+      if (lane < 16) {
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        float acc = 0.f;
+        for (int j = 0; j < kChunk; ++j) sm.As[lane][j] = (j < lane) ? r[j] : 0.f;
+      } else {
 #pragma unroll
-        for (int m = 0; m < i; ++m)
-          if (m >= j) acc += sm.Am[i * (kChunk + 1) + m] * tc[m];
-        tc[i] = (i < j) ? 0.f : (i == j ? 1.f : -sm.bs[i] * acc);
-        sm.Tm[i * (kChunk + 1) + j] = tc[i];
+        for (int j = 0; j < kChunk; ++j) sm.Bs[lane - 16][j] = (j <= lane - 16) ? r[j] : 0.f;
       }
     }
+    tc::fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    // ---- W by forward substitution and the output (one state row per thread)
+    if (warp < 4) {
+      float w[kChunk];
+#pragma unroll
+      for (int t = 0; t < kChunk; ++t) {
+        float acc = sm.Vs[t * kLds + sv] - yp[t];
+#pragma unroll
+        for (int j = 0; j < t; ++j) acc -= sm.As[t][j] * w[j];
+        w[t] = sm.bs[t] * acc;
+        if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc;  // u_t for the backward
+      }
+#pragma unroll
+      for (int t = 0; t < kChunk; ++t) {
+        float acc = op[t];
+#pragma unroll
+        for (int j = 0; j <= t; ++j) acc += sm.Bs[t][j] * w[j];
+        if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * acc);
+      }
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) {
+        float hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[e] = tc::round_tf32(w[4 * t4 + e]);
+          lo[e] = tc::round_tf32(w[4 * t4 + e] - hi[e]);
+        }
+        *reinterpret_cast<float4*>(sm.Wa[0] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<float4*>(sm.Wa[1] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    tc::fence_async_smem();
     __syncthreads();
-    // ---- state products for row sv of the state
-    float y[kChunk], oa[kChunk];
+    // ---- tensor cores: rank-16 state update W^T (k^ gamma_C / gamma) in split TF32
+    // (hi hi + lo hi + hi lo: the state keeps FP32-level accuracy)
+    if (tid == 0) {
+      tc::fence_after();
+      const uint32_t wa[2] = {tc::smem_u32(sm.Wa[0]), tc::smem_u32(sm.Wa[1])};
+      const uint32_t kb[2] = {tc::smem_u32(sm.KbT[0]), tc::smem_u32(sm.KbT[1])};
+      const int pa[3] = {0, 1, 0}, pb[3] = {0, 0, 1};
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) { y[i] = 0.f; oa[i] = 0.f; }
+      for (int p = 0; p < 3; ++p)
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const int kk = m * 8 + half * 4;
-      const float4 s4 = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        y[i] += dot4(*reinterpret_cast<const float4*>(sm.Kt + i * kLds + kk), s4);
-        oa[i] += dot4(*reinterpret_cast<const float4*>(sm.Qt + i * kLds + kk), s4);
-      }
+        for (int s = 0; s < kChunk / 8; ++s)
+          tc::mma_ss(tbase + kColU, tc::kdesc(wa[pa[p]], s, kChunk), tc::kdesc(kb[pb[p]], s, kChunk),
+                     tc::idesc_tf32(128, 128), (p | s) > 0);
+      tc::mma_commit(mbar);
     }
+    ok = ok && tc::mbar_wait(mbar, parity);
+    parity ^= 1;
+    tc::fence_after();
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      y[i] += __shfl_xor_sync(0xffffffffu, y[i], 1);
-      oa[i] += __shfl_xor_sync(0xffffffffu, oa[i], 1);
-      y[i] = sm.bs[i] * (sm.Vs[i * kLds + sv] - y[i]);  // beta_i (v_i - S0 k~_i)
+    for (int q = 0; q < 4; ++q) {
+      float u[16];
+      tc::tmem_ld16(tbase + lane_off + kColU + 64 * ch + 16 * q, u);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) S[16 * q + j] = fmaf(S[16 * q + j], sm.gC[64 * ch + 16 * q + j], u[j]);
     }
-    float w[kChunk];
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      float acc = 0.f;
-#pragma unroll
-      for (int j = 0; j <= i; ++j) acc += sm.Tm[i * (kChunk + 1) + j] * y[j];
-      w[i] = acc;
-    }
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      float acc = oa[i];
-#pragma unroll
-      for (int j = 0; j <= i; ++j) acc += sm.Bm[i * (kChunk + 1) + j] * w[j];
-      if ((i & 1) == half && i < nt)
-        out.o[((tc0 + i) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * acc);
-    }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const int kk = m * 8 + half * 4;
-      const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + kk);
-      float s0 = S[4 * m] * g4.x, s1 = S[4 * m + 1] * g4.y, s2 = S[4 * m + 2] * g4.z,
-            s3 = S[4 * m + 3] * g4.w;
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const float4 kb = *reinterpret_cast<const float4*>(sm.Kb + i * kLds + kk);
-        s0 += w[i] * kb.x; s1 += w[i] * kb.y; s2 += w[i] * kb.z; s3 += w[i] * kb.w;
-      }
-      S[4 * m] = s0; S[4 * m + 1] = s1; S[4 * m + 2] = s2; S[4 * m + 3] = s3;
-    }
-    __syncthreads();
+    tc::fence_before();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
   }
-  float* dst = out.hT + ((n * P.Hv + h) * kDim + sv) * kDim;
+  if (!aborted) {
+    float* dst = out.hT + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
 #pragma unroll
-  for (int m = 0; m < 16; ++m)
-    *reinterpret_cast<float4*>(dst + m * 8 + half * 4) =
-        make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+    for (int m = 0; m < 16; ++m)
+      *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+  } else if (tid == 0) {
+    atomicExch(P.status, 1);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tbase, kTmemCols);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_forward(const Problem& P, const FwdOut& out, int64_t units, cudaStream_t s) {
   const size_t smem = sizeof(FwdSmem);
-  cudaError_t e = cudaFuncSetAttribute(kda_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kda_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kda_fwd_kernel<<<(unsigned)units, kThreads, smem, s>>>(P, out);
   return cudaGetLastError();

@@ -149,10 +149,12 @@ extern "C" kda_status kda_bwd_noalloc(
   const size_t o_seq = off;   off = up(off + sizeof(kda::SeqInfo) * N);
   const size_t o_cu = off;    off = up(off + sizeof(int64_t) * (N + 1));
   const size_t o_ck = off;    off = up(off + sizeof(float) * (size_t)n_ck * Hv * D * D);
+  const size_t o_ut = off;    off = up(off + sizeof(float) * (size_t)Ttot * Hv * D);
   const size_t o_dqk = off;   if (r > 1) off = up(off + sizeof(float) * (size_t)Ttot * Hv * 2 * D);
   const size_t o_par = off;   off = up(off + sizeof(float) * (size_t)units * kda::kParStride);
   const size_t o_o = off;     off = up(off + sizeof(kda_bf16) * (size_t)Ttot * Hv * D);
   const size_t o_hT = off;    off = up(off + sizeof(float) * (size_t)N * Hv * D * D);
+  const size_t o_status = off; off = up(off + 16);
   if (off > kNoAllocScratchBytes)
     return nfail(KDA_ERR_WORKSPACE_TOO_SMALL,
                  "problem needs %zu bytes of scratch; kda_bwd_noalloc has %zu (use kda_fwd + kda_bwd)",
@@ -210,6 +212,8 @@ extern "C" kda_status kda_bwd_noalloc(
   P.order = reinterpret_cast<const int32_t*>(sc + o_order);
   P.seq = reinterpret_cast<const kda::SeqInfo*>(sc + o_seq);
   P.ckpt = reinterpret_cast<float*>(sc + o_ck);
+  P.status = reinterpret_cast<int32_t*>(sc + o_status);
+  P.utape = reinterpret_cast<float*>(sc + o_ut);
   P.N = N;
   P.Hqk = Hqk;
   P.Hv = Hv;

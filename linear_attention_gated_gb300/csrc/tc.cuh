@@ -1,0 +1,155 @@
+// tc.cuh -- thin inline-PTX helpers for the sm_103a tensor-core path:
+// TMEM allocation, tcgen05.mma (kind::tf32, FP32 accumulate), commit to an
+// mbarrier, bounded mbarrier waits, TMEM loads, and the shared-memory operand
+// layout the MMAs read.
+//
+// Operand layout (canonical "no swizzle" K-major form): a tile of R rows by C
+// 4-byte elements along K is stored as 8-row x 16-byte core matrices; element
+// (r, c) sits at  (r / 8) * SBO + (c / 4) * 128 + (r % 8) * 16 + (c % 4) * 4
+// with SBO = (C / 4) * 128 bytes (8-row groups) and LBO = 128 bytes (the
+// K-adjacent core matrix). One MMA K-step of 8 TF32 elements covers two core
+// matrices, so step s starts 256 bytes further along.
+// The tensor core reads TF32 by dropping the low 13 mantissa bits of an FP32
+// operand; operands are therefore rounded to nearest (cvt.rna.tf32.f32) when
+// they are written.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t u;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
+  return __uint_as_float(u);
+}
+
+// Byte offset of element (r, c) in a K-major operand tile with kcols elements along K.
+__device__ __forceinline__ uint32_t kmaj(int r, int c, int kcols) {
+  return (uint32_t)((r >> 3) * (kcols >> 2) * 128 + (c >> 2) * 128 + (r & 7) * 16 + (c & 3) * 4);
+}
+
+// Shared-memory matrix descriptor (no swizzle, sm_100 family version bits).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// Descriptor of K-step s (8 TF32 elements) of a K-major tile with kcols along K.
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile_saddr, int s, int kcols) {
+  return sdesc(tile_saddr + (uint32_t)s * 256u, 128u, (uint32_t)(kcols >> 2) * 128u);
+}
+
+// Instruction descriptor: kind::tf32, FP32 accumulator, K-major A and B.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool negA = false) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((negA ? 1u : 0u) << 13) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// A operand read from tensor memory (128 lanes x K columns at a_tmem).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
+  asm volatile("fence.mbarrier_init.release.cluster;");
+}
+
+// Bounded wait for the given phase parity (about two seconds of SM clock);
+// false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > (1ll << 32)) return false;
+  }
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Make generic-proxy shared-memory writes visible to the tensor core.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane (caller
+// issues tcgen05.wait::st before the values are consumed by an MMA).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])));
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 4x4 transpose among the four lanes of an aligned lane quad: on entry lane
+// (quad base + j) holds row j of the block, on exit it holds column j.
+__device__ __forceinline__ void quad_transpose(float x[4], int lane) {
+  const bool odd = lane & 1;
+  float a = odd ? x[0] : x[1];
+  float b = odd ? x[2] : x[3];
+  a = __shfl_xor_sync(0xffffffffu, a, 1);
+  b = __shfl_xor_sync(0xffffffffu, b, 1);
+  if (odd) { x[0] = a; x[2] = b; } else { x[1] = a; x[3] = b; }
+  const bool hi = lane & 2;
+  float c = hi ? x[0] : x[2];
+  float d = hi ? x[1] : x[3];
+  c = __shfl_xor_sync(0xffffffffu, c, 2);
+  d = __shfl_xor_sync(0xffffffffu, d, 2);
+  if (hi) { x[0] = c; x[1] = d; } else { x[2] = c; x[3] = d; }
+}
+
+}  // namespace tc
+}  // namespace kda
