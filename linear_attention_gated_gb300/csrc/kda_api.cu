@@ -38,7 +38,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Shape {
-  int64_t B = 0, T = 0, Hqk = 0, Hv = 0, N = 0, Ttot = 0, units = 0, n_ck = 0;
+  int64_t B = 0, T = 0, Hqk = 0, Hv = 0, N = 0, Ttot = 0, units = 0, n_ck = 0, n_ch = 0;
   bool packed = false;
   std::vector<int64_t> cu;  // N + 1 token offsets
   bool operator==(const Shape& o) const {
@@ -47,7 +47,7 @@ struct Shape {
 };
 
 struct Layout {
-  size_t order = 0, seq = 0, ckpt = 0, utape = 0, dqk = 0, par = 0, status = 0, total = 0;
+  size_t order = 0, seq = 0, ckpt = 0, utape = 0, abtape = 0, dqk = 0, par = 0, status = 0, total = 0;
 };
 
 Layout make_layout(const Shape& s) {
@@ -57,6 +57,7 @@ Layout make_layout(const Shape& s) {
   L.seq = off;   off = align_up(off + sizeof(SeqInfo) * s.N);
   L.ckpt = off;  off = align_up(off + sizeof(float) * (size_t)s.n_ck * s.Hv * kda::kDim * kda::kDim);
   L.utape = off; off = align_up(off + sizeof(float) * (size_t)s.Ttot * s.Hv * kda::kDim);
+  L.abtape = off; off = align_up(off + sizeof(float) * (size_t)s.n_ch * s.Hv * 2 * kda::kChunk * kda::kChunk);
   L.dqk = off;
   if (s.Hv != s.Hqk) off = align_up(off + sizeof(float) * (size_t)s.Ttot * s.Hv * 2 * kda::kDim);
   L.par = off;   off = align_up(off + sizeof(float) * (size_t)s.units * kda::kParStride);
@@ -99,7 +100,11 @@ kda_status make_shape(int64_t B, int64_t T, int64_t Hqk, int64_t Hv, const int64
   if (s.N * Hv > INT32_MAX) return fail(KDA_ERR_UNSUPPORTED, "too many (sequence, head) units");
   s.units = s.N * Hv;
   s.n_ck = 0;
-  for (int64_t i = 0; i < s.N; ++i) s.n_ck += (s.cu[i + 1] - s.cu[i] + kda::kCkTokens - 1) / kda::kCkTokens;
+  s.n_ch = 0;
+  for (int64_t i = 0; i < s.N; ++i) {
+    s.n_ck += (s.cu[i + 1] - s.cu[i] + kda::kCkTokens - 1) / kda::kCkTokens;
+    s.n_ch += (s.cu[i + 1] - s.cu[i] + kda::kChunk - 1) / kda::kChunk;
+  }
   *out = std::move(s);
   return KDA_OK;
 }
@@ -262,13 +267,14 @@ kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, cons
       return la > lb;
     });
     c->seq.resize(s.N);
-    int64_t ck = 0;
+    int64_t ck = 0, chn = 0;
     for (int64_t i = 0; i < s.N; ++i) {
       c->seq[i].t0 = s.cu[i];
       c->seq[i].len = s.cu[i + 1] - s.cu[i];
       c->seq[i].ck_base = ck;
-      c->seq[i].pad = 0;
+      c->seq[i].ch_base = chn;
       ck += (c->seq[i].len + kda::kCkTokens - 1) / kda::kCkTokens;
+      chn += (c->seq[i].len + kda::kChunk - 1) / kda::kChunk;
     }
   } else {
     if (!(c->shape == s)) return fail(KDA_ERR_CONTEXT, "context was created for a different shape");
@@ -302,6 +308,7 @@ kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, cons
   P.ckpt = reinterpret_cast<float*>(c->ws + L.ckpt);
   P.status = reinterpret_cast<int32_t*>(c->ws + L.status);
   P.utape = reinterpret_cast<float*>(c->ws + L.utape);
+  P.abtape = reinterpret_cast<float*>(c->ws + L.abtape);
   P.N = s.N;
   P.Hqk = Hqk;
   P.Hv = Hv;

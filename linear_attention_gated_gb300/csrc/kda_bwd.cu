@@ -28,9 +28,11 @@
 // sub-chunks (a running sum over the whole sequence drifts in FP32).
 //
 // Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
-// state-sized contractions: [k^g; q^g] (k^/g)^T (A and B), S0^T [dO; dV]^T,
-// Gd (k^/g)^T, Gd^T W^T (W split into TF32 hi + lo) and the rank-32 adjoint
-// update (dV split into hi + lo; dO is exact in TF32). The 16x16 intra-chunk
+// state-sized contractions S0^T [dO; dV]^T, Gd (k^/g)^T, Gd^T W^T (W split into
+// TF32 hi + lo) and the rank-32 adjoint update (dV split into hi + lo; dO is
+// exact in TF32). The forward's FP32 A and B of each sub-chunk are reused. The
+// next sub-chunk's token tiles, u, A/B and state checkpoint are prefetched with
+// cp.async into buffers freed earlier in the current sub-chunk. The 16x16 intra-chunk
 // products, the substitutions and the combination run in FP32 on CUDA cores:
 // the decay gradient is a difference of nearly equal terms and needs them at
 // full single precision. The gate, sigmoid and L2-norm backward are applied in
@@ -51,42 +53,44 @@ constexpr uint32_t kColG = 0;     // G^T, FP32 accumulator (lanes k, columns v)
 constexpr uint32_t kColGr = 128;  // Gd^T rounded to TF32 (A operand of Gd^T W^T)
 constexpr uint32_t kColS = 256;   // S0^T rounded to TF32 (A operand of S0^T [dO; dV]^T)
 constexpr uint32_t kColDW = 384;  // Gd (k^/g)^T : lanes v, 16 columns
-constexpr uint32_t kColAB = 400;  // [k^g; q^g] (k^/g)^T : lanes 0..31, 16 columns
-constexpr uint32_t kColQ = 416;   // S0^T dO^T : lanes k, 16 columns
-constexpr uint32_t kColR = 432;   // S0^T dV^T : lanes k, 16 columns
-constexpr uint32_t kColWG = 448;  // Gd^T W^T  : lanes k, 16 columns
+constexpr uint32_t kColQ = 400;   // S0^T dO^T : lanes k, 16 columns
+constexpr uint32_t kColR = 416;   // S0^T dV^T : lanes k, 16 columns
+constexpr uint32_t kColWG = 432;  // Gd^T [W_hi; W_lo]^T : lanes k, 32 columns
 
 struct BwdSmem {
-  // KQ must directly precede Gdv: the A operand of the A/B product is 128 rows
-  // starting at KQ (rows 32..127 read Gdv and are unused).
-  unsigned char KQ[32 * kDim * 4];        // rows 0..15 k^ gamma, 16..31 q^ gamma (K-major, K = 128)
-  unsigned char Gdv[kDim * kDim * 4];     // Gd rows v, TF32                     (K-major, K = 128)
+  // Gd rows v for the A operand of Gd (k^/g)^T. Once that product has been
+  // read, the region stages the next sub-chunk's state checkpoint (cp.async).
+  unsigned char Gdv[kDim * kDim * 4];     // (K-major, K = 128)
   unsigned char Ki[kChunk * kDim * 4];    // k^ / gamma rows t                  (K-major, K = 128)
   // Wt and dOU are contiguous: after the second MMA group they hold the
   // combination tiles (d q^, d k^, gauge term).
-  unsigned char Wt[2][kChunk * kDim * 4]; // W rows t, TF32 hi / lo              (K-major, K = 128)
+  unsigned char Wt[2][kChunk * kDim * 4]; // W rows t, TF32 hi then lo (one N = 32 operand)
   unsigned char dOU[32 * kDim * 4];       // rows 0..15 dO, 16..31 dV           (K-major, K = 128)
   unsigned char dOUv[kDim * 32 * 4];      // rows v: cols 0..15 dO, 16..31 dV (hi) (K-major, K = 32)
   unsigned char dUlo[kDim * kChunk * 4];  // rows v: dV lo part                 (K-major, K = 16)
   unsigned char QKT[kDim * 32 * 4];       // rows k: cols 0..15 scale q^g, 16..31 -k^g (K-major, K = 32)
   float Pa[kTileF];                       // log decay, then gamma
-  float Qtp[kTileF];                      // q^ gamma (FP32)
-  float Ktp[kTileF];                      // k^ gamma (FP32)
+  float Qtp[kTileF];                      // q^, then q^ gamma (FP32)
+  float Ktp[kTileF];                      // k^, then k^ gamma (FP32)
   float Kip[kTileF];                      // k^ / gamma (FP32)
-  float Up[kTileF];                       // u from the forward
+  float Up[kTileF];                       // u from the forward (cp.async staging)
   float DUp[kTileF];                      // dV
-  __nv_bfloat16 dOp[kChunk * kDim];       // do
-  float As[kChunk][kSq];
-  float Bs[kChunk][kSq];
+  __nv_bfloat16 Sq[kChunk * kDim];        // q, k, g, do of the sub-chunk (cp.async staging)
+  __nv_bfloat16 Sk[kChunk * kDim];
+  __nv_bfloat16 Sg[kChunk * kDim];
+  __nv_bfloat16 dOp[kChunk * kDim];
+  float As[kChunk][kChunk];               // A and B of the sub-chunk, from the forward (cp.async staging);
+  float Bs[kChunk][kChunk];               // As and Bs must stay contiguous
   float M1[kChunk][kSq];                  // dO W^T
   float M2[kChunk][kSq];                  // dV W^T
   float bs[kChunk];
+  float braw[kChunk];
   float dba[kChunk];
   float gC[kDim];
   float rho0[2][kDim];                    // halves of sum_v Gd * S0
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
   float dbp[4][kChunk];                   // per-warp partial dbeta
-  unsigned long long mbar;
+  unsigned long long mbar[2];
   uint32_t tmem_base;
 };
 
@@ -106,16 +110,58 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   const int hv = warp >> 2;               // column half handled by this thread
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
-  if (tid == 0) tc::mbar_init(tc::smem_u32(&sm.mbar), 1);
+  if (tid == 0) {
+    tc::mbar_init(tc::smem_u32(&sm.mbar[0]), 1);
+    tc::mbar_init(tc::smem_u32(&sm.mbar[1]), 1);
+  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = sm.tmem_base;
   const uint32_t tl = tbase + lane_off;
-  const uint32_t mbar = tc::smem_u32(&sm.mbar);
-  uint32_t parity = 0;
+  const uint32_t mb0 = tc::smem_u32(&sm.mbar[0]), mb1 = tc::smem_u32(&sm.mbar[1]);
+  uint32_t par0 = 0, par1 = 0;
   bool ok = true;
   bool aborted = false;
+
+  const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
+  const int ck_every = kCkTokens / kChunk;
+  // staging mapping: row tid / 16, 8 consecutive columns
+  const int srow = tid >> 4, scol = (tid & 15) * 8;
+  __nv_bfloat16 nb = __float2bfloat16_rn(0.f);
+  auto rows_of = [&](int64_t cc) { return (int)((si.len - cc * kChunk) < kChunk ? (si.len - cc * kChunk) : kChunk); };
+  auto prefetch_qkg = [&](int64_t cc) {
+    const int ntc = rows_of(cc);
+    const bool okr = srow < ntc;
+    const int64_t t = si.t0 + cc * kChunk + srow;
+    tc::cp_async16(sm.Sq + srow * kDim + scol, okr ? P.q + (t * P.Hqk + qh) * kDim + scol : P.q, okr ? 16u : 0u);
+    tc::cp_async16(sm.Sk + srow * kDim + scol, okr ? P.k + (t * P.Hqk + qh) * kDim + scol : P.k, okr ? 16u : 0u);
+    tc::cp_async16(sm.Sg + srow * kDim + scol, okr ? P.g + (t * P.Hv + h) * kDim + scol : P.g, okr ? 16u : 0u);
+    tc::cp_async_commit();
+    if (tid < kChunk)
+      nb = (tid < ntc) ? P.beta[(si.t0 + cc * kChunk + tid) * P.Hv + h] : __float2bfloat16_rn(0.f);
+  };
+  auto prefetch_late = [&](int64_t cc) {
+    const int ntc = rows_of(cc);
+    const bool okr = srow < ntc;
+    const int64_t t = si.t0 + cc * kChunk + srow;
+    tc::cp_async16(sm.dOp + srow * kDim + scol, okr ? a.d_o + (t * P.Hv + h) * kDim + scol : a.d_o, okr ? 16u : 0u);
+    const float* us = okr ? P.utape + (t * P.Hv + h) * kDim + scol : P.utape;
+    tc::cp_async16(sm.Up + srow * kLds + scol, us, okr ? 16u : 0u);
+    tc::cp_async16(sm.Up + srow * kLds + scol + 4, okr ? us + 4 : us, okr ? 16u : 0u);
+    if (tid < 128)
+      tc::cp_async16(&sm.As[0][0] + tid * 4, P.abtape + ((si.ch_base + cc) * P.Hv + h) * 512 + tid * 4, 16u);
+    tc::cp_async_commit();
+  };
+  auto prefetch_state = [&](int64_t cc) {
+    const float* src = P.ckpt + ((si.ck_base + cc / ck_every) * P.Hv + h) * kDim * kDim;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int f = tid + kThreads * i;
+      tc::cp_async16(sm.Gdv + f * 16, src + f * 4, 16u);
+    }
+    tc::cp_async_commit();
+  };
 
   // G^T <- dfinal_state^T
   {
@@ -130,6 +176,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     }
     tc::tmem_wait_st();
   }
+  prefetch_qkg(nchunks - 1);
+  prefetch_late(nchunks - 1);
+  prefetch_state(nchunks - 1);
 
   const int ti = tid >> 4;
   const int c8 = (tid & 15) * 8;
@@ -142,42 +191,21 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   for (int e = 0; e < 8; ++e) ddt_acc[e] = 0.f;
   float dA_acc = 0.f;
   float* cmb = reinterpret_cast<float*>(sm.Wt[0]);  // d q^, d k^, gauge / da tiles (after the MMAs)
+  const int ot = tid & 15, oq = tid >> 4;           // operand-tile mapping: token ot, quads oq, oq + 16
 
-  const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
-  const int ck_every = kCkTokens / kChunk;
   for (int64_t c = nchunks - 1; c >= 0; --c) {
     const int64_t tc0 = si.t0 + c * kChunk;
-    const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
-    // ---- P0: token tiles and prologue (token row ti, columns c8..c8+7)
-    float qhat[8], khat[8], zz[8], uu[8], rq, rk;
+    const int nt = rows_of(c);
+    tc::cp_async_wait_all();
+    __syncthreads();
+    // ---- P0: prologue (token row ti, columns c8..c8+7): L2 norm, gate, sigmoid beta
+    float qhat[8], khat[8], zz[8], rq, rk;
     {
       float qv[8], kv[8], gv[8];
-      uint4 draw = make_uint4(0u, 0u, 0u, 0u);
       const bool valid = ti < nt;
-      const int64_t t = tc0 + ti;
-      if (valid) {
-        load_bf16x8(P.q + (t * P.Hqk + qh) * kDim + c8, qv);
-        load_bf16x8(P.k + (t * P.Hqk + qh) * kDim + c8, kv);
-        load_bf16x8(P.g + (t * P.Hv + h) * kDim + c8, gv);
-        draw = *reinterpret_cast<const uint4*>(a.d_o + (t * P.Hv + h) * kDim + c8);
-        const float4 u0 = *reinterpret_cast<const float4*>(P.utape + (t * P.Hv + h) * kDim + c8);
-        const float4 u1 = *reinterpret_cast<const float4*>(P.utape + (t * P.Hv + h) * kDim + c8 + 4);
-        uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
-        uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] = kv[e] = gv[e] = uu[e] = 0.f;
-      }
-      float dv8[8];
-      {
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&draw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h2[e]);
-          dv8[2 * e] = f.x;
-          dv8[2 * e + 1] = f.y;
-        }
-      }
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sq + ti * kDim + c8), qv);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sk + ti * kDim + c8), kv);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sg + ti * kDim + c8), gv);
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
@@ -185,24 +213,30 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       sk = row16_sum(sk);
       rq = valid ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
       rk = valid ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+      float la[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         qhat[e] = qv[e] * rq;
         khat[e] = kv[e] * rk;
         zz[e] = ea * (gv[e] + dtb[e]);
-        sm.Pa[ti * kLds + c8 + e] = valid ? P.lb / (1.0f + expf(-zz[e])) : 0.f;
-        sm.Up[ti * kLds + c8 + e] = uu[e];
-        // dO is exact in TF32: it goes straight into both operand layouts
-        *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(c8 + e, ti, 32)) = dv8[e];
+        la[e] = valid ? P.lb / (1.0f + expf(-zz[e])) : 0.f;
       }
-      *reinterpret_cast<uint4*>(sm.dOp + ti * kDim + c8) = draw;
-      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ti, c8, kDim)) = make_float4(dv8[0], dv8[1], dv8[2], dv8[3]);
-      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ti, c8 + 4, kDim)) = make_float4(dv8[4], dv8[5], dv8[6], dv8[7]);
-      if (tid < kChunk)
-        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-__bfloat162float(P.beta[(tc0 + tid) * P.Hv + h]))) : 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int o = 4 * hh;
+        *reinterpret_cast<float4*>(sm.Qtp + ti * kLds + c8 + o) = make_float4(qhat[o], qhat[o + 1], qhat[o + 2], qhat[o + 3]);
+        *reinterpret_cast<float4*>(sm.Ktp + ti * kLds + c8 + o) = make_float4(khat[o], khat[o + 1], khat[o + 2], khat[o + 3]);
+        *reinterpret_cast<float4*>(sm.Pa + ti * kLds + c8 + o) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
+      }
+      if (tid < kChunk) {
+        const float bl = __bfloat162float(nb);
+        sm.braw[tid] = bl;
+        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-bl)) : 0.f;
+      }
     }
     __syncthreads();
-    // ---- P1: cumulative decay (one key column per thread)
+    // ---- P1: cumulative decay (one key column per thread); the next q, k, g are fetched meanwhile
+    if (c > 0) prefetch_qkg(c - 1);
     if (tid < kDim) {
       float G = 0.f;
 #pragma unroll
@@ -213,69 +247,89 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       sm.gC[tid] = expf(G);
     }
     __syncthreads();
-    // ---- P2a: operand tiles from q^, k^, gamma, u
-    {
-      const float bt = sm.bs[ti];
-      float kt[8], qt[8], ki[8], w[8];
+    // ---- P2a: operand tiles (token ot, quads oq and oq + 16)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float gam = sm.Pa[ti * kLds + c8 + e];
-        kt[e] = khat[e] * gam;
-        qt[e] = qhat[e] * gam;
-        ki[e] = khat[e] / gam;
-        w[e] = bt * uu[e];
-        sm.Ktp[ti * kLds + c8 + e] = kt[e];
-        sm.Qtp[ti * kLds + c8 + e] = qt[e];
-        sm.Kip[ti * kLds + c8 + e] = ki[e];
-        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(c8 + e, ti, 32)) = tc::round_tf32(s * qt[e]);
-        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(c8 + e, 16 + ti, 32)) = tc::round_tf32(-kt[e]);
+    for (int rep = 0; rep < 2; ++rep) {
+      const int k0 = 4 * (oq + 16 * rep);
+      const float4 qh4 = *reinterpret_cast<const float4*>(sm.Qtp + ot * kLds + k0);
+      const float4 kh4 = *reinterpret_cast<const float4*>(sm.Ktp + ot * kLds + k0);
+      const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + ot * kLds + k0);
+      const float4 u4 = *reinterpret_cast<const float4*>(sm.Up + ot * kLds + k0);
+      const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
+      const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ua[4] = {u4.x, u4.y, u4.z, u4.w};
+      const float bt = sm.bs[ot];
+      float kt[4], qt[4], ki[4], whi[4], wlo[4], dof[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kt[e] = ka[e] * ga[e];
+        qt[e] = qa[e] * ga[e];
+        ki[e] = ka[e] / ga[e];
+        const float w = bt * ua[e];
+        whi[e] = tc::round_tf32(w);
+        wlo[e] = tc::round_tf32(w - whi[e]);
+        dof[e] = __bfloat162float(sm.dOp[ot * kDim + k0 + e]);
       }
-#pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        const int o = 4 * hlf;
-        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(ti, c8 + o, kDim)) =
-            make_float4(tc::round_tf32(kt[o]), tc::round_tf32(kt[o + 1]), tc::round_tf32(kt[o + 2]),
-                        tc::round_tf32(kt[o + 3]));
-        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(16 + ti, c8 + o, kDim)) =
-            make_float4(tc::round_tf32(qt[o]), tc::round_tf32(qt[o + 1]), tc::round_tf32(qt[o + 2]),
-                        tc::round_tf32(qt[o + 3]));
-        *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ti, c8 + o, kDim)) =
-            make_float4(tc::round_tf32(ki[o]), tc::round_tf32(ki[o + 1]), tc::round_tf32(ki[o + 2]),
-                        tc::round_tf32(ki[o + 3]));
-        float whi[4], wlo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          whi[e] = tc::round_tf32(w[o + e]);
-          wlo[e] = tc::round_tf32(w[o + e] - whi[e]);
-        }
-        *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ti, c8 + o, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
-        *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ti, c8 + o, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
-      }
+      *reinterpret_cast<float4*>(sm.Ktp + ot * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
+      *reinterpret_cast<float4*>(sm.Qtp + ot * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
+      *reinterpret_cast<float4*>(sm.Kip + ot * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
+      *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ot, k0, kDim)) =
+          make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
+      *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ot, k0, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
+      *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ot, k0, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
+      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ot, k0, kDim)) = make_float4(dof[0], dof[1], dof[2], dof[3]);
     }
-    // ---- P2b: decay the adjoint (Gd = G diag(gamma_C)); S0 and Gd as TF32 operands
+    __syncthreads();
+    // ---- P2b: decay the adjoint (Gd = G diag(gamma_C)); S0 and Gd as TF32 operands (lane k)
     {
       const float gck = sm.gC[kl];
-      const float* s0 = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
       float racc = 0.f;
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         const int v0 = 64 * hv + 16 * q;
-        float g16[16], sv16[16], r16[16];
+        float g16[16], s16[16], r16[16];
         tc::tmem_ld16(tl + kColG + v0, g16);
 #pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          // lane quad (k0..k0+3) reads S0[v0 + 4b + j][k0..k0+3] and transposes
+          const float4 x4 = *reinterpret_cast<const float4*>(
+              sm.Gdv + (((kl >> 2) * 128 + v0 + 4 * b + (lane & 3)) * 16));
+          float x[4] = {x4.x, x4.y, x4.z, x4.w};
+          tc::quad_transpose(x, lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s16[4 * b + e] = x[e];
+        }
+#pragma unroll
         for (int j = 0; j < 16; ++j) {
-          sv16[j] = s0[(v0 + j) * kDim + kl];  // S0[v][k], coalesced over k
           g16[j] *= gck;
-          racc = fmaf(g16[j], sv16[j], racc);
+          racc = fmaf(g16[j], s16[j], racc);
+          r16[j] = tc::round_tf32(g16[j]);
+          s16[j] = tc::round_tf32(s16[j]);
         }
         tc::tmem_st16(tl + kColG + v0, g16);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r16[j] = tc::round_tf32(g16[j]);
         tc::tmem_st16(tl + kColGr + v0, r16);
+        tc::tmem_st16(tl + kColS + v0, s16);
+      }
+      sm.rho0[hv][kl] = racc;
+      // adjoint-update operand: row k, columns t (scale q^g for hv = 0, -k^g for hv = 1)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) sv16[j] = tc::round_tf32(sv16[j]);
-        tc::tmem_st16(tl + kColS + v0, sv16);
-        // Gd rows v for the A operand of Gd (k^/g)^T: transpose 4x4 blocks across lane quads
+      for (int a4 = 0; a4 < 4; ++a4) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * a4 + e;
+          x[e] = hv == 0 ? tc::round_tf32(s * sm.Qtp[t * kLds + kl]) : tc::round_tf32(-sm.Ktp[t * kLds + kl]);
+        }
+        *reinterpret_cast<float4*>(sm.QKT + tc::kmaj(kl, 16 * hv + 4 * a4, 32)) = make_float4(x[0], x[1], x[2], x[3]);
+      }
+      tc::tmem_wait_st();
+    }
+    __syncthreads();  // the staged S0 has been read
+    {
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int v0 = 64 * hv + 16 * q;
+        float r16[16];
+        tc::tmem_ld16(tl + kColGr + v0, r16);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           float x[4] = {r16[4 * b], r16[4 * b + 1], r16[4 * b + 2], r16[4 * b + 3]};
@@ -284,80 +338,28 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
               make_float4(x[0], x[1], x[2], x[3]);
         }
       }
-      sm.rho0[hv][kl] = racc;
-      tc::tmem_wait_st();
     }
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- MMA group 1: A/B, S0^T dO^T, Gd (k^/g)^T, Gd^T W^T
+    // ---- MMA group 1: Gd (k^/g)^T first (the dV chain needs it), then S0^T dO^T and Gd^T W^T
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t kq = tc::smem_u32(sm.KQ), ki = tc::smem_u32(sm.Ki), gdv = tc::smem_u32(sm.Gdv);
-      const uint32_t dou = tc::smem_u32(sm.dOU);
-      const uint32_t wt0 = tc::smem_u32(sm.Wt[0]), wt1 = tc::smem_u32(sm.Wt[1]);
-      const uint32_t i16 = tc::idesc_tf32(128, 16);
+      const uint32_t ki = tc::smem_u32(sm.Ki), gdv = tc::smem_u32(sm.Gdv);
+      const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
+      const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
+#pragma unroll 1
+      for (int st = 0; st < kDim / 8; ++st)
+        tc::mma_ss(tbase + kColDW, tc::kdesc(gdv, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
+      tc::mma_commit(mb0);
 #pragma unroll 1
       for (int st = 0; st < kDim / 8; ++st) {
-        tc::mma_ss(tbase + kColAB, tc::kdesc(kq, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
         tc::mma_ts(tbase + kColQ, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
-        tc::mma_ss(tbase + kColDW, tc::kdesc(gdv, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
-        tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt0, st, kDim), i16, st > 0);
-        tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt1, st, kDim), i16, 1);
+        tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
       }
-      tc::mma_commit(mbar);
+      tc::mma_commit(mb1);
     }
-    ok = ok && tc::mbar_wait(mbar, parity);
-    parity ^= 1;
-    tc::fence_after();
-    float dwk[16];
-    if (warp < 4) tc::tmem_ld16(tl + kColDW, dwk);
-    if (warp == 0) {
-      float r[16];
-      tc::tmem_ld16(tl + kColAB, r);
-      if (lane < 16) {
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) sm.As[lane][j] = (j < lane) ? r[j] : 0.f;
-      } else {
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) sm.Bs[lane - 16][j] = (j <= lane - 16) ? r[j] : 0.f;
-      }
-    }
-    tc::fence_before();
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-    // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials; warps 4-7: dO W^T
-    if (warp < 4) {
-      const int vv = kl;
-      float dw[kChunk], e[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        float acc = dwk[i];
-#pragma unroll
-        for (int j = i; j < kChunk; ++j) acc += s * sm.Bs[j][i] * __bfloat162float(sm.dOp[j * kDim + vv]);
-        dw[i] = acc;
-      }
-#pragma unroll
-      for (int i = kChunk - 1; i >= 0; --i) {
-        float acc = dw[i];
-#pragma unroll
-        for (int j = i + 1; j < kChunk; ++j) acc -= sm.As[j][i] * sm.bs[j] * e[j];
-        e[i] = acc;
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const float du = sm.bs[i] * e[i];
-        if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(du);
-        sm.DUp[i * kLds + vv] = du;
-        const float dhi = tc::round_tf32(du);
-        *reinterpret_cast<float*>(sm.dOU + tc::kmaj(16 + i, vv, kDim)) = dhi;
-        *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(vv, 16 + i, 32)) = dhi;
-        *reinterpret_cast<float*>(sm.dUlo + tc::kmaj(vv, i, kChunk)) = tc::round_tf32(du - dhi);
-        float pb = e[i] * sm.Up[i * kLds + vv];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, off);
-        if (lane == 0) sm.dbp[warp][i] = pb;
-      }
-    } else {
+    if (warp >= 4) {  // dO W^T with W = beta u, in FP32
       const int t2 = tid - 128;
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
@@ -369,7 +371,68 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         sm.M1[i][j] = acc * sm.bs[j];
       }
     }
+    ok = ok && tc::mbar_wait(mb0, par0);
+    par0 ^= 1;
+    tc::fence_after();
+    if (c > 0) prefetch_state(c - 1);  // Gdv has been read by the tensor core
+    // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
+    if (warp < 4) {
+      const int vv = kl;
+      float dwk[16];
+      tc::tmem_ld16(tl + kColDW, dwk);
+      float dof[kChunk], acc[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) dof[j] = __bfloat162float(sm.dOp[j * kDim + vv]);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        float x = dwk[i];
+#pragma unroll
+        for (int j = i; j < kChunk; ++j) x = fmaf(s * sm.Bs[j][i], dof[j], x);
+        acc[i] = x;
+      }
+      // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
+#pragma unroll
+      for (int i = kChunk - 1; i >= 0; --i) {
+        const float ei = acc[i];
+        const float du = sm.bs[i] * ei;
+        acc[i] = du;  // keep dV in place
+#pragma unroll
+        for (int m = 0; m < i; ++m) acc[m] = fmaf(-sm.As[i][m], du, acc[m]);
+        float pb = ei * sm.Up[i * kLds + vv];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, off);
+        if (lane == 0) sm.dbp[warp][i] = pb;
+      }
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(acc[i]);
+        sm.DUp[i * kLds + vv] = acc[i];
+      }
+#pragma unroll
+      for (int a4 = 0; a4 < 4; ++a4) {
+        float hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[e] = tc::round_tf32(acc[4 * a4 + e]);
+          lo[e] = tc::round_tf32(acc[4 * a4 + e] - hi[e]);
+        }
+        *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(vv, 4 * a4, 32)) =
+            make_float4(dof[4 * a4], dof[4 * a4 + 1], dof[4 * a4 + 2], dof[4 * a4 + 3]);
+        *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(vv, 16 + 4 * a4, 32)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<float4*>(sm.dUlo + tc::kmaj(vv, 4 * a4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    __syncthreads();
+    // dV rows of the S0^T dV^T operand (token ot, quads oq and oq + 16)
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int k0 = 4 * (oq + 16 * rep);
+      const float4 d4 = *reinterpret_cast<const float4*>(sm.DUp + ot * kLds + k0);
+      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(16 + ot, k0, kDim)) =
+          make_float4(tc::round_tf32(d4.x), tc::round_tf32(d4.y), tc::round_tf32(d4.z), tc::round_tf32(d4.w));
+    }
     tc::fence_async_smem();
+    tc::fence_before();
     __syncthreads();
     // ---- MMA group 2: S0^T dV^T and the adjoint update
     if (tid == 0) {
@@ -386,9 +449,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
       for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) times the dV lo part
         tc::mma_ss(tbase + kColG, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
-      tc::mma_commit(mbar);
+      tc::mma_commit(mb0);
     }
-    if (warp >= 4) {
+    if (warp >= 4) {  // dV W^T in FP32
       const int t2 = tid - 128;
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
@@ -401,19 +464,23 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     } else if (tid < kChunk) {
       sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
     }
-    ok = ok && tc::mbar_wait(mbar, parity);
-    parity ^= 1;
+    ok = ok && tc::mbar_wait(mb1, par1);
+    par1 ^= 1;
+    ok = ok && tc::mbar_wait(mb0, par0);
+    par0 ^= 1;
     tc::fence_after();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (c > 0) prefetch_late(c - 1);  // dO, u and A/B of this sub-chunk are no longer read
     // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows 8 hv .. 8 hv + 7)
     {
       float* dQh = cmb;
       float* dKh = cmb + kTileF;
       float* tv = cmb + 2 * kTileF;
-      float qd[16], rd[16], wg[16];
-      tc::tmem_ld16(tl + kColQ, qd);
-      tc::tmem_ld16(tl + kColR, rd);
-      tc::tmem_ld16(tl + kColWG, wg);
+      float qd[8], rd[8], wh[8], wl[8];
+      tc::tmem_ld8(tl + kColQ + 8 * hv, qd);
+      tc::tmem_ld8(tl + kColR + 8 * hv, rd);
+      tc::tmem_ld8(tl + kColWG + 8 * hv, wh);
+      tc::tmem_ld8(tl + kColWG + 16 + 8 * hv, wl);
       const int k = kl, i0 = 8 * hv;
       float rp = 0.f;
 #pragma unroll
@@ -421,8 +488,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         const int i = i0 + ii;
         const float gam = sm.Pa[i * kLds + k];
         const float inv = 1.0f / gam;
-        float pq = qd[i], pr = rd[i], pw = wg[i];
-        rp = fmaf(sm.Kip[i * kLds + k], wg[i], rp);
+        const float wg = wh[ii] + wl[ii];
+        float pq = qd[ii], pr = rd[ii], pw = wg;
+        rp = fmaf(sm.Kip[i * kLds + k], wg, rp);
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
           const float kij = sm.Kip[j * kLds + k];
@@ -498,14 +566,14 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         }
       }
       if (tid < nt) {
-        const float bl = __bfloat162float(P.beta[(tc0 + tid) * P.Hv + h]);
-        const float bn = 1.0f / (1.0f + expf(bl));  // sigmoid(-logit)
+        const float bn = 1.0f / (1.0f + expf(sm.braw[tid]));  // sigmoid(-logit)
         a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
       }
     }
     tc::fence_before();
-    __syncthreads();
   }
+  tc::cp_async_wait_all();
+  __syncthreads();
   if (!aborted) {
     // dinitial_state = G (stored transposed in TMEM)
     float* dst = a.dh0 + (n * P.Hv + h) * kDim * kDim;
@@ -520,7 +588,6 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     }
     // per-unit parameter-gradient partials, reduced in a fixed order
     float* red = sm.Qtp;  // [16 rows][128] + [256]: spans Qtp and Ktp
-    __syncthreads();
 #pragma unroll
     for (int e = 0; e < 8; ++e) red[ti * kDim + c8 + e] = ddt_acc[e];
     red[kChunk * kDim + tid] = dA_acc;

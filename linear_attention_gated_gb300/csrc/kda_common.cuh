@@ -19,7 +19,7 @@ struct SeqInfo {
   int64_t t0;       // first token of the sequence on the packed token axis
   int64_t len;      // tokens in the sequence (>= 1)
   int64_t ck_base;  // first checkpoint slot of the sequence
-  int64_t pad;
+  int64_t ch_base;  // first sub-chunk slot of the sequence (sub-chunk tapes)
 };
 
 struct Problem {
@@ -33,8 +33,11 @@ struct Problem {
   const float* h0;
   const int32_t* order;   // launch slot -> unit id (n * Hv + h), longest sequence first
   const SeqInfo* seq;     // [N]
-  float* ckpt;            // [n_ck, Hv, 128, 128] state at the start of every checkpoint interval
+  float* ckpt;            // [n_ck, Hv, 128 x 128] state at the start of every checkpoint interval,
+                          // element (v, k) at ckpt_index(v, k) (see below)
   float* utape;           // [Ttot, Hv, 128]: u_t = v_t - S'_t k^_t of every token (forward -> backward)
+  float* abtape;          // [n_sub_chunks, Hv, 2, 16, 16]: the FP32 A (strictly lower) and B (lower)
+                          // matrices of every sub-chunk (forward -> backward)
   int32_t* status;        // device status word: non-zero when a bounded device wait gave up
   int64_t N, Hqk, Hv;
   int32_t r;              // Hv / Hqk
@@ -61,7 +64,23 @@ struct BwdArgs {
 
 constexpr int kParStride = 132;
 
+// Position of state element (v, k) inside one saved checkpoint: key quads are
+// outermost, then the value row, then the 4 keys of the quad. The forward
+// (thread per value row) then writes 512 contiguous bytes per warp, and the
+// backward (thread per key) reads 16-byte runs.
+__host__ __device__ __forceinline__ int ckpt_index(int v, int k) { return ((k >> 2) * 128 + v) * 4 + (k & 3); }
+
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
+  const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h2[i]);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
 
 __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float* out) {
   uint4 raw = *reinterpret_cast<const uint4*>(p);

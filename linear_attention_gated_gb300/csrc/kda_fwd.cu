@@ -17,12 +17,15 @@
 // reading the library adopts).
 //
 // Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
-// three contractions: [k^ gamma; q^ gamma] (k^/gamma)^T (A and B, 16x16 each),
-// S0 [k^ gamma; q^ gamma]^T (128x32) and W^T (k^ gamma_C/gamma) (128x128).
+// two state-sized contractions S0 [k^ gamma; q^ gamma]^T (128x32) and
+// W^T (k^ gamma_C/gamma) (128x128); the 16x16 A and B run in FP32 on CUDA
+// cores while the first contraction is in flight. The next sub-chunk's token
+// tiles are prefetched into registers while the current one is processed.
 // Operands are rounded to TF32 when written to shared memory; the state update
 // uses split TF32 (x = hi + lo, three products) so that the carried state keeps
 // FP32-level accuracy. Accumulation, the triangular solve, the output and the
-// state stay FP32. Each token's u = v - S' k^ is saved for the backward. The gate, L2 norm
+// state stay FP32. Each token's u = v - S' k^ and each sub-chunk's A and B
+// are saved for the backward. The gate, L2 norm
 // and sigmoid of each token are computed on chip (the fused prologue). The
 // state at the start of every checkpoint interval is stored for the backward.
 #include "kda_common.cuh"
@@ -34,20 +37,18 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColAB = 0;    // [k^g; q^g] (k^/g)^T   : 16 columns, lanes 0..31 used
 constexpr uint32_t kColYO = 32;   // S0 [k^g; q^g]^T       : 32 columns
 constexpr uint32_t kColU = 128;   // W^T (k^ gC / g)       : 128 columns
 
 struct FwdSmem {
-  // Tensor-core operands. KQ must directly precede Sa: the A operand of the
-  // A/B product is 128 rows starting at KQ (rows 32..127 read Sa and are unused).
+  // Tensor-core operands.
   unsigned char KQ[32 * kDim * 4];      // rows 0..15 k^ gamma, rows 16..31 q^ gamma   (K-major, K = 128)
   unsigned char Sa[kDim * kDim * 4];    // chunk-start state, rows v                  (K-major, K = 128)
-  unsigned char Ki[kChunk * kDim * 4];  // k^ / gamma, rows t                          (K-major, K = 128)
   unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo parts (K = 16)
   unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo parts                     (K = 16)
-  float Pq[kTileF];                     // q^
-  float Pk[kTileF];                     // k^
+  float Pq[kTileF];                     // q^, then q^ gamma
+  float Pk[kTileF];                     // k^, then k^ gamma
+  float Pi[kTileF];                     // k^ / gamma
   float Pa[kTileF];                     // log decay, then gamma
   float Vs[kTileF];                     // v
   float As[kChunk][kChunk + 1];
@@ -101,29 +102,43 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
   const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
   const int ck_every = kCkTokens / kChunk;
   bool aborted = false;
+  // raw BF16 tiles of the next sub-chunk (token row ti, columns c8..c8+7)
+  uint4 nq = make_uint4(0u, 0u, 0u, 0u), nk = nq, ng = nq, nv = nq;
+  __nv_bfloat16 nb = __float2bfloat16_rn(0.f);
+  auto prefetch = [&](int64_t cc) {
+    const int64_t t = si.t0 + cc * kChunk + ti;
+    const bool ok_row = cc < nchunks && (cc * kChunk + ti) < si.len;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    nq = ok_row ? *reinterpret_cast<const uint4*>(P.q + (t * P.Hqk + qh) * kDim + c8) : z;
+    nk = ok_row ? *reinterpret_cast<const uint4*>(P.k + (t * P.Hqk + qh) * kDim + c8) : z;
+    ng = ok_row ? *reinterpret_cast<const uint4*>(P.g + (t * P.Hv + h) * kDim + c8) : z;
+    nv = ok_row ? *reinterpret_cast<const uint4*>(P.v + (t * P.Hv + h) * kDim + c8) : z;
+    if (tid < kChunk) {
+      const int64_t tb = si.t0 + cc * kChunk + tid;
+      nb = (cc < nchunks && (cc * kChunk + tid) < si.len) ? P.beta[tb * P.Hv + h] : __float2bfloat16_rn(0.f);
+    }
+  };
+  prefetch(0);
   for (int64_t c = 0; c < nchunks; ++c) {
     const int64_t tc0 = si.t0 + c * kChunk;
     const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
     if (c % ck_every == 0) {
-      float* dst = P.ckpt + (((si.ck_base + c / ck_every) * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
+      float* dst = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
 #pragma unroll
       for (int m = 0; m < 16; ++m)
-        *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+        *reinterpret_cast<float4*>(dst + ckpt_index(sv, 64 * ch + 4 * m)) =
+            make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
     }
     // ---- prologue: L2 norm, gate, sigmoid beta (token row ti, columns c8..c8+7)
     {
       float qv[8], kv[8], gv[8], vv[8];
       const bool valid = ti < nt;
-      if (valid) {
-        const int64_t t = tc0 + ti;
-        load_bf16x8(P.q + (t * P.Hqk + qh) * kDim + c8, qv);
-        load_bf16x8(P.k + (t * P.Hqk + qh) * kDim + c8, kv);
-        load_bf16x8(P.g + (t * P.Hv + h) * kDim + c8, gv);
-        load_bf16x8(P.v + (t * P.Hv + h) * kDim + c8, vv);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] = kv[e] = gv[e] = vv[e] = 0.f;
-      }
+      unpack_bf16x8(nq, qv);
+      unpack_bf16x8(nk, kv);
+      unpack_bf16x8(ng, gv);
+      unpack_bf16x8(nv, vv);
+      const float braw = __bfloat162float(nb);
+      prefetch(c + 1);
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
@@ -139,8 +154,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         sm.Pa[ti * kLds + c8 + e] = valid ? P.lb / (1.0f + expf(-z)) : 0.f;
         sm.Vs[ti * kLds + c8 + e] = vv[e];
       }
-      if (tid < kChunk)
-        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-__bfloat162float(P.beta[(tc0 + tid) * P.Hv + h]))) : 0.f;
+      if (tid < kChunk) sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-braw)) : 0.f;
     }
     // ---- chunk-start state as a TF32 operand
 #pragma unroll
@@ -178,33 +192,53 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float inv = 1.0f / ga[e];
-          kt[e] = tc::round_tf32(ka[e] * ga[e]);
-          qt[e] = tc::round_tf32(qa[e] * ga[e]);
-          ki[e] = tc::round_tf32(ka[e] * inv);
+          kt[e] = ka[e] * ga[e];
+          qt[e] = qa[e] * ga[e];
+          ki[e] = ka[e] * inv;
           const float kb = ka[e] * (ca[e] * inv);
           const float kb_hi = tc::round_tf32(kb);
           *reinterpret_cast<float*>(sm.KbT[0] + tc::kmaj(k0 + e, t, kChunk)) = kb_hi;
           *reinterpret_cast<float*>(sm.KbT[1] + tc::kmaj(k0 + e, t, kChunk)) = tc::round_tf32(kb - kb_hi);
         }
-        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(t, k0, kDim)) = make_float4(kt[0], kt[1], kt[2], kt[3]);
-        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(16 + t, k0, kDim)) = make_float4(qt[0], qt[1], qt[2], qt[3]);
-        *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(t, k0, kDim)) = make_float4(ki[0], ki[1], ki[2], ki[3]);
+        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(t, k0, kDim)) =
+            make_float4(tc::round_tf32(kt[0]), tc::round_tf32(kt[1]), tc::round_tf32(kt[2]), tc::round_tf32(kt[3]));
+        *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(16 + t, k0, kDim)) =
+            make_float4(tc::round_tf32(qt[0]), tc::round_tf32(qt[1]), tc::round_tf32(qt[2]), tc::round_tf32(qt[3]));
+        // plain FP32 copies for the 16x16 A and B (overwriting q^ / k^ of the same elements)
+        *reinterpret_cast<float4*>(sm.Pk + t * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
+        *reinterpret_cast<float4*>(sm.Pq + t * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
+        *reinterpret_cast<float4*>(sm.Pi + t * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
       }
     }
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- tensor cores: A/B matrices and S0 [k^g; q^g]^T
+    // ---- tensor cores: S0 [k^g; q^g]^T
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t kq = tc::smem_u32(sm.KQ), sa = tc::smem_u32(sm.Sa), ki = tc::smem_u32(sm.Ki);
-#pragma unroll 1
-      for (int s = 0; s < kDim / 8; ++s)
-        tc::mma_ss(tbase + kColAB, tc::kdesc(kq, s, kDim), tc::kdesc(ki, s, kDim), tc::idesc_tf32(128, 16), s > 0);
+      const uint32_t kq = tc::smem_u32(sm.KQ), sa = tc::smem_u32(sm.Sa);
 #pragma unroll 1
       for (int s = 0; s < kDim / 8; ++s)
         tc::mma_ss(tbase + kColYO, tc::kdesc(sa, s, kDim), tc::kdesc(kq, s, kDim), tc::idesc_tf32(128, 32), s > 0);
       tc::mma_commit(mbar);
+    }
+    // ---- meanwhile, A_ij = (k^g)_i . (k^/g)_j (j < i) and B_ij = (q^g)_i . (k^/g)_j (j <= i) in FP32
+    {
+      const int mat = tid >> 7, i = (tid & 127) >> 3, j0 = tid & 7;
+      const float* X = mat ? sm.Pq : sm.Pk;
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int j = j0 + 8 * rep;
+        float acc = 0.f;
+        if (j < i || (mat && j == i)) {
+#pragma unroll 8
+          for (int kk = 0; kk < kDim; kk += 4)
+            acc += dot4(*reinterpret_cast<const float4*>(X + i * kLds + kk),
+                        *reinterpret_cast<const float4*>(sm.Pi + j * kLds + kk));
+        }
+        (mat ? sm.Bs : sm.As)[i][j] = acc;
+        P.abtape[((si.ch_base + c) * P.Hv + h) * 512 + mat * 256 + i * 16 + j] = acc;  // for the backward
+      }
     }
     ok = ok && tc::mbar_wait(mbar, parity);
     parity ^= 1;
@@ -214,29 +248,21 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       tc::tmem_ld16(tbase + lane_off + kColYO, yp);
       tc::tmem_ld16(tbase + lane_off + kColYO + 16, op);
     }
-    if (warp == 0) {
-      float r[16];
-      tc::tmem_ld16(tbase + lane_off + kColAB, r);
-      if (lane < 16) {
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) sm.As[lane][j] = (j < lane) ? r[j] : 0.f;
-      } else {
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) sm.Bs[lane - 16][j] = (j <= lane - 16) ? r[j] : 0.f;
-      }
-    }
     tc::fence_before();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     // ---- W by forward substitution and the output (one state row per thread)
     if (warp < 4) {
-      float w[kChunk];
+      // right-looking substitution: once w_j is known it is removed from every
+      // later row, so the dependent chain is one FMA per token
+      float w[kChunk], acc[kChunk];
 #pragma unroll
-      for (int t = 0; t < kChunk; ++t) {
-        float acc = sm.Vs[t * kLds + sv] - yp[t];
+      for (int t = 0; t < kChunk; ++t) acc[t] = sm.Vs[t * kLds + sv] - yp[t];
 #pragma unroll
-        for (int j = 0; j < t; ++j) acc -= sm.As[t][j] * w[j];
-        w[t] = sm.bs[t] * acc;
-        if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc;  // u_t for the backward
+      for (int j = 0; j < kChunk; ++j) {
+        w[j] = sm.bs[j] * acc[j];
+        if (j < nt) P.utape[((tc0 + j) * P.Hv + h) * kDim + sv] = acc[j];  // u_j for the backward
+#pragma unroll
+        for (int t = j + 1; t < kChunk; ++t) acc[t] = fmaf(-sm.As[t][j], w[j], acc[t]);
       }
 #pragma unroll
       for (int t = 0; t < kChunk; ++t) {

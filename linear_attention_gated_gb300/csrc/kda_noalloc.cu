@@ -67,14 +67,15 @@ kda_status scratch_for_device(int dev, void** out) {
 __global__ void kda_noalloc_plan_kernel(const int64_t* cu, int64_t N, int64_t Hv, int64_t ck_tokens,
                                         int32_t* order, kda::SeqInfo* seq) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    int64_t ck = 0;
+    int64_t ck = 0, chn = 0;
     for (int64_t n = 0; n < N; ++n) {
       const int64_t len = cu[n + 1] - cu[n];
       seq[n].t0 = cu[n];
       seq[n].len = len;
       seq[n].ck_base = ck;
-      seq[n].pad = 0;
+      seq[n].ch_base = chn;
       ck += (len + ck_tokens - 1) / ck_tokens;
+      chn += (len + kda::kChunk - 1) / kda::kChunk;
     }
   }
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < N * Hv;
@@ -123,7 +124,7 @@ extern "C" kda_status kda_bwd_noalloc(
   if (B < 1 || T < 1 || Hqk < 1 || Hv < 1 || Hv % Hqk != 0)
     return nfail(KDA_ERR_INVALID_ARGUMENT, "need B, T >= 1 and Hv a positive multiple of Hqk");
   int64_t N = B;
-  int64_t n_ck = 0;
+  int64_t n_ck = 0, n_ch = 0;
   if (cu_seqlens_host) {
     if (B != 1 || num_seqs < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "packed input needs B == 1, num_seqs >= 1");
     N = num_seqs;
@@ -133,9 +134,11 @@ extern "C" kda_status kda_bwd_noalloc(
       const int64_t len = cu_seqlens_host[i + 1] - cu_seqlens_host[i];
       if (len < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "sequence %lld is empty", (long long)i);
       n_ck += (len + kda::kCkTokens - 1) / kda::kCkTokens;
+      n_ch += (len + kda::kChunk - 1) / kda::kChunk;
     }
   } else {
     n_ck = B * ((T + kda::kCkTokens - 1) / kda::kCkTokens);
+    n_ch = B * ((T + kda::kChunk - 1) / kda::kChunk);
   }
   const void* vec_ptrs[] = {q, k, v, g, h0, d_o, d_hT, dq, dk, dv, dg, dh0};
   for (const void* p : vec_ptrs)
@@ -150,6 +153,7 @@ extern "C" kda_status kda_bwd_noalloc(
   const size_t o_cu = off;    off = up(off + sizeof(int64_t) * (N + 1));
   const size_t o_ck = off;    off = up(off + sizeof(float) * (size_t)n_ck * Hv * D * D);
   const size_t o_ut = off;    off = up(off + sizeof(float) * (size_t)Ttot * Hv * D);
+  const size_t o_ab = off;    off = up(off + sizeof(float) * (size_t)n_ch * Hv * 2 * kda::kChunk * kda::kChunk);
   const size_t o_dqk = off;   if (r > 1) off = up(off + sizeof(float) * (size_t)Ttot * Hv * 2 * D);
   const size_t o_par = off;   off = up(off + sizeof(float) * (size_t)units * kda::kParStride);
   const size_t o_o = off;     off = up(off + sizeof(kda_bf16) * (size_t)Ttot * Hv * D);
@@ -214,6 +218,7 @@ extern "C" kda_status kda_bwd_noalloc(
   P.ckpt = reinterpret_cast<float*>(sc + o_ck);
   P.status = reinterpret_cast<int32_t*>(sc + o_status);
   P.utape = reinterpret_cast<float*>(sc + o_ut);
+  P.abtape = reinterpret_cast<float*>(sc + o_ab);
   P.N = N;
   P.Hqk = Hqk;
   P.Hv = Hv;
