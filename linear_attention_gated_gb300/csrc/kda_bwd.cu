@@ -47,7 +47,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTileF = kChunk * kLds;
-constexpr int kSq = kChunk + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // G^T, FP32 accumulator (lanes k, columns v)
 constexpr uint32_t kColGr = 128;  // Gd^T rounded to TF32 (A operand of Gd^T W^T)
@@ -79,10 +78,12 @@ struct BwdSmem {
   __nv_bfloat16 Sk[kChunk * kDim];
   __nv_bfloat16 Sg[kChunk * kDim];
   __nv_bfloat16 dOp[kChunk * kDim];
-  float As[kChunk][kChunk];               // A and B of the sub-chunk, from the forward (cp.async staging);
-  float Bs[kChunk][kChunk];               // As and Bs must stay contiguous
-  float M1[kChunk][kSq];                  // dO W^T
-  float M2[kChunk][kSq];                  // dV W^T
+  float As[kChunk][kChunk];               // A and B^T of the sub-chunk, from the forward (cp.async
+  float BsT[kChunk][kChunk];              // staging); As and BsT must stay contiguous
+  float M1[kChunk][kChunk];               // dO W^T
+  float M2[kChunk][kChunk];               // dV W^T
+  float M1T[kChunk][kChunk];
+  float M2T[kChunk][kChunk];
   float bs[kChunk];
   float braw[kChunk];
   float dba[kChunk];
@@ -238,13 +239,18 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     // ---- P1: cumulative decay (one key column per thread); the next q, k, g are fetched meanwhile
     if (c > 0) prefetch_qkg(c - 1);
     if (tid < kDim) {
+      float av[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) av[i] = sm.Pa[i * kLds + tid];
       float G = 0.f;
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        G += sm.Pa[i * kLds + tid];
-        sm.Pa[i * kLds + tid] = expf(G);
+        G += av[i];
+        av[i] = expf(G);
       }
-      sm.gC[tid] = expf(G);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
+      sm.gC[tid] = av[kChunk - 1];
     }
     __syncthreads();
     // ---- P2a: operand tiles (token ot, quads oq and oq + 16)
@@ -287,7 +293,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       for (int q = 0; q < 4; ++q) {
         const int v0 = 64 * hv + 16 * q;
         float g16[16], s16[16], r16[16];
-        tc::tmem_ld16(tl + kColG + v0, g16);
+        tc::tmem_ld16_nowait(tl + kColG + v0, g16);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           // lane quad (k0..k0+3) reads S0[v0 + 4b + j][k0..k0+3] and transposes
@@ -298,6 +304,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) s16[4 * b + e] = x[e];
         }
+        tc::tmem_wait_ld(g16);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           g16[j] *= gck;
@@ -365,10 +372,17 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       for (int rep = 0; rep < 2; ++rep) {
         const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
         float acc = 0.f;
-#pragma unroll 8
-        for (int vv = 0; vv < kDim; ++vv)
-          acc = fmaf(__bfloat162float(sm.dOp[i * kDim + vv]), sm.Up[j * kLds + vv], acc);
+#pragma unroll 4
+        for (int vv = 0; vv < kDim; vv += 8) {
+          float d8[8];
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.dOp + i * kDim + vv), d8);
+          const float4 u0 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv);
+          const float4 u1 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv + 4);
+          acc += d8[0] * u0.x + d8[1] * u0.y + d8[2] * u0.z + d8[3] * u0.w +
+                 d8[4] * u1.x + d8[5] * u1.y + d8[6] * u1.z + d8[7] * u1.w;
+        }
         sm.M1[i][j] = acc * sm.bs[j];
+        sm.M1T[j][i] = acc * sm.bs[j];
       }
     }
     ok = ok && tc::mbar_wait(mb0, par0);
@@ -380,15 +394,21 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       const int vv = kl;
       float dwk[16];
       tc::tmem_ld16(tl + kColDW, dwk);
-      float dof[kChunk], acc[kChunk];
+      float dof[kChunk], acc[kChunk], pbv[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) dof[j] = __bfloat162float(sm.dOp[j * kDim + vv]);
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        float x = dwk[i];
+        float brow[kChunk];  // B[j][i] for all j (zero for j < i)
 #pragma unroll
-        for (int j = i; j < kChunk; ++j) x = fmaf(s * sm.Bs[j][i], dof[j], x);
-        acc[i] = x;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.BsT[i][4 * q4]);
+          brow[4 * q4] = x.x; brow[4 * q4 + 1] = x.y; brow[4 * q4 + 2] = x.z; brow[4 * q4 + 3] = x.w;
+        }
+        float x = 0.f;
+#pragma unroll
+        for (int j = i; j < kChunk; ++j) x = fmaf(brow[j], dof[j], x);
+        acc[i] = fmaf(s, x, dwk[i]);
       }
       // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
 #pragma unroll
@@ -396,12 +416,40 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         const float ei = acc[i];
         const float du = sm.bs[i] * ei;
         acc[i] = du;  // keep dV in place
+        float arow[kChunk];
 #pragma unroll
-        for (int m = 0; m < i; ++m) acc[m] = fmaf(-sm.As[i][m], du, acc[m]);
-        float pb = ei * sm.Up[i * kLds + vv];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.As[i][4 * q4]);
+          arow[4 * q4] = x.x; arow[4 * q4 + 1] = x.y; arow[4 * q4 + 2] = x.z; arow[4 * q4 + 3] = x.w;
+        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, off);
-        if (lane == 0) sm.dbp[warp][i] = pb;
+        for (int m = 0; m < i; ++m) acc[m] = fmaf(-arow[m], du, acc[m]);
+        pbv[i] = ei * sm.Up[i * kLds + vv];
+      }
+      // dbeta partial sums over the warp's 32 value rows: halving butterfly
+      // (16 shuffles); lane l ends with the sum for token 8 b4 + 4 b3 + 2 b2 + b1
+      {
+        float y8[8], y4[4], y2[2];
+        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float send = b4 ? pbv[j] : pbv[j + 8], keep = b4 ? pbv[j + 8] : pbv[j];
+          y8[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float send = b3 ? y8[j] : y8[j + 4], keep = b3 ? y8[j + 4] : y8[j];
+          y4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float send = b2 ? y4[j] : y4[j + 2], keep = b2 ? y4[j + 2] : y4[j];
+          y2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        const float send = b1 ? y2[0] : y2[1], keep = b1 ? y2[1] : y2[0];
+        float y1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+        if ((lane & 1) == 0) sm.dbp[warp][(b4 ? 8 : 0) + (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0)] = y1;
       }
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
@@ -458,8 +506,11 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
         float acc = 0.f;
 #pragma unroll 8
-        for (int vv = 0; vv < kDim; ++vv) acc = fmaf(sm.DUp[i * kLds + vv], sm.Up[j * kLds + vv], acc);
+        for (int vv = 0; vv < kDim; vv += 4)
+          acc += dot4(*reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
+                      *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
         sm.M2[i][j] = acc * sm.bs[j];
+        sm.M2T[j][i] = acc * sm.bs[j];
       }
     } else if (tid < kChunk) {
       sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
@@ -482,29 +533,50 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::tmem_ld8(tl + kColWG + 8 * hv, wh);
       tc::tmem_ld8(tl + kColWG + 16 + 8 * hv, wl);
       const int k = kl, i0 = 8 * hv;
+      float kic[kChunk], qtc[kChunk], ktc[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        kic[j] = sm.Kip[j * kLds + k];
+        qtc[j] = sm.Qtp[j * kLds + k];
+        ktc[j] = sm.Ktp[j * kLds + k];
+      }
       float rp = 0.f;
 #pragma unroll
       for (int ii = 0; ii < 8; ++ii) {
+        // rows of this thread: i = i0 + ii (i0 is 0 or 8; the masks below compare with it)
         const int i = i0 + ii;
         const float gam = sm.Pa[i * kLds + k];
         const float inv = 1.0f / gam;
         const float wg = wh[ii] + wl[ii];
         float pq = qd[ii], pr = rd[ii], pw = wg;
-        rp = fmaf(sm.Kip[i * kLds + k], wg, rp);
+        float kii = 0.f, qti = 0.f, kti = 0.f;
+        float m1r[kChunk], m2r[kChunk], m1c[kChunk], m2c[kChunk];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(&sm.M1[i][4 * q4]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&sm.M2[i][4 * q4]);
+          const float4 c4 = *reinterpret_cast<const float4*>(&sm.M1T[i][4 * q4]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&sm.M2T[i][4 * q4]);
+          m1r[4 * q4] = a4.x; m1r[4 * q4 + 1] = a4.y; m1r[4 * q4 + 2] = a4.z; m1r[4 * q4 + 3] = a4.w;
+          m2r[4 * q4] = b4.x; m2r[4 * q4 + 1] = b4.y; m2r[4 * q4 + 2] = b4.z; m2r[4 * q4 + 3] = b4.w;
+          m1c[4 * q4] = c4.x; m1c[4 * q4 + 1] = c4.y; m1c[4 * q4 + 2] = c4.z; m1c[4 * q4 + 3] = c4.w;
+          m2c[4 * q4] = d4.x; m2c[4 * q4 + 1] = d4.y; m2c[4 * q4 + 2] = d4.z; m2c[4 * q4 + 3] = d4.w;
+        }
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          const float kij = sm.Kip[j * kLds + k];
-          if (j <= i) pq = fmaf(sm.M1[i][j], kij, pq);
-          if (j < i) pr = fmaf(sm.M2[i][j], kij, pr);
-          if (j >= i) pw = fmaf(s * sm.M1[j][i], sm.Qtp[j * kLds + k], pw);
-          if (j > i) pw = fmaf(-sm.M2[j][i], sm.Ktp[j * kLds + k], pw);
+          if (j == i) { kii = kic[j]; qti = qtc[j]; kti = ktc[j]; }
+          if (j <= i) pq = fmaf(m1r[j], kic[j], pq);
+          if (j < i) pr = fmaf(m2r[j], kic[j], pr);
+          if (j >= i) pw = fmaf(s * m1c[j], qtc[j], pw);
+          if (j > i) pw = fmaf(-m2c[j], ktc[j], pw);
         }
+        rp = fmaf(kii, wg, rp);
         const float dq_ = s * gam * pq;
         const float dkr = -gam * pr;
         const float dkw = inv * pw;
         dQh[i * kLds + k] = dq_;
         dKh[i * kLds + k] = dkr + dkw;
-        tv[i * kLds + k] = sm.Qtp[i * kLds + k] * inv * dq_ + sm.Ktp[i * kLds + k] * inv * (dkr - dkw);
+        tv[i * kLds + k] = qti * inv * dq_ + kti * inv * (dkr - dkw);
       }
       sm.rho2[hv][k] = rp;
     }
@@ -531,10 +603,10 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       float pq = 0.f, pk = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        // sigmoid'(z) = sigmoid(z) sigmoid(-z), both evaluated directly (no 1 - s cancellation)
-        const float sg = 1.0f / (1.0f + expf(-zz[e]));
-        const float sn = 1.0f / (1.0f + expf(zz[e]));
-        const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * sg * sn : 0.f;
+        // sigmoid'(z) = sigmoid(z) sigmoid(-z) = e / (1 + e)^2 with e = exp(-|z|) (no cancellation)
+        const float ex = expf(-fabsf(zz[e]));
+        const float den = 1.0f / (1.0f + ex);
+        const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * ex * den * den : 0.f;
         dg8[e] = dz * ea;
         ddt_acc[e] += dg8[e];
         dA_acc += dz * zz[e];

@@ -51,8 +51,8 @@ struct FwdSmem {
   float Pi[kTileF];                     // k^ / gamma
   float Pa[kTileF];                     // log decay, then gamma
   float Vs[kTileF];                     // v
-  float As[kChunk][kChunk + 1];
-  float Bs[kChunk][kChunk + 1];
+  float AsT[kChunk][kChunk];            // A transposed: AsT[j][t] = A[t][j]
+  float Bs[kChunk][kChunk];
   float bs[kChunk];
   float gC[kDim];
   unsigned long long mbar;
@@ -146,13 +146,21 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       sk = row16_sum(sk);
       const float rq = valid ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
       const float rk = valid ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+      float la[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float z = ea * (gv[e] + dtb[e]);
-        sm.Pq[ti * kLds + c8 + e] = qv[e] * rq;
-        sm.Pk[ti * kLds + c8 + e] = kv[e] * rk;
-        sm.Pa[ti * kLds + c8 + e] = valid ? P.lb / (1.0f + expf(-z)) : 0.f;
-        sm.Vs[ti * kLds + c8 + e] = vv[e];
+        qv[e] *= rq;
+        kv[e] *= rk;
+        la[e] = valid ? P.lb / (1.0f + expf(-z)) : 0.f;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int o = 4 * hh, col = ti * kLds + c8 + o;
+        *reinterpret_cast<float4*>(sm.Pq + col) = make_float4(qv[o], qv[o + 1], qv[o + 2], qv[o + 3]);
+        *reinterpret_cast<float4*>(sm.Pk + col) = make_float4(kv[o], kv[o + 1], kv[o + 2], kv[o + 3]);
+        *reinterpret_cast<float4*>(sm.Pa + col) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
+        *reinterpret_cast<float4*>(sm.Vs + col) = make_float4(vv[o], vv[o + 1], vv[o + 2], vv[o + 3]);
       }
       if (tid < kChunk) sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-braw)) : 0.f;
     }
@@ -167,13 +175,18 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     __syncthreads();
     // ---- cumulative decay along the sub-chunk (one key column per thread)
     if (tid < kDim) {
+      float av[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) av[i] = sm.Pa[i * kLds + tid];
       float G = 0.f;
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        G += sm.Pa[i * kLds + tid];
-        sm.Pa[i * kLds + tid] = expf(G);
+        G += av[i];
+        av[i] = expf(G);
       }
-      sm.gC[tid] = expf(G);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
+      sm.gC[tid] = av[kChunk - 1];
     }
     __syncthreads();
     // ---- operand tiles: token t, key quads q4 and q4 + 16
@@ -236,22 +249,21 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
             acc += dot4(*reinterpret_cast<const float4*>(X + i * kLds + kk),
                         *reinterpret_cast<const float4*>(sm.Pi + j * kLds + kk));
         }
-        (mat ? sm.Bs : sm.As)[i][j] = acc;
-        P.abtape[((si.ch_base + c) * P.Hv + h) * 512 + mat * 256 + i * 16 + j] = acc;  // for the backward
+        if (mat) sm.Bs[i][j] = acc; else sm.AsT[j][i] = acc;
+        // for the backward: A row-major, B transposed (its columns are read there)
+        P.abtape[((si.ch_base + c) * P.Hv + h) * 512 + (mat ? 256 + j * 16 + i : i * 16 + j)] = acc;
       }
     }
     ok = ok && tc::mbar_wait(mbar, parity);
     parity ^= 1;
     tc::fence_after();
-    float yp[16], op[16];
-    if (warp < 4) {
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
+    // ---- W by forward substitution and the output: both warps of a state row
+    // solve for W; each then writes half of the tokens and one TF32 part of W
+    {
+      float yp[16], op[16];
       tc::tmem_ld16(tbase + lane_off + kColYO, yp);
       tc::tmem_ld16(tbase + lane_off + kColYO + 16, op);
-    }
-    tc::fence_before();
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-    // ---- W by forward substitution and the output (one state row per thread)
-    if (warp < 4) {
       // right-looking substitution: once w_j is known it is removed from every
       // later row, so the dependent chain is one FMA per token
       float w[kChunk], acc[kChunk];
@@ -260,27 +272,39 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
         w[j] = sm.bs[j] * acc[j];
-        if (j < nt) P.utape[((tc0 + j) * P.Hv + h) * kDim + sv] = acc[j];  // u_j for the backward
+        if ((j >> 3) == ch && j < nt) P.utape[((tc0 + j) * P.Hv + h) * kDim + sv] = acc[j];  // u_j for the backward
+        float arow[kChunk];
 #pragma unroll
-        for (int t = j + 1; t < kChunk; ++t) acc[t] = fmaf(-sm.As[t][j], w[j], acc[t]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.AsT[j][4 * q4]);
+          arow[4 * q4] = x.x; arow[4 * q4 + 1] = x.y; arow[4 * q4 + 2] = x.z; arow[4 * q4 + 3] = x.w;
+        }
+#pragma unroll
+        for (int t = j + 1; t < kChunk; ++t) acc[t] = fmaf(-arow[t], w[j], acc[t]);
       }
 #pragma unroll
-      for (int t = 0; t < kChunk; ++t) {
-        float acc = op[t];
+      for (int tt = 0; tt < 8; ++tt) {
+        const int t = 8 * ch + tt;
+        float o = ch ? op[8 + tt] : op[tt];
+        float brow[kChunk];
 #pragma unroll
-        for (int j = 0; j <= t; ++j) acc += sm.Bs[t][j] * w[j];
-        if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * acc);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * q4]);
+          brow[4 * q4] = x.x; brow[4 * q4 + 1] = x.y; brow[4 * q4 + 2] = x.z; brow[4 * q4 + 3] = x.w;
+        }
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) o = fmaf(brow[j], w[j], o);  // B is zero above the diagonal
+        if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o);
       }
 #pragma unroll
       for (int t4 = 0; t4 < 4; ++t4) {
-        float hi[4], lo[4];
+        float x[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          hi[e] = tc::round_tf32(w[4 * t4 + e]);
-          lo[e] = tc::round_tf32(w[4 * t4 + e] - hi[e]);
+          const float hi = tc::round_tf32(w[4 * t4 + e]);
+          x[e] = ch == 0 ? hi : tc::round_tf32(w[4 * t4 + e] - hi);
         }
-        *reinterpret_cast<float4*>(sm.Wa[0] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<float4*>(sm.Wa[1] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<float4*>(sm.Wa[ch] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(x[0], x[1], x[2], x[3]);
       }
     }
     tc::fence_async_smem();
