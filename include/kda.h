@@ -157,7 +157,7 @@ const char* kda_last_error_message(void);
  * module is loaded until the process exits. A problem whose checkpoints and
  * intermediates exceed it is rejected with KDA_ERR_WORKSPACE_TOO_SMALL (use
  * kda_fwd + kda_bwd for it). With a checkpoint every kda_checkpoint_tokens()
- * = 16 tokens about 4.3 KiB per token-head (5.3 KiB when Hv > Hqk) plus 65 KiB
+ * = 16 tokens about 4.9 KiB per token-head (5.9 KiB when Hv > Hqk) plus 65 KiB
  * per (sequence, head) are needed: e.g. 1024 tokens x 12 heads with Hv = Hqk fit.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
