@@ -3,8 +3,8 @@
 //
 // One CTA owns one (sequence, value head) unit and walks its tokens in
 // sub-chunks of kChunk = 16, keeping the 128x128 FP32 value-first state in
-// registers (thread (warp w, lane l) owns row 32 (w % 4) + l, columns
-// [64 (w / 4), +64)). Within a sub-chunk starting from state S0, with Gam_i the
+// tensor memory (lane = value row), where it is also the accumulator of the
+// state update; two CTAs fit on one SM. Within a sub-chunk starting from state S0, with Gam_i the
 // cumulative log-decay of tokens 1..i (per key dim) and gamma_i = exp(Gam_i):
 //   A_ij = k^_i . (k^_j gamma_i / gamma_j)   (j < i)      B_ij likewise with q^_i (j <= i)
 //   Y    = V - (k^ gamma) S0^T
@@ -17,13 +17,15 @@
 // reading the library adopts).
 //
 // Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
-// two state-sized contractions S0 [k^ gamma; q^ gamma]^T (128x32) and
-// W^T (k^ gamma_C/gamma) (128x128); the 16x16 A and B run in FP32 on CUDA
-// cores while the first contraction is in flight. The next sub-chunk's token
-// tiles are prefetched into registers while the current one is processed.
-// Operands are rounded to TF32 when written to shared memory; the state update
-// uses split TF32 (x = hi + lo, three products) so that the carried state keeps
-// FP32-level accuracy. Accumulation, the triangular solve, the output and the
+// two state-sized contractions S0 [k^ gamma; q^ gamma]^T (128x32, the state as
+// the tensor-memory A operand) and W^T (k^ gamma_C/gamma) (128x128, added into
+// the state); the 16x16 A and B run in FP32 on CUDA cores while the first
+// contraction is in flight, and the next sub-chunk's prologue while the second
+// one is. Token tiles are prefetched into registers one sub-chunk ahead.
+// Operands written to shared memory are rounded to TF32; the state read as the
+// A operand is truncated to TF32 by the tensor core (it only feeds the sub-chunk's
+// Y and O); the state update uses split TF32 (x = hi + lo, three products) so
+// that the carried FP32 state keeps FP32-level accuracy. Accumulation, the triangular solve, the output and the
 // state stay FP32. Each token's u = v - S' k^ and each sub-chunk's A and B
 // are saved for the backward. The gate, L2 norm
 // and sigmoid of each token are computed on chip (the fused prologue). The
@@ -36,22 +38,20 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTileF = kChunk * kLds;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColYO = 32;   // S0 [k^g; q^g]^T       : 32 columns
-constexpr uint32_t kColU = 128;   // W^T (k^ gC / g)       : 128 columns
+constexpr uint32_t kTmemCols = 256;  // two CTAs per SM share the 512 columns
+constexpr uint32_t kColS = 0;        // FP32 state S (lane = value row v, column = key k)
+constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns
 
 struct FwdSmem {
-  // Tensor-core operands.
-  unsigned char KQ[32 * kDim * 4];      // rows 0..15 k^ gamma, rows 16..31 q^ gamma   (K-major, K = 128)
-  unsigned char Sa[kDim * kDim * 4];    // chunk-start state, rows v                  (K-major, K = 128)
-  unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo parts (K = 16)
-  unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo parts                     (K = 16)
-  float Pq[kTileF];                     // q^, then q^ gamma
-  float Pk[kTileF];                     // k^, then k^ gamma
-  float Pi[kTileF];                     // k^ / gamma
-  float Pa[kTileF];                     // log decay, then gamma
-  float Vs[kTileF];                     // v
-  float AsT[kChunk][kChunk];            // A transposed: AsT[j][t] = A[t][j]
+  unsigned char KQ[32 * kDim * 4];         // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128)
+  unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo (K = 16)
+  unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo                     (K = 16)
+  float Pq[kTileF];                        // q^, then q^ gamma
+  float Pk[kTileF];                        // k^, then k^ gamma
+  float Pi[kTileF];                        // k^ / gamma
+  float Pa[kTileF];                        // log decay, then gamma
+  float Vs[kTileF];                        // v
+  float AsT[kChunk][kChunk];               // A transposed: AsT[j][t] = A[t][j]
   float Bs[kChunk][kChunk];
   float bs[kChunk];
   float gC[kDim];
@@ -59,7 +59,7 @@ struct FwdSmem {
   uint32_t tmem_base;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 kda_fwd_kernel(const Problem P, const FwdOut out) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(smem_raw);
@@ -70,27 +70,35 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
   const int64_t qh = h / P.r;
   const SeqInfo si = P.seq[n];
 
-  const int sv = 32 * (warp & 3) + lane;  // state row owned by this thread
+  const int sv = 32 * (warp & 3) + lane;  // state row (TMEM lane) of this thread
   const int ch = warp >> 2;               // column half [64 ch, 64 ch + 64)
-  float S[64];
-  {
-    const float* src = P.h0 + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float4 x = *reinterpret_cast<const float4*>(src + 4 * m);
-      S[4 * m] = x.x; S[4 * m + 1] = x.y; S[4 * m + 2] = x.z; S[4 * m + 3] = x.w;
-    }
-  }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) tc::mbar_init(tc::smem_u32(&sm.mbar), 1);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = sm.tmem_base;
-  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
   const uint32_t mbar = tc::smem_u32(&sm.mbar);
   uint32_t parity = 0;
   bool ok = true;
+  bool aborted = false;
+
+  // S <- h0
+  {
+    const float* src = P.h0 + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      float x[16];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 y = *reinterpret_cast<const float4*>(src + 16 * q + 4 * m);
+        x[4 * m] = y.x; x[4 * m + 1] = y.y; x[4 * m + 2] = y.z; x[4 * m + 3] = y.w;
+      }
+      tc::tmem_st16(tl + kColS + 64 * ch + 16 * q, x);
+    }
+    tc::tmem_wait_st();
+  }
 
   const int ti = tid >> 4;
   const int c8 = (tid & 15) * 8;
@@ -101,7 +109,6 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 
   const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
   const int ck_every = kCkTokens / kChunk;
-  bool aborted = false;
   // raw BF16 tiles of the next sub-chunk (token row ti, columns c8..c8+7)
   uint4 nq = make_uint4(0u, 0u, 0u, 0u), nk = nq, ng = nq, nv = nq;
   __nv_bfloat16 nb = __float2bfloat16_rn(0.f);
@@ -118,27 +125,18 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       nb = (cc < nchunks && (cc * kChunk + tid) < si.len) ? P.beta[tb * P.Hv + h] : __float2bfloat16_rn(0.f);
     }
   };
-  prefetch(0);
-  for (int64_t c = 0; c < nchunks; ++c) {
-    const int64_t tc0 = si.t0 + c * kChunk;
-    const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
-    if (c % ck_every == 0) {
-      float* dst = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        *reinterpret_cast<float4*>(dst + ckpt_index(sv, 64 * ch + 4 * m)) =
-            make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
-    }
-    // ---- prologue: L2 norm, gate, sigmoid beta (token row ti, columns c8..c8+7)
+  // prologue and cumulative decay of sub-chunk cc (token tiles already prefetched)
+  auto prologue = [&](int64_t cc) {
+    const int ntc = (int)((si.len - cc * kChunk) < kChunk ? (si.len - cc * kChunk) : kChunk);
     {
       float qv[8], kv[8], gv[8], vv[8];
-      const bool valid = ti < nt;
+      const bool valid = ti < ntc;
       unpack_bf16x8(nq, qv);
       unpack_bf16x8(nk, kv);
       unpack_bf16x8(ng, gv);
       unpack_bf16x8(nv, vv);
       const float braw = __bfloat162float(nb);
-      prefetch(c + 1);
+      prefetch(cc + 1);
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
@@ -162,18 +160,9 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         *reinterpret_cast<float4*>(sm.Pa + col) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
         *reinterpret_cast<float4*>(sm.Vs + col) = make_float4(vv[o], vv[o + 1], vv[o + 2], vv[o + 3]);
       }
-      if (tid < kChunk) sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-braw)) : 0.f;
-    }
-    // ---- chunk-start state as a TF32 operand
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const int k = 64 * ch + 4 * m;
-      *reinterpret_cast<float4*>(sm.Sa + tc::kmaj(sv, k, kDim)) =
-          make_float4(tc::round_tf32(S[4 * m]), tc::round_tf32(S[4 * m + 1]), tc::round_tf32(S[4 * m + 2]),
-                      tc::round_tf32(S[4 * m + 3]));
+      if (tid < kChunk) sm.bs[tid] = (tid < ntc) ? 1.0f / (1.0f + expf(-braw)) : 0.f;
     }
     __syncthreads();
-    // ---- cumulative decay along the sub-chunk (one key column per thread)
     if (tid < kDim) {
       float av[kChunk];
 #pragma unroll
@@ -188,7 +177,14 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
       sm.gC[tid] = av[kChunk - 1];
     }
-    __syncthreads();
+  };
+
+  prefetch(0);
+  prologue(0);
+  for (int64_t c = 0; c < nchunks; ++c) {
+    const int64_t tc0 = si.t0 + c * kChunk;
+    const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
+    __syncthreads();  // prologue of this sub-chunk complete; the previous update's MMA has finished
     // ---- operand tiles: token t, key quads q4 and q4 + 16
     {
       const int t = tid & 15;
@@ -226,13 +222,13 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- tensor cores: S0 [k^g; q^g]^T
+    // ---- tensor cores: S0 [k^g; q^g]^T with the state read from tensor memory
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t kq = tc::smem_u32(sm.KQ), sa = tc::smem_u32(sm.Sa);
+      const uint32_t kq = tc::smem_u32(sm.KQ);
 #pragma unroll 1
-      for (int s = 0; s < kDim / 8; ++s)
-        tc::mma_ss(tbase + kColYO, tc::kdesc(sa, s, kDim), tc::kdesc(kq, s, kDim), tc::idesc_tf32(128, 32), s > 0);
+      for (int st = 0; st < kDim / 8; ++st)
+        tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, tc::kdesc(kq, st, kDim), tc::idesc_tf32(128, 32), st > 0);
       tc::mma_commit(mbar);
     }
     // ---- meanwhile, A_ij = (k^g)_i . (k^/g)_j (j < i) and B_ij = (q^g)_i . (k^/g)_j (j <= i) in FP32
@@ -258,12 +254,35 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     parity ^= 1;
     tc::fence_after();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
+    // ---- state checkpoint and decay S <- S0 diag(gamma_C) in tensor memory
+    {
+      const bool ck = (c % ck_every) == 0;
+      float* dst = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int col = 64 * ch + 16 * q;
+        float x[16];
+        tc::tmem_ld16(tl + kColS + col, x);
+        if (ck) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4*>(dst + ckpt_index(sv, col + 4 * m)) =
+                make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + col + 4 * m);
+          x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
+        }
+        tc::tmem_st16(tl + kColS + col, x);
+      }
+    }
     // ---- W by forward substitution and the output: both warps of a state row
     // solve for W; each then writes half of the tokens and one TF32 part of W
     {
       float yp[16], op[16];
-      tc::tmem_ld16(tbase + lane_off + kColYO, yp);
-      tc::tmem_ld16(tbase + lane_off + kColYO + 16, op);
+      tc::tmem_ld16(tl + kColYO, yp);
+      tc::tmem_ld16(tl + kColYO + 16, op);
       // right-looking substitution: once w_j is known it is removed from every
       // later row, so the dependent chain is one FMA per token
       float w[kChunk], acc[kChunk];
@@ -273,27 +292,28 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       for (int j = 0; j < kChunk; ++j) {
         w[j] = sm.bs[j] * acc[j];
         if ((j >> 3) == ch && j < nt) P.utape[((tc0 + j) * P.Hv + h) * kDim + sv] = acc[j];  // u_j for the backward
-        float arow[kChunk];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
+          if (4 * q4 + 3 <= j) continue;
           const float4 x = *reinterpret_cast<const float4*>(&sm.AsT[j][4 * q4]);
-          arow[4 * q4] = x.x; arow[4 * q4 + 1] = x.y; arow[4 * q4 + 2] = x.z; arow[4 * q4 + 3] = x.w;
-        }
+          const float ar[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int t = j + 1; t < kChunk; ++t) acc[t] = fmaf(-arow[t], w[j], acc[t]);
+          for (int e = 0; e < 4; ++e)
+            if (4 * q4 + e > j) acc[4 * q4 + e] = fmaf(-ar[e], w[j], acc[4 * q4 + e]);
+        }
       }
 #pragma unroll
       for (int tt = 0; tt < 8; ++tt) {
         const int t = 8 * ch + tt;
         float o = ch ? op[8 + tt] : op[tt];
-        float brow[kChunk];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const float4 x = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * q4]);
-          brow[4 * q4] = x.x; brow[4 * q4 + 1] = x.y; brow[4 * q4 + 2] = x.z; brow[4 * q4 + 3] = x.w;
+          o = fmaf(x.x, w[4 * q4], o);  // B is zero above the diagonal
+          o = fmaf(x.y, w[4 * q4 + 1], o);
+          o = fmaf(x.z, w[4 * q4 + 2], o);
+          o = fmaf(x.w, w[4 * q4 + 3], o);
         }
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) o = fmaf(brow[j], w[j], o);  // B is zero above the diagonal
         if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o);
       }
 #pragma unroll
@@ -307,10 +327,11 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         *reinterpret_cast<float4*>(sm.Wa[ch] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(x[0], x[1], x[2], x[3]);
       }
     }
+    tc::tmem_wait_st();
     tc::fence_async_smem();
+    tc::fence_before();
     __syncthreads();
-    // ---- tensor cores: rank-16 state update W^T (k^ gamma_C / gamma) in split TF32
-    // (hi hi + lo hi + hi lo: the state keeps FP32-level accuracy)
+    // ---- tensor cores: S += W^T (k^ gamma_C / gamma) in split TF32 (hi hi + lo hi + hi lo)
     if (tid == 0) {
       tc::fence_after();
       const uint32_t wa[2] = {tc::smem_u32(sm.Wa[0]), tc::smem_u32(sm.Wa[1])};
@@ -319,29 +340,28 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 #pragma unroll
       for (int p = 0; p < 3; ++p)
 #pragma unroll
-        for (int s = 0; s < kChunk / 8; ++s)
-          tc::mma_ss(tbase + kColU, tc::kdesc(wa[pa[p]], s, kChunk), tc::kdesc(kb[pb[p]], s, kChunk),
-                     tc::idesc_tf32(128, 128), (p | s) > 0);
+        for (int st = 0; st < kChunk / 8; ++st)
+          tc::mma_ss(tbase + kColS, tc::kdesc(wa[pa[p]], st, kChunk), tc::kdesc(kb[pb[p]], st, kChunk),
+                     tc::idesc_tf32(128, 128), 1);
       tc::mma_commit(mbar);
     }
+    // ---- meanwhile, the next sub-chunk's prologue (it touches no tensor-core operand)
+    if (c + 1 < nchunks) prologue(c + 1);
     ok = ok && tc::mbar_wait(mbar, parity);
     parity ^= 1;
     tc::fence_after();
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float u[16];
-      tc::tmem_ld16(tbase + lane_off + kColU + 64 * ch + 16 * q, u);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) S[16 * q + j] = fmaf(S[16 * q + j], sm.gC[64 * ch + 16 * q + j], u[j]);
-    }
-    tc::fence_before();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
   }
   if (!aborted) {
     float* dst = out.hT + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      float x[16];
+      tc::tmem_ld16(tl + kColS + 64 * ch + 16 * q, x);
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
-      *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(S[4 * m], S[4 * m + 1], S[4 * m + 2], S[4 * m + 3]);
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<float4*>(dst + 16 * q + 4 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+    }
   } else if (tid == 0) {
     atomicExch(P.status, 1);
   }
