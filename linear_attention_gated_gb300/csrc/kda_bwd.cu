@@ -350,21 +350,24 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     tc::fence_before();
     __syncthreads();
     // ---- MMA group 1: Gd (k^/g)^T first (the dV chain needs it), then S0^T dO^T and Gd^T W^T
-    if (tid == 0) {
-      tc::fence_after();
-      const uint32_t ki = tc::smem_u32(sm.Ki), gdv = tc::smem_u32(sm.Gdv);
-      const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
-      const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
-#pragma unroll 1
-      for (int st = 0; st < kDim / 8; ++st)
-        tc::mma_ss(tbase + kColDW, tc::kdesc(gdv, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
-      tc::mma_commit(mb0);
-#pragma unroll 1
-      for (int st = 0; st < kDim / 8; ++st) {
-        tc::mma_ts(tbase + kColQ, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
-        tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
+    if (warp == 0) {
+      if (tc::elect_one()) {
+        tc::fence_after();
+        const uint32_t ki = tc::smem_u32(sm.Ki), gdv = tc::smem_u32(sm.Gdv);
+        const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
+        const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
+#pragma unroll
+        for (int st = 0; st < kDim / 8; ++st)
+          tc::mma_ss(tbase + kColDW, tc::kdesc(gdv, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
+        tc::mma_commit(mb0);
+#pragma unroll
+        for (int st = 0; st < kDim / 8; ++st) {
+          tc::mma_ts(tbase + kColQ, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
+          tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
+        }
+        tc::mma_commit(mb1);
       }
-      tc::mma_commit(mb1);
+      __syncwarp();
     }
     if (warp >= 4) {  // dO W^T with W = beta u, in FP32
       const int t2 = tid - 128;
@@ -483,21 +486,24 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     tc::fence_before();
     __syncthreads();
     // ---- MMA group 2: S0^T dV^T and the adjoint update
-    if (tid == 0) {
-      tc::fence_after();
-      const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
-      const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
-      const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
-#pragma unroll 1
-      for (int st = 0; st < kDim / 8; ++st)
-        tc::mma_ts(tbase + kColR, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
+    if (warp == 0) {
+      if (tc::elect_one()) {
+        tc::fence_after();
+        const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
+        const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
+        const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
 #pragma unroll
-      for (int st = 0; st < 4; ++st)
-        tc::mma_ss(tbase + kColG, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
+        for (int st = 0; st < kDim / 8; ++st)
+          tc::mma_ts(tbase + kColR, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
 #pragma unroll
-      for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) times the dV lo part
-        tc::mma_ss(tbase + kColG, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
-      tc::mma_commit(mb0);
+        for (int st = 0; st < 4; ++st)
+          tc::mma_ss(tbase + kColG, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
+#pragma unroll
+        for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) times the dV lo part
+          tc::mma_ss(tbase + kColG, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
+        tc::mma_commit(mb0);
+      }
+      __syncwarp();
     }
     if (warp >= 4) {  // dV W^T in FP32
       const int t2 = tid - 128;

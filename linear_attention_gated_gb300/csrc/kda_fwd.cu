@@ -223,13 +223,16 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     tc::fence_before();
     __syncthreads();
     // ---- tensor cores: S0 [k^g; q^g]^T with the state read from tensor memory
-    if (tid == 0) {
-      tc::fence_after();
-      const uint32_t kq = tc::smem_u32(sm.KQ);
-#pragma unroll 1
-      for (int st = 0; st < kDim / 8; ++st)
-        tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, tc::kdesc(kq, st, kDim), tc::idesc_tf32(128, 32), st > 0);
-      tc::mma_commit(mbar);
+    if (warp == 0) {
+      if (tc::elect_one()) {
+        tc::fence_after();
+        const uint32_t kq = tc::smem_u32(sm.KQ);
+#pragma unroll
+        for (int st = 0; st < kDim / 8; ++st)
+          tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, tc::kdesc(kq, st, kDim), tc::idesc_tf32(128, 32), st > 0);
+        tc::mma_commit(mbar);
+      }
+      __syncwarp();
     }
     // ---- meanwhile, A_ij = (k^g)_i . (k^/g)_j (j < i) and B_ij = (q^g)_i . (k^/g)_j (j <= i) in FP32
     {
@@ -332,18 +335,21 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     tc::fence_before();
     __syncthreads();
     // ---- tensor cores: S += W^T (k^ gamma_C / gamma) in split TF32 (hi hi + lo hi + hi lo)
-    if (tid == 0) {
-      tc::fence_after();
-      const uint32_t wa[2] = {tc::smem_u32(sm.Wa[0]), tc::smem_u32(sm.Wa[1])};
-      const uint32_t kb[2] = {tc::smem_u32(sm.KbT[0]), tc::smem_u32(sm.KbT[1])};
-      const int pa[3] = {0, 1, 0}, pb[3] = {0, 0, 1};
+    if (warp == 0) {
+      if (tc::elect_one()) {
+        tc::fence_after();
+        const uint32_t wa[2] = {tc::smem_u32(sm.Wa[0]), tc::smem_u32(sm.Wa[1])};
+        const uint32_t kb[2] = {tc::smem_u32(sm.KbT[0]), tc::smem_u32(sm.KbT[1])};
+        const int pa[3] = {0, 1, 0}, pb[3] = {0, 0, 1};
 #pragma unroll
-      for (int p = 0; p < 3; ++p)
+        for (int p = 0; p < 3; ++p)
 #pragma unroll
-        for (int st = 0; st < kChunk / 8; ++st)
-          tc::mma_ss(tbase + kColS, tc::kdesc(wa[pa[p]], st, kChunk), tc::kdesc(kb[pb[p]], st, kChunk),
-                     tc::idesc_tf32(128, 128), 1);
-      tc::mma_commit(mbar);
+          for (int st = 0; st < kChunk / 8; ++st)
+            tc::mma_ss(tbase + kColS, tc::kdesc(wa[pa[p]], st, kChunk), tc::kdesc(kb[pb[p]], st, kChunk),
+                       tc::idesc_tf32(128, 128), 1);
+        tc::mma_commit(mbar);
+      }
+      __syncwarp();
     }
     // ---- meanwhile, the next sub-chunk's prologue (it touches no tensor-core operand)
     if (c + 1 < nchunks) prologue(c + 1);
