@@ -3,8 +3,10 @@
 //
 // One CTA owns one (sequence, value head) unit. It walks the unit's sub-chunks
 // from last to first, carrying the state adjoint G = dL/dS as an FP32
-// accumulator in tensor memory, stored transposed (lane = key dim k, column =
-// value dim v). Per sub-chunk it reads the chunk-start state S0 saved by the
+// accumulator in tensor memory twice, as G (lane = value dim v) and as G^T
+// (lane = key dim k): both receive the same rank-32 update, and each is the
+// tensor-memory A operand of the products that contract over its columns.
+// Per sub-chunk it reads the chunk-start state S0 saved by the
 // forward and the forward's per-token u = v - S' k^ (so W = diag(beta) U is
 // never recomputed), and with Gd = G diag(gamma_C) (the adjoint moved to the
 // decayed end state):
@@ -28,9 +30,15 @@
 // sub-chunks (a running sum over the whole sequence drifts in FP32).
 //
 // Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
-// state-sized contractions S0^T [dO; dV]^T, Gd (k^/g)^T, Gd^T W^T (W split into
-// TF32 hi + lo) and the rank-32 adjoint update (dV split into hi + lo; dO is
-// exact in TF32). The forward's FP32 A and B of each sub-chunk are reused. The
+// state-sized contractions G (k^ gamma_C/gamma)^T (= Gd (k^/g)^T, the decay
+// folded into the operand), S0^T [dO; dV]^T, G^T W^T (W split into TF32 hi +
+// lo; scaled by gamma_C per key afterwards) and the rank-32 adjoint update (dV
+// split into hi + lo; dO is exact in TF32). The forward saves S0 transposed,
+// so the staged checkpoint is itself the shared-memory A operand S0^T; it is
+// rounded to TF32 in place after sum_v G * S0 has been taken from it in FP32.
+// G is read by the tensor core at TF32 (truncated); G^T W^T adds the product
+// of G^T's truncated-away low part, so it is split TF32 on both sides. The decay
+// G <- Gd runs on warps 4-7 while warps 0-3 solve for dV. The forward's FP32 A and B of each sub-chunk are reused. The
 // next sub-chunk's token tiles, u, A/B and state checkpoint are prefetched with
 // cp.async into buffers freed earlier in the current sub-chunk. The 16x16 intra-chunk
 // products, the substitutions and the combination run in FP32 on CUDA cores:
@@ -48,19 +56,20 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0;     // G^T, FP32 accumulator (lanes k, columns v)
-constexpr uint32_t kColGr = 128;  // Gd^T rounded to TF32 (A operand of Gd^T W^T)
-constexpr uint32_t kColS = 256;   // S0^T rounded to TF32 (A operand of S0^T [dO; dV]^T)
-constexpr uint32_t kColDW = 384;  // Gd (k^/g)^T : lanes v, 16 columns
+constexpr uint32_t kColG = 0;     // G, FP32 accumulator (lanes v, columns k)
+constexpr uint32_t kColGT = 128;  // G^T, the same adjoint transposed (lanes k, columns v)
+constexpr uint32_t kColGL = 256;  // G^T minus its TF32 truncation (the part the tensor core drops)
+constexpr uint32_t kColDW = 384;  // G (k^ gamma_C / gamma)^T : lanes v, 16 columns
 constexpr uint32_t kColQ = 400;   // S0^T dO^T : lanes k, 16 columns
 constexpr uint32_t kColR = 416;   // S0^T dV^T : lanes k, 16 columns
-constexpr uint32_t kColWG = 432;  // Gd^T [W_hi; W_lo]^T : lanes k, 32 columns
+constexpr uint32_t kColWG = 432;  // G^T [W_hi; W_lo]^T : lanes k, 32 columns
 
 struct BwdSmem {
-  // Gd rows v for the A operand of Gd (k^/g)^T. Once that product has been
-  // read, the region stages the next sub-chunk's state checkpoint (cp.async).
-  unsigned char Gdv[kDim * kDim * 4];     // (K-major, K = 128)
-  unsigned char Ki[kChunk * kDim * 4];    // k^ / gamma rows t                  (K-major, K = 128)
+  // chunk-start state as saved (ckpt_index layout, cp.async staging): S0^T,
+  // the K-major A operand (rows k, K = v) of S0^T dO^T and S0^T dV^T once
+  // rounded to TF32 in place
+  unsigned char S0s[kDim * kDim * 4];
+  unsigned char Kb[kChunk * kDim * 4];    // k^ gamma_C / gamma rows t          (K-major, K = 128)
   // Wt and dOU are contiguous: after the second MMA group they hold the
   // combination tiles (d q^, d k^, gauge term).
   unsigned char Wt[2][kChunk * kDim * 4]; // W rows t, TF32 hi then lo (one N = 32 operand)
@@ -88,10 +97,10 @@ struct BwdSmem {
   float braw[kChunk];
   float dba[kChunk];
   float gC[kDim];
-  float rho0[2][kDim];                    // halves of sum_v Gd * S0
+  float rho0[2][kDim];                    // halves of sum_v G * S0 (before the decay factor)
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
   float dbp[4][kChunk];                   // per-warp partial dbeta
-  unsigned long long mbar[2];
+  unsigned long long mbar[3];
   uint32_t tmem_base;
 };
 
@@ -112,16 +121,17 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) {
-    tc::mbar_init(tc::smem_u32(&sm.mbar[0]), 1);
-    tc::mbar_init(tc::smem_u32(&sm.mbar[1]), 1);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), 1);
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = sm.tmem_base;
   const uint32_t tl = tbase + lane_off;
-  const uint32_t mb0 = tc::smem_u32(&sm.mbar[0]), mb1 = tc::smem_u32(&sm.mbar[1]);
-  uint32_t par0 = 0, par1 = 0;
+  const uint32_t mbD = tc::smem_u32(&sm.mbar[0]), mb1 = tc::smem_u32(&sm.mbar[1]);
+  const uint32_t mb2 = tc::smem_u32(&sm.mbar[2]);
+  uint32_t ph = 0;  // every barrier completes once per sub-chunk
   bool ok = true;
   bool aborted = false;
 
@@ -159,21 +169,27 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int f = tid + kThreads * i;
-      tc::cp_async16(sm.Gdv + f * 16, src + f * 4, 16u);
+      tc::cp_async16(sm.S0s + f * 16, src + f * 4, 16u);
     }
     tc::cp_async_commit();
   };
 
-  // G^T <- dfinal_state^T
+  // G <- dfinal_state (lanes v) and G^T (lanes k)
   {
     const float* src = a.d_hT + (n * P.Hv + h) * kDim * kDim;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
-      const int v0 = 64 * hv + 16 * q;
+      const int c0 = 64 * hv + 16 * q;
       float x[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) x[j] = src[(v0 + j) * kDim + kl];
-      tc::tmem_st16(tl + kColG + v0, x);
+      for (int j = 0; j < 16; ++j) x[j] = src[(c0 + j) * kDim + kl];
+      tc::tmem_st16(tl + kColGT + c0, x);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 y = *reinterpret_cast<const float4*>(src + kl * kDim + c0 + 4 * m);
+        x[4 * m] = y.x; x[4 * m + 1] = y.y; x[4 * m + 2] = y.z; x[4 * m + 3] = y.w;
+      }
+      tc::tmem_st16(tl + kColG + c0, x);
     }
     tc::tmem_wait_st();
   }
@@ -199,6 +215,39 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     const int nt = rows_of(c);
     tc::cp_async_wait_all();
     __syncthreads();
+    // ---- sum_v G * S0 from the FP32 checkpoint (lane k, values of half hv; the
+    // decay factor gamma_C is applied in P8), then S0 rounded to TF32 in place
+    // for the tensor core (the products below see it rounded, not truncated),
+    // and the low part of G^T for the split G^T W^T
+    {
+      float racc = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int v0 = 64 * hv + 16 * q;
+        float g16[16];
+        tc::tmem_ld16_nowait(tl + kColGT + v0, g16);
+        float4 s4[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) s4[b] = *reinterpret_cast<const float4*>(sm.S0s + ckpt_index(v0 + 4 * b, kl) * 4);
+        tc::tmem_wait_ld(g16);
+        float lo16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) lo16[j] = g16[j] - __uint_as_float(__float_as_uint(g16[j]) & 0xFFFFE000u);
+        tc::tmem_st16(tl + kColGL + v0, lo16);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          racc = fmaf(g16[4 * b], s4[b].x, racc);
+          racc = fmaf(g16[4 * b + 1], s4[b].y, racc);
+          racc = fmaf(g16[4 * b + 2], s4[b].z, racc);
+          racc = fmaf(g16[4 * b + 3], s4[b].w, racc);
+          *reinterpret_cast<float4*>(sm.S0s + ckpt_index(v0 + 4 * b, kl) * 4) =
+              make_float4(tc::round_tf32(s4[b].x), tc::round_tf32(s4[b].y), tc::round_tf32(s4[b].z),
+                          tc::round_tf32(s4[b].w));
+        }
+      }
+      sm.rho0[hv][kl] = racc;
+      tc::tmem_wait_st();
+    }
     // ---- P0: prologue (token row ti, columns c8..c8+7): L2 norm, gate, sigmoid beta
     float qhat[8], khat[8], zz[8], rq, rk;
     {
@@ -253,7 +302,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       sm.gC[tid] = av[kChunk - 1];
     }
     __syncthreads();
-    // ---- P2a: operand tiles (token ot, quads oq and oq + 16)
+    // ---- P2: operand tiles (token ot, quads oq and oq + 16)
 #pragma unroll
     for (int rep = 0; rep < 2; ++rep) {
       const int k0 = 4 * (oq + 16 * rep);
@@ -261,139 +310,112 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       const float4 kh4 = *reinterpret_cast<const float4*>(sm.Ktp + ot * kLds + k0);
       const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + ot * kLds + k0);
       const float4 u4 = *reinterpret_cast<const float4*>(sm.Up + ot * kLds + k0);
+      const float4 c4 = *reinterpret_cast<const float4*>(sm.gC + k0);
       const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
       const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ua[4] = {u4.x, u4.y, u4.z, u4.w};
+      const float ca[4] = {c4.x, c4.y, c4.z, c4.w};
       const float bt = sm.bs[ot];
-      float kt[4], qt[4], ki[4], whi[4], wlo[4], dof[4];
+      float kt[4], qt[4], ki[4], kb[4], whi[4], wlo[4], dof[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
+        const float inv = 1.0f / ga[e];
         kt[e] = ka[e] * ga[e];
         qt[e] = qa[e] * ga[e];
-        ki[e] = ka[e] / ga[e];
+        ki[e] = ka[e] * inv;
+        kb[e] = tc::round_tf32(ka[e] * (ca[e] * inv));
         const float w = bt * ua[e];
         whi[e] = tc::round_tf32(w);
         wlo[e] = tc::round_tf32(w - whi[e]);
         dof[e] = __bfloat162float(sm.dOp[ot * kDim + k0 + e]);
+        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, ot, 32)) = tc::round_tf32(s * qt[e]);
+        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, 16 + ot, 32)) = tc::round_tf32(-kt[e]);
       }
       *reinterpret_cast<float4*>(sm.Ktp + ot * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
       *reinterpret_cast<float4*>(sm.Qtp + ot * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
       *reinterpret_cast<float4*>(sm.Kip + ot * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
-      *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ot, k0, kDim)) =
-          make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
+      *reinterpret_cast<float4*>(sm.Kb + tc::kmaj(ot, k0, kDim)) = make_float4(kb[0], kb[1], kb[2], kb[3]);
       *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ot, k0, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
       *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ot, k0, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
       *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ot, k0, kDim)) = make_float4(dof[0], dof[1], dof[2], dof[3]);
     }
-    __syncthreads();
-    // ---- P2b: decay the adjoint (Gd = G diag(gamma_C)); S0 and Gd as TF32 operands (lane k)
-    {
-      const float gck = sm.gC[kl];
-      float racc = 0.f;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const int v0 = 64 * hv + 16 * q;
-        float g16[16], s16[16], r16[16];
-        tc::tmem_ld16_nowait(tl + kColG + v0, g16);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          // lane quad (k0..k0+3) reads S0[v0 + 4b + j][k0..k0+3] and transposes
-          const float4 x4 = *reinterpret_cast<const float4*>(
-              sm.Gdv + (((kl >> 2) * 128 + v0 + 4 * b + (lane & 3)) * 16));
-          float x[4] = {x4.x, x4.y, x4.z, x4.w};
-          tc::quad_transpose(x, lane);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s16[4 * b + e] = x[e];
-        }
-        tc::tmem_wait_ld(g16);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          g16[j] *= gck;
-          racc = fmaf(g16[j], s16[j], racc);
-          r16[j] = tc::round_tf32(g16[j]);
-          s16[j] = tc::round_tf32(s16[j]);
-        }
-        tc::tmem_st16(tl + kColG + v0, g16);
-        tc::tmem_st16(tl + kColGr + v0, r16);
-        tc::tmem_st16(tl + kColS + v0, s16);
-      }
-      sm.rho0[hv][kl] = racc;
-      // adjoint-update operand: row k, columns t (scale q^g for hv = 0, -k^g for hv = 1)
-#pragma unroll
-      for (int a4 = 0; a4 < 4; ++a4) {
-        float x[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 4 * a4 + e;
-          x[e] = hv == 0 ? tc::round_tf32(s * sm.Qtp[t * kLds + kl]) : tc::round_tf32(-sm.Ktp[t * kLds + kl]);
-        }
-        *reinterpret_cast<float4*>(sm.QKT + tc::kmaj(kl, 16 * hv + 4 * a4, 32)) = make_float4(x[0], x[1], x[2], x[3]);
-      }
-      tc::tmem_wait_st();
-    }
-    __syncthreads();  // the staged S0 has been read
-    {
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const int v0 = 64 * hv + 16 * q;
-        float r16[16];
-        tc::tmem_ld16(tl + kColGr + v0, r16);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float x[4] = {r16[4 * b], r16[4 * b + 1], r16[4 * b + 2], r16[4 * b + 3]};
-          tc::quad_transpose(x, lane);
-          *reinterpret_cast<float4*>(sm.Gdv + tc::kmaj(v0 + 4 * b + (lane & 3), kl & ~3, kDim)) =
-              make_float4(x[0], x[1], x[2], x[3]);
-        }
-      }
-    }
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- MMA group 1: Gd (k^/g)^T first (the dV chain needs it), then S0^T dO^T and Gd^T W^T
+    // ---- MMA group 1: G Kb^T first (the dV chain needs it), then S0^T dO^T and G^T W^T
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
-        const uint32_t ki = tc::smem_u32(sm.Ki), gdv = tc::smem_u32(sm.Gdv);
+        const uint32_t kb = tc::smem_u32(sm.Kb), s0 = tc::smem_u32(sm.S0s);
         const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
         const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ss(tbase + kColDW, tc::kdesc(gdv, st, kDim), tc::kdesc(ki, st, kDim), i16, st > 0);
-        tc::mma_commit(mb0);
+          tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, tc::kdesc(kb, st, kDim), i16, st > 0);
+        tc::mma_commit(mbD);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st) {
-          tc::mma_ts(tbase + kColQ, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
-          tc::mma_ts(tbase + kColWG, tbase + kColGr + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
+          tc::mma_ss(tbase + kColQ, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
+                     st > 0);
+          tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
         }
+#pragma unroll
+        for (int st = 0; st < kDim / 8; ++st)  // the low part of G^T with [W_hi; W_lo]
+          tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
         tc::mma_commit(mb1);
       }
       __syncwarp();
     }
-    if (warp >= 4) {  // dO W^T with W = beta u, in FP32
-      const int t2 = tid - 128;
+    if (warp >= 4) {
+      // dO W^T with W = beta u, in FP32
+      {
+        const int t2 = tid - 128;
 #pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
-        float acc = 0.f;
+        for (int rep = 0; rep < 2; ++rep) {
+          const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
+          float acc = 0.f;
 #pragma unroll 4
-        for (int vv = 0; vv < kDim; vv += 8) {
-          float d8[8];
-          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.dOp + i * kDim + vv), d8);
-          const float4 u0 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv);
-          const float4 u1 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv + 4);
-          acc += d8[0] * u0.x + d8[1] * u0.y + d8[2] * u0.z + d8[3] * u0.w +
-                 d8[4] * u1.x + d8[5] * u1.y + d8[6] * u1.z + d8[7] * u1.w;
+          for (int vv = 0; vv < kDim; vv += 8) {
+            float d8[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.dOp + i * kDim + vv), d8);
+            const float4 u0 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv);
+            const float4 u1 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv + 4);
+            acc += d8[0] * u0.x + d8[1] * u0.y + d8[2] * u0.z + d8[3] * u0.w +
+                   d8[4] * u1.x + d8[5] * u1.y + d8[6] * u1.z + d8[7] * u1.w;
+          }
+          sm.M1[i][j] = acc * sm.bs[j];
+          sm.M1T[j][i] = acc * sm.bs[j];
         }
-        sm.M1[i][j] = acc * sm.bs[j];
-        sm.M1T[j][i] = acc * sm.bs[j];
       }
-    }
-    ok = ok && tc::mbar_wait(mb0, par0);
-    par0 ^= 1;
-    tc::fence_after();
-    if (c > 0) prefetch_state(c - 1);  // Gdv has been read by the tensor core
-    // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
-    if (warp < 4) {
+      ok = ok && tc::mbar_wait(mb1, ph);
+      tc::fence_after();
+      // ---- decay: G <- G diag(gamma_C), G^T <- diag(gamma_C) G^T (this thread's lane kl)
+      {
+        const float gck = sm.gC[kl];
+#pragma unroll 2
+        for (int q = 0; q < 8; ++q) {
+          float g16[16];
+          tc::tmem_ld16(tl + kColGT + 16 * q, g16);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) g16[j] *= gck;
+          tc::tmem_st16(tl + kColGT + 16 * q, g16);
+        }
+#pragma unroll 2
+        for (int q = 0; q < 8; ++q) {
+          float x[16];
+          tc::tmem_ld16(tl + kColG + 16 * q, x);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + 16 * q + 4 * m);
+            x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
+          }
+          tc::tmem_st16(tl + kColG + 16 * q, x);
+        }
+        tc::tmem_wait_st();
+      }
+    } else {
+      ok = ok && tc::mbar_wait(mbD, ph);
+      tc::fence_after();
+      // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
       const int vv = kl;
       float dwk[16];
       tc::tmem_ld16(tl + kColDW, dwk);
@@ -473,6 +495,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         *reinterpret_cast<float4*>(sm.dUlo + tc::kmaj(vv, 4 * a4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
+    tc::fence_before();
     __syncthreads();
     // dV rows of the S0^T dV^T operand (token ot, quads oq and oq + 16)
 #pragma unroll
@@ -485,23 +508,29 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- MMA group 2: S0^T dV^T and the adjoint update
+    // ---- MMA group 2: S0^T dV^T and the adjoint update of G and G^T
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
         const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
         const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
+        const uint32_t s0 = tc::smem_u32(sm.S0s);
         const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ts(tbase + kColR, tbase + kColS + 8 * st, tc::kdesc(dou, st, kDim), i16, st > 0);
+          tc::mma_ss(tbase + kColR, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
+                     st > 0);
 #pragma unroll
-        for (int st = 0; st < 4; ++st)
-          tc::mma_ss(tbase + kColG, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
+        for (int st = 0; st < 4; ++st) {
+          tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
+          tc::mma_ss(tbase + kColG, tc::kdesc(douv, st, 32), tc::kdesc(qkt, st, 32), i128, 1);
+        }
 #pragma unroll
-        for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) times the dV lo part
-          tc::mma_ss(tbase + kColG, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
-        tc::mma_commit(mb0);
+        for (int st = 0; st < 2; ++st) {  // -k^g (columns 16..31 of QKT) with the dV lo part
+          tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
+          tc::mma_ss(tbase + kColG, tc::kdesc(dul, st, kChunk), tc::kdesc(qkt, 2 + st, 32), i128, 1);
+        }
+        tc::mma_commit(mb2);
       }
       __syncwarp();
     }
@@ -521,13 +550,13 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     } else if (tid < kChunk) {
       sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
     }
-    ok = ok && tc::mbar_wait(mb1, par1);
-    par1 ^= 1;
-    ok = ok && tc::mbar_wait(mb0, par0);
-    par0 ^= 1;
+    ok = ok && tc::mbar_wait(mb2, ph);
     tc::fence_after();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
-    if (c > 0) prefetch_late(c - 1);  // dO, u and A/B of this sub-chunk are no longer read
+    if (c > 0) {  // dO, u, A/B and S0 of this sub-chunk are no longer read
+      prefetch_late(c - 1);
+      prefetch_state(c - 1);
+    }
     // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows 8 hv .. 8 hv + 7)
     {
       float* dQh = cmb;
@@ -539,6 +568,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::tmem_ld8(tl + kColWG + 8 * hv, wh);
       tc::tmem_ld8(tl + kColWG + 16 + 8 * hv, wl);
       const int k = kl, i0 = 8 * hv;
+      const float gck = sm.gC[k];  // G^T W^T was taken before the decay
       float kic[kChunk], qtc[kChunk], ktc[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
@@ -553,7 +583,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         const int i = i0 + ii;
         const float gam = sm.Pa[i * kLds + k];
         const float inv = 1.0f / gam;
-        const float wg = wh[ii] + wl[ii];
+        const float wg = gck * (wh[ii] + wl[ii]);
         float pq = qd[ii], pr = rd[ii], pw = wg;
         float kii = 0.f, qti = 0.f, kti = 0.f;
         float m1r[kChunk], m2r[kChunk], m1c[kChunk], m2c[kChunk];
@@ -590,7 +620,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     // ---- P8: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
     if (tid < kDim) {
       float* tv = cmb + 2 * kTileF;
-      float run = sm.rho0[0][tid] + sm.rho0[1][tid] + sm.rho2[0][tid] + sm.rho2[1][tid];
+      float run = sm.gC[tid] * (sm.rho0[0][tid] + sm.rho0[1][tid]) + sm.rho2[0][tid] + sm.rho2[1][tid];
 #pragma unroll
       for (int i = kChunk - 1; i >= 0; --i) {
         run += tv[i * kLds + tid];
@@ -648,19 +678,20 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
       }
     }
+    ph ^= 1;
     tc::fence_before();
   }
   tc::cp_async_wait_all();
   __syncthreads();
   if (!aborted) {
-    // dinitial_state = G (stored transposed in TMEM)
+    // dinitial_state = G (from its transposed copy, for coalesced stores)
     float* dst = a.dh0 + (n * P.Hv + h) * kDim * kDim;
     tc::fence_after();
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       const int v0 = 64 * hv + 16 * q;
       float x[16];
-      tc::tmem_ld16(tl + kColG + v0, x);
+      tc::tmem_ld16(tl + kColGT + v0, x);
 #pragma unroll
       for (int j = 0; j < 16; ++j) dst[(v0 + j) * kDim + kl] = x[j];
     }

@@ -64,11 +64,13 @@ struct BwdArgs {
 
 constexpr int kParStride = 132;
 
-// Position of state element (v, k) inside one saved checkpoint: key quads are
-// outermost, then the value row, then the 4 keys of the quad. The forward
-// (thread per value row) then writes 512 contiguous bytes per warp, and the
-// backward (thread per key) reads 16-byte runs.
-__host__ __device__ __forceinline__ int ckpt_index(int v, int k) { return ((k >> 2) * 128 + v) * 4 + (k & 3); }
+// Position of state element (v, k) inside one saved checkpoint: value quads
+// are outermost, then the key, then the 4 values of the quad. Copied unchanged
+// to shared memory these bytes are S^T as a K-major tensor-core operand (rows
+// k, K = v: 8-row groups 128 bytes apart, K-adjacent 4-element core matrices
+// 2048 bytes apart), and a thread per key reads 16-byte runs of its own row
+// with the warp covering 512 contiguous bytes.
+__host__ __device__ __forceinline__ int ckpt_index(int v, int k) { return ((v >> 2) * 128 + k) * 4 + (v & 3); }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
 

@@ -29,7 +29,8 @@
 // state stay FP32. Each token's u = v - S' k^ and each sub-chunk's A and B
 // are saved for the backward. The gate, L2 norm
 // and sigmoid of each token are computed on chip (the fused prologue). The
-// state at the start of every checkpoint interval is stored for the backward.
+// state at the start of every checkpoint interval is stored for the backward
+// (transposed, in the layout the backward's tensor-core products read).
 #include "kda_common.cuh"
 #include "tc.cuh"
 
@@ -267,10 +268,15 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         float x[16];
         tc::tmem_ld16(tl + kColS + col, x);
         if (ck) {
+          // 4x4 blocks transposed across each lane quad: lane (quad base + j)
+          // then holds the four values of key col + 4 m + j
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
-            *reinterpret_cast<float4*>(dst + ckpt_index(sv, col + 4 * m)) =
-                make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+          for (int m = 0; m < 4; ++m) {
+            float y[4] = {x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]};
+            tc::quad_transpose(y, lane);
+            *reinterpret_cast<float4*>(dst + ckpt_index(sv & ~3, col + 4 * m + (lane & 3))) =
+                make_float4(y[0], y[1], y[2], y[3]);
+          }
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {

@@ -155,6 +155,17 @@ __device__ __forceinline__ void tmem_wait_ld(float* v) {
                :: "memory");
 }
 
+// Completes two outstanding 16-column loads (the empty statement orders the
+// second array's registers after the wait).
+__device__ __forceinline__ void tmem_wait_ld2(float* a, float* b) {
+  tmem_wait_ld(a);
+  uint32_t* r = reinterpret_cast<uint32_t*>(b);
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :: "memory");
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
