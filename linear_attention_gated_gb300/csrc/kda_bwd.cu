@@ -29,18 +29,19 @@
 // so no per-token elementwise state product is needed and no sum runs across
 // sub-chunks (a running sum over the whole sequence drifts in FP32).
 //
-// Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
-// state-sized contractions G (k^ gamma_C/gamma)^T (= Gd (k^/g)^T, the decay
-// folded into the operand), S0^T [dO; dV]^T, G^T W^T (W split into TF32 hi +
-// lo; scaled by gamma_C per key afterwards) and the rank-32 adjoint update (dV
-// split into hi + lo; dO is exact in TF32). The forward saves S0 transposed,
-// so the staged checkpoint is itself the shared-memory A operand S0^T; it is
-// rounded to TF32 in place after sum_v G * S0 has been taken from it in FP32.
-// G is read by the tensor core at TF32 (truncated); G^T W^T adds the product
-// of G^T's truncated-away low part, so it is split TF32 on both sides. The decay
-// G <- Gd runs on warps 4-7 while warps 0-3 solve for dV. The forward's FP32 A and B of each sub-chunk are reused. The
-// next sub-chunk's token tiles, u, A/B and state checkpoint are prefetched with
-// cp.async into buffers freed earlier in the current sub-chunk. The 16x16 intra-chunk
+// Each sub-chunk first decays both copies of the adjoint to Gd = G diag(gamma_C)
+// on CUDA cores. Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in
+// TMEM) then compute the state-sized contractions dW = Gd (k^/g)^T + scale dO^T B
+// (B split into TF32 hi + lo), S0^T [dO; dV]^T,
+// Gd^T W^T (W split into TF32 hi + lo) and the rank-32 adjoint update (dV split
+// into hi + lo; dO is exact in TF32). The forward saves S0 transposed, so the
+// staged checkpoint is itself the shared-memory A operand S0^T; it is rounded
+// to TF32 in place after sum_v Gd * S0 has been taken from it in FP32. Gd is
+// read by the tensor core at TF32 (truncated); Gd^T W^T adds the product of
+// Gd^T's truncated-away low part, so it is split TF32 on both sides. The
+// forward's FP32 A and B of each sub-chunk are reused. The next sub-chunk's
+// token tiles, u, A/B and state checkpoint are prefetched with cp.async into
+// buffers freed earlier in the current sub-chunk. The 16x16 intra-chunk
 // products, the substitutions and the combination run in FP32 on CUDA cores:
 // the decay gradient is a difference of nearly equal terms and needs them at
 // full single precision. The gate, sigmoid and L2-norm backward are applied in
@@ -58,18 +59,18 @@ constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // G, FP32 accumulator (lanes v, columns k)
 constexpr uint32_t kColGT = 128;  // G^T, the same adjoint transposed (lanes k, columns v)
-constexpr uint32_t kColGL = 256;  // G^T minus its TF32 truncation (the part the tensor core drops)
-constexpr uint32_t kColDW = 384;  // G (k^ gamma_C / gamma)^T : lanes v, 16 columns
+constexpr uint32_t kColGL = 256;  // Gd^T minus its TF32 truncation (the part the tensor core drops)
+constexpr uint32_t kColDW = 384;  // Gd (k^ / gamma)^T : lanes v, 16 columns
 constexpr uint32_t kColQ = 400;   // S0^T dO^T : lanes k, 16 columns
 constexpr uint32_t kColR = 416;   // S0^T dV^T : lanes k, 16 columns
-constexpr uint32_t kColWG = 432;  // G^T [W_hi; W_lo]^T : lanes k, 32 columns
+constexpr uint32_t kColWG = 432;  // Gd^T [W_hi; W_lo]^T : lanes k, 32 columns
 
 struct BwdSmem {
   // chunk-start state as saved (ckpt_index layout, cp.async staging): S0^T,
   // the K-major A operand (rows k, K = v) of S0^T dO^T and S0^T dV^T once
   // rounded to TF32 in place
   unsigned char S0s[kDim * kDim * 4];
-  unsigned char Kb[kChunk * kDim * 4];    // k^ gamma_C / gamma rows t          (K-major, K = 128)
+  unsigned char Ki[kChunk * kDim * 4];    // k^ / gamma rows t                  (K-major, K = 128)
   // Wt and dOU are contiguous: after the second MMA group they hold the
   // combination tiles (d q^, d k^, gauge term).
   unsigned char Wt[2][kChunk * kDim * 4]; // W rows t, TF32 hi then lo (one N = 32 operand)
@@ -77,6 +78,7 @@ struct BwdSmem {
   unsigned char dOUv[kDim * 32 * 4];      // rows v: cols 0..15 dO, 16..31 dV (hi) (K-major, K = 32)
   unsigned char dUlo[kDim * kChunk * 4];  // rows v: dV lo part                 (K-major, K = 16)
   unsigned char QKT[kDim * 32 * 4];       // rows k: cols 0..15 scale q^g, 16..31 -k^g (K-major, K = 32)
+  unsigned char Bsc[2][kChunk * kChunk * 4]; // scale B^T rows t (K = token j), TF32 hi / lo  (K = 16)
   float Pa[kTileF];                       // log decay, then gamma
   float Qtp[kTileF];                      // q^, then q^ gamma (FP32)
   float Ktp[kTileF];                      // k^, then k^ gamma (FP32)
@@ -97,7 +99,7 @@ struct BwdSmem {
   float braw[kChunk];
   float dba[kChunk];
   float gC[kDim];
-  float rho0[2][kDim];                    // halves of sum_v G * S0 (before the decay factor)
+  float rho0[2][kDim];                    // halves of sum_v Gd * S0
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
   float dbp[4][kChunk];                   // per-warp partial dbeta
   unsigned long long mbar[3];
@@ -215,39 +217,6 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     const int nt = rows_of(c);
     tc::cp_async_wait_all();
     __syncthreads();
-    // ---- sum_v G * S0 from the FP32 checkpoint (lane k, values of half hv; the
-    // decay factor gamma_C is applied in P8), then S0 rounded to TF32 in place
-    // for the tensor core (the products below see it rounded, not truncated),
-    // and the low part of G^T for the split G^T W^T
-    {
-      float racc = 0.f;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const int v0 = 64 * hv + 16 * q;
-        float g16[16];
-        tc::tmem_ld16_nowait(tl + kColGT + v0, g16);
-        float4 s4[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) s4[b] = *reinterpret_cast<const float4*>(sm.S0s + ckpt_index(v0 + 4 * b, kl) * 4);
-        tc::tmem_wait_ld(g16);
-        float lo16[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) lo16[j] = g16[j] - __uint_as_float(__float_as_uint(g16[j]) & 0xFFFFE000u);
-        tc::tmem_st16(tl + kColGL + v0, lo16);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          racc = fmaf(g16[4 * b], s4[b].x, racc);
-          racc = fmaf(g16[4 * b + 1], s4[b].y, racc);
-          racc = fmaf(g16[4 * b + 2], s4[b].z, racc);
-          racc = fmaf(g16[4 * b + 3], s4[b].w, racc);
-          *reinterpret_cast<float4*>(sm.S0s + ckpt_index(v0 + 4 * b, kl) * 4) =
-              make_float4(tc::round_tf32(s4[b].x), tc::round_tf32(s4[b].y), tc::round_tf32(s4[b].z),
-                          tc::round_tf32(s4[b].w));
-        }
-      }
-      sm.rho0[hv][kl] = racc;
-      tc::tmem_wait_st();
-    }
     // ---- P0: prologue (token row ti, columns c8..c8+7): L2 norm, gate, sigmoid beta
     float qhat[8], khat[8], zz[8], rq, rk;
     {
@@ -261,15 +230,15 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
       sq = row16_sum(sq);
       sk = row16_sum(sk);
-      rq = valid ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
-      rk = valid ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+      rq = valid ? inv_norm_of(sq) : 0.f;
+      rk = valid ? inv_norm_of(sk) : 0.f;
       float la[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         qhat[e] = qv[e] * rq;
         khat[e] = kv[e] * rk;
         zz[e] = ea * (gv[e] + dtb[e]);
-        la[e] = valid ? P.lb / (1.0f + expf(-zz[e])) : 0.f;
+        la[e] = valid ? log_decay_of(P.lb, zz[e]) : 0.f;
       }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -281,7 +250,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       if (tid < kChunk) {
         const float bl = __bfloat162float(nb);
         sm.braw[tid] = bl;
-        sm.bs[tid] = (tid < nt) ? 1.0f / (1.0f + expf(-bl)) : 0.f;
+        sm.bs[tid] = (tid < nt) ? sigmoid_of(bl) : 0.f;
       }
     }
     __syncthreads();
@@ -302,7 +271,49 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       sm.gC[tid] = av[kChunk - 1];
     }
     __syncthreads();
-    // ---- P2: operand tiles (token ot, quads oq and oq + 16)
+    // ---- P2: decay of the adjoint, G <- G diag(gamma_C) (lanes v) and G^T <- diag(gamma_C) G^T
+    // (lanes k), with sum_v Gd * S0 from the FP32 checkpoint, the low part of Gd^T for the
+    // split Gd^T W^T, and S0 rounded to TF32 in place for the tensor core; then the operand tiles
+    {
+      const float gck = sm.gC[kl];
+      float racc = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int c0 = 64 * hv + 16 * q;
+        float g16[16], x16[16];
+        tc::tmem_ld16_nowait(tl + kColGT + c0, g16);
+        tc::tmem_ld16_nowait(tl + kColG + c0, x16);
+        float4 s4[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) s4[b] = *reinterpret_cast<const float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4);
+        tc::tmem_wait_ld2(g16, x16);
+        float lo16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          g16[j] *= gck;
+          lo16[j] = g16[j] - __uint_as_float(__float_as_uint(g16[j]) & 0xFFFFE000u);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 y = *reinterpret_cast<const float4*>(sm.gC + c0 + 4 * m);
+          x16[4 * m] *= y.x; x16[4 * m + 1] *= y.y; x16[4 * m + 2] *= y.z; x16[4 * m + 3] *= y.w;
+        }
+        tc::tmem_st16(tl + kColGT + c0, g16);
+        tc::tmem_st16(tl + kColGL + c0, lo16);
+        tc::tmem_st16(tl + kColG + c0, x16);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          racc = fmaf(g16[4 * b], s4[b].x, racc);
+          racc = fmaf(g16[4 * b + 1], s4[b].y, racc);
+          racc = fmaf(g16[4 * b + 2], s4[b].z, racc);
+          racc = fmaf(g16[4 * b + 3], s4[b].w, racc);
+          *reinterpret_cast<float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4) =
+              make_float4(tc::round_tf32(s4[b].x), tc::round_tf32(s4[b].y), tc::round_tf32(s4[b].z),
+                          tc::round_tf32(s4[b].w));
+        }
+      }
+      sm.rho0[hv][kl] = racc;
+    }
 #pragma unroll
     for (int rep = 0; rep < 2; ++rep) {
       const int k0 = 4 * (oq + 16 * rep);
@@ -310,47 +321,63 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       const float4 kh4 = *reinterpret_cast<const float4*>(sm.Ktp + ot * kLds + k0);
       const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + ot * kLds + k0);
       const float4 u4 = *reinterpret_cast<const float4*>(sm.Up + ot * kLds + k0);
-      const float4 c4 = *reinterpret_cast<const float4*>(sm.gC + k0);
       const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
       const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ua[4] = {u4.x, u4.y, u4.z, u4.w};
-      const float ca[4] = {c4.x, c4.y, c4.z, c4.w};
       const float bt = sm.bs[ot];
-      float kt[4], qt[4], ki[4], kb[4], whi[4], wlo[4], dof[4];
+      float kt[4], qt[4], ki[4], whi[4], wlo[4], dof[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float inv = 1.0f / ga[e];
+        const float inv = __fdividef(1.0f, ga[e]);  // gamma is in [e^-80, 1]
         kt[e] = ka[e] * ga[e];
         qt[e] = qa[e] * ga[e];
         ki[e] = ka[e] * inv;
-        kb[e] = tc::round_tf32(ka[e] * (ca[e] * inv));
         const float w = bt * ua[e];
         whi[e] = tc::round_tf32(w);
         wlo[e] = tc::round_tf32(w - whi[e]);
         dof[e] = __bfloat162float(sm.dOp[ot * kDim + k0 + e]);
+        *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(k0 + e, ot, 32)) = dof[e];
         *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, ot, 32)) = tc::round_tf32(s * qt[e]);
         *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, 16 + ot, 32)) = tc::round_tf32(-kt[e]);
       }
       *reinterpret_cast<float4*>(sm.Ktp + ot * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
       *reinterpret_cast<float4*>(sm.Qtp + ot * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
       *reinterpret_cast<float4*>(sm.Kip + ot * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
-      *reinterpret_cast<float4*>(sm.Kb + tc::kmaj(ot, k0, kDim)) = make_float4(kb[0], kb[1], kb[2], kb[3]);
+      *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ot, k0, kDim)) =
+          make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
       *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ot, k0, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
       *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ot, k0, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
       *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ot, k0, kDim)) = make_float4(dof[0], dof[1], dof[2], dof[3]);
     }
+    {  // scale B^T as rows t, K = j (B[j][t] is BsT[t][j]), split into TF32 hi + lo
+      const int t = tid >> 4, j = tid & 15;
+      const float x = s * sm.BsT[t][j];
+      const float hi = tc::round_tf32(x);
+      *reinterpret_cast<float*>(sm.Bsc[0] + tc::kmaj(t, j, kChunk)) = hi;
+      *reinterpret_cast<float*>(sm.Bsc[1] + tc::kmaj(t, j, kChunk)) = tc::round_tf32(x - hi);
+    }
+    tc::tmem_wait_st();
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- MMA group 1: G Kb^T first (the dV chain needs it), then S0^T dO^T and G^T W^T
-    if (warp == 0) {
+    // ---- MMA group 1: dW = Gd (k^/g)^T + scale dO^T B first (the dV chain needs it), then S0^T dO^T
+    // and Gd^T W^T
+    // (issued from warp 4, whose next work, dO W^T, is not needed until the combination)
+    if (warp == 4) {
       if (tc::elect_one()) {
         tc::fence_after();
-        const uint32_t kb = tc::smem_u32(sm.Kb), s0 = tc::smem_u32(sm.S0s);
+        const uint32_t ki = tc::smem_u32(sm.Ki), s0 = tc::smem_u32(sm.S0s);
         const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
+        const uint32_t douv = tc::smem_u32(sm.dOUv);
+        const uint32_t bsc[2] = {tc::smem_u32(sm.Bsc[0]), tc::smem_u32(sm.Bsc[1])};
         const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, tc::kdesc(kb, st, kDim), i16, st > 0);
+          tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, tc::kdesc(ki, st, kDim), i16, st > 0);
+#pragma unroll
+        for (int p = 0; p < 2; ++p)  // dO (rows v, exact in TF32) with scale B^T hi and lo
+#pragma unroll
+          for (int st = 0; st < 2; ++st)
+            tc::mma_ss(tbase + kColDW, tc::kdesc(douv, st, 32), tc::kdesc(bsc[p], st, kChunk), i16, 1);
         tc::mma_commit(mbD);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st) {
@@ -359,7 +386,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
         }
 #pragma unroll
-        for (int st = 0; st < kDim / 8; ++st)  // the low part of G^T with [W_hi; W_lo]
+        for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
           tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
         tc::mma_commit(mb1);
       }
@@ -386,55 +413,13 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           sm.M1T[j][i] = acc * sm.bs[j];
         }
       }
-      ok = ok && tc::mbar_wait(mb1, ph);
-      tc::fence_after();
-      // ---- decay: G <- G diag(gamma_C), G^T <- diag(gamma_C) G^T (this thread's lane kl)
-      {
-        const float gck = sm.gC[kl];
-#pragma unroll 2
-        for (int q = 0; q < 8; ++q) {
-          float g16[16];
-          tc::tmem_ld16(tl + kColGT + 16 * q, g16);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) g16[j] *= gck;
-          tc::tmem_st16(tl + kColGT + 16 * q, g16);
-        }
-#pragma unroll 2
-        for (int q = 0; q < 8; ++q) {
-          float x[16];
-          tc::tmem_ld16(tl + kColG + 16 * q, x);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + 16 * q + 4 * m);
-            x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
-          }
-          tc::tmem_st16(tl + kColG + 16 * q, x);
-        }
-        tc::tmem_wait_st();
-      }
     } else {
       ok = ok && tc::mbar_wait(mbD, ph);
       tc::fence_after();
       // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
       const int vv = kl;
-      float dwk[16];
-      tc::tmem_ld16(tl + kColDW, dwk);
-      float dof[kChunk], acc[kChunk], pbv[kChunk];
-#pragma unroll
-      for (int j = 0; j < kChunk; ++j) dof[j] = __bfloat162float(sm.dOp[j * kDim + vv]);
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        float brow[kChunk];  // B[j][i] for all j (zero for j < i)
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 x = *reinterpret_cast<const float4*>(&sm.BsT[i][4 * q4]);
-          brow[4 * q4] = x.x; brow[4 * q4 + 1] = x.y; brow[4 * q4 + 2] = x.z; brow[4 * q4 + 3] = x.w;
-        }
-        float x = 0.f;
-#pragma unroll
-        for (int j = i; j < kChunk; ++j) x = fmaf(brow[j], dof[j], x);
-        acc[i] = fmaf(s, x, dwk[i]);
-      }
+      float acc[kChunk], pbv[kChunk];
+      tc::tmem_ld16(tl + kColDW, acc);  // dW (rows v)
       // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
 #pragma unroll
       for (int i = kChunk - 1; i >= 0; --i) {
@@ -489,8 +474,6 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           hi[e] = tc::round_tf32(acc[4 * a4 + e]);
           lo[e] = tc::round_tf32(acc[4 * a4 + e] - hi[e]);
         }
-        *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(vv, 4 * a4, 32)) =
-            make_float4(dof[4 * a4], dof[4 * a4 + 1], dof[4 * a4 + 2], dof[4 * a4 + 3]);
         *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(vv, 16 + 4 * a4, 32)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<float4*>(sm.dUlo + tc::kmaj(vv, 4 * a4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
       }
@@ -550,6 +533,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     } else if (tid < kChunk) {
       sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
     }
+    ok = ok && tc::mbar_wait(mb1, ph);
     ok = ok && tc::mbar_wait(mb2, ph);
     tc::fence_after();
     if (__syncthreads_or(!ok)) { aborted = true; break; }
@@ -568,7 +552,6 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::tmem_ld8(tl + kColWG + 8 * hv, wh);
       tc::tmem_ld8(tl + kColWG + 16 + 8 * hv, wl);
       const int k = kl, i0 = 8 * hv;
-      const float gck = sm.gC[k];  // G^T W^T was taken before the decay
       float kic[kChunk], qtc[kChunk], ktc[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
@@ -582,8 +565,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         // rows of this thread: i = i0 + ii (i0 is 0 or 8; the masks below compare with it)
         const int i = i0 + ii;
         const float gam = sm.Pa[i * kLds + k];
-        const float inv = 1.0f / gam;
-        const float wg = gck * (wh[ii] + wl[ii]);
+        const float inv = __fdividef(1.0f, gam);
+        const float wg = wh[ii] + wl[ii];
         float pq = qd[ii], pr = rd[ii], pw = wg;
         float kii = 0.f, qti = 0.f, kti = 0.f;
         float m1r[kChunk], m2r[kChunk], m1c[kChunk], m2c[kChunk];
@@ -620,7 +603,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     // ---- P8: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
     if (tid < kDim) {
       float* tv = cmb + 2 * kTileF;
-      float run = sm.gC[tid] * (sm.rho0[0][tid] + sm.rho0[1][tid]) + sm.rho2[0][tid] + sm.rho2[1][tid];
+      float run = sm.rho0[0][tid] + sm.rho0[1][tid] + sm.rho2[0][tid] + sm.rho2[1][tid];
 #pragma unroll
       for (int i = kChunk - 1; i >= 0; --i) {
         run += tv[i * kLds + tid];
@@ -641,7 +624,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       for (int e = 0; e < 8; ++e) {
         // sigmoid'(z) = sigmoid(z) sigmoid(-z) = e / (1 + e)^2 with e = exp(-|z|) (no cancellation)
         const float ex = expf(-fabsf(zz[e]));
-        const float den = 1.0f / (1.0f + ex);
+        const float den = __fdividef(1.0f, 1.0f + ex);
         const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * ex * den * den : 0.f;
         dg8[e] = dz * ea;
         ddt_acc[e] += dg8[e];
@@ -674,7 +657,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         }
       }
       if (tid < nt) {
-        const float bn = 1.0f / (1.0f + expf(sm.braw[tid]));  // sigmoid(-logit)
+        const float bn = sigmoid_of(-sm.braw[tid]);
         a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
       }
     }
@@ -761,7 +744,7 @@ __global__ void kda_gqa_reduce_kernel(const Problem P, const float* __restrict__
     float ss = xv[0] * xv[0] + xv[1] * xv[1] + xv[2] * xv[2] + xv[3] * xv[3];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float r = 1.0f / sqrtf(ss + kNormEps);
+    const float r = inv_norm_of(ss);
     float pd = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) { xv[e] *= r; pd += xv[e] * acc[e]; }

@@ -72,7 +72,14 @@ constexpr int kParStride = 132;
 // with the warp covering 512 contiguous bytes.
 __host__ __device__ __forceinline__ int ckpt_index(int v, int k) { return ((v >> 2) * 128 + k) * 4 + (v & 3); }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// Element maths of the prologue and epilogue. Divisions use __fdividef (at most
+// 2 ulp off for divisors in [2^-126, 2^126], 0 for an infinite divisor) and the
+// norm factor rsqrtf: neither has the IEEE special-case branch, so the eight
+// independent per-thread chains interleave. Forward and backward call the same
+// functions, so they see bit-identical decays and normalised vectors.
+__device__ __forceinline__ float sigmoid_of(float x) { return __fdividef(1.0f, 1.0f + expf(-x)); }
+__device__ __forceinline__ float log_decay_of(float lb, float z) { return __fdividef(lb, 1.0f + expf(-z)); }
+__device__ __forceinline__ float inv_norm_of(float sumsq) { return rsqrtf(sumsq + kNormEps); }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
   const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);

@@ -143,15 +143,15 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
       sq = row16_sum(sq);
       sk = row16_sum(sk);
-      const float rq = valid ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
-      const float rk = valid ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+      const float rq = valid ? inv_norm_of(sq) : 0.f;
+      const float rk = valid ? inv_norm_of(sk) : 0.f;
       float la[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float z = ea * (gv[e] + dtb[e]);
         qv[e] *= rq;
         kv[e] *= rk;
-        la[e] = valid ? P.lb / (1.0f + expf(-z)) : 0.f;
+        la[e] = valid ? log_decay_of(P.lb, z) : 0.f;
       }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -161,7 +161,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         *reinterpret_cast<float4*>(sm.Pa + col) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
         *reinterpret_cast<float4*>(sm.Vs + col) = make_float4(vv[o], vv[o + 1], vv[o + 2], vv[o + 3]);
       }
-      if (tid < kChunk) sm.bs[tid] = (tid < ntc) ? 1.0f / (1.0f + expf(-braw)) : 0.f;
+      if (tid < kChunk) sm.bs[tid] = (tid < ntc) ? sigmoid_of(braw) : 0.f;
     }
     __syncthreads();
     if (tid < kDim) {
@@ -201,7 +201,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         float kt[4], qt[4], ki[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float inv = 1.0f / ga[e];
+          const float inv = __fdividef(1.0f, ga[e]);  // gamma is in [e^-80, 1]
           kt[e] = ka[e] * ga[e];
           qt[e] = qa[e] * ga[e];
           ki[e] = ka[e] * inv;
