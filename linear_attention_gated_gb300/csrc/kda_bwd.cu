@@ -623,7 +623,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         // sigmoid'(z) = sigmoid(z) sigmoid(-z) = e / (1 + e)^2 with e = exp(-|z|) (no cancellation)
-        const float ex = expf(-fabsf(zz[e]));
+        const float ex = __expf(-fabsf(zz[e]));
         const float den = __fdividef(1.0f, 1.0f + ex);
         const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * ex * den * den : 0.f;
         dg8[e] = dz * ea;

@@ -73,12 +73,14 @@ constexpr int kParStride = 132;
 __host__ __device__ __forceinline__ int ckpt_index(int v, int k) { return ((v >> 2) * 128 + k) * 4 + (v & 3); }
 
 // Element maths of the prologue and epilogue. Divisions use __fdividef (at most
-// 2 ulp off for divisors in [2^-126, 2^126], 0 for an infinite divisor) and the
-// norm factor rsqrtf: neither has the IEEE special-case branch, so the eight
-// independent per-thread chains interleave. Forward and backward call the same
+// 2 ulp off for divisors in [2^-126, 2^126], 0 for an infinite divisor), the
+// sigmoids __expf (its error grows with |x|, but where e^-x is not negligible
+// next to 1, |x| < 20, it stays near 1e-6 relative) and the norm factor rsqrtf:
+// none has a special-case branch, so the eight independent per-thread chains
+// interleave. Forward and backward call the same
 // functions, so they see bit-identical decays and normalised vectors.
-__device__ __forceinline__ float sigmoid_of(float x) { return __fdividef(1.0f, 1.0f + expf(-x)); }
-__device__ __forceinline__ float log_decay_of(float lb, float z) { return __fdividef(lb, 1.0f + expf(-z)); }
+__device__ __forceinline__ float sigmoid_of(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float log_decay_of(float lb, float z) { return __fdividef(lb, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float inv_norm_of(float sumsq) { return rsqrtf(sumsq + kNormEps); }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float* out) {
