@@ -276,7 +276,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     // split Gd^T W^T, and S0 rounded to TF32 in place for the tensor core; then the operand tiles
     {
       const float gck = sm.gC[kl];
-      float racc = 0.f;
+      float4 racc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         const int c0 = 64 * hv + 16 * q;
@@ -303,16 +303,13 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         tc::tmem_st16(tl + kColG + c0, x16);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          racc = fmaf(g16[4 * b], s4[b].x, racc);
-          racc = fmaf(g16[4 * b + 1], s4[b].y, racc);
-          racc = fmaf(g16[4 * b + 2], s4[b].z, racc);
-          racc = fmaf(g16[4 * b + 3], s4[b].w, racc);
+          fma4(racc, make_float4(g16[4 * b], g16[4 * b + 1], g16[4 * b + 2], g16[4 * b + 3]), s4[b]);
           *reinterpret_cast<float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4) =
               make_float4(tc::round_tf32(s4[b].x), tc::round_tf32(s4[b].y), tc::round_tf32(s4[b].z),
                           tc::round_tf32(s4[b].w));
         }
       }
-      sm.rho0[hv][kl] = racc;
+      sm.rho0[hv][kl] = hsum4(racc);
     }
 #pragma unroll
     for (int rep = 0; rep < 2; ++rep) {
@@ -399,16 +396,16 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
         for (int rep = 0; rep < 2; ++rep) {
           const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
-          float acc = 0.f;
+          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
           for (int vv = 0; vv < kDim; vv += 8) {
             float d8[8];
             unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.dOp + i * kDim + vv), d8);
-            const float4 u0 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv);
-            const float4 u1 = *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv + 4);
-            acc += d8[0] * u0.x + d8[1] * u0.y + d8[2] * u0.z + d8[3] * u0.w +
-                   d8[4] * u1.x + d8[5] * u1.y + d8[6] * u1.z + d8[7] * u1.w;
+            fma4(a4, make_float4(d8[0], d8[1], d8[2], d8[3]), *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
+            fma4(a4, make_float4(d8[4], d8[5], d8[6], d8[7]),
+                 *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv + 4));
           }
+          const float acc = hsum4(a4);
           sm.M1[i][j] = acc * sm.bs[j];
           sm.M1T[j][i] = acc * sm.bs[j];
         }
@@ -522,11 +519,12 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
         const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
-        float acc = 0.f;
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int vv = 0; vv < kDim; vv += 4)
-          acc += dot4(*reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
-                      *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
+          fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
+               *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
+        const float acc = hsum4(a4);
         sm.M2[i][j] = acc * sm.bs[j];
         sm.M2T[j][i] = acc * sm.bs[j];
       }

@@ -112,9 +112,15 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* p, const float* in) 
   *reinterpret_cast<uint4*>(p) = raw;
 }
 
-__device__ __forceinline__ float dot4(float4 a, float4 b) {
-  return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+// acc += a * b elementwise: four independent FMA chains for long dot products
+// (one running sum would make every FMA wait for the previous one).
+__device__ __forceinline__ void fma4(float4& acc, float4 a, float4 b) {
+  acc.x = fmaf(a.x, b.x, acc.x);
+  acc.y = fmaf(a.y, b.y, acc.y);
+  acc.z = fmaf(a.z, b.z, acc.z);
+  acc.w = fmaf(a.w, b.w, acc.w);
 }
+__device__ __forceinline__ float hsum4(float4 a) { return (a.x + a.y) + (a.z + a.w); }
 
 // Sum over the 16 lanes that share a token row (lanes 0-15 or 16-31 of a warp).
 __device__ __forceinline__ float row16_sum(float x) {

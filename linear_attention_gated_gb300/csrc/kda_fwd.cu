@@ -244,10 +244,12 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         const int j = j0 + 8 * rep;
         float acc = 0.f;
         if (j < i || (mat && j == i)) {
+          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
           for (int kk = 0; kk < kDim; kk += 4)
-            acc += dot4(*reinterpret_cast<const float4*>(X + i * kLds + kk),
-                        *reinterpret_cast<const float4*>(sm.Pi + j * kLds + kk));
+            fma4(a4, *reinterpret_cast<const float4*>(X + i * kLds + kk),
+                 *reinterpret_cast<const float4*>(sm.Pi + j * kLds + kk));
+          acc = hsum4(a4);
         }
         if (mat) sm.Bs[i][j] = acc; else sm.AsT[j][i] = acc;
         // for the backward: A row-major, B transposed (its columns are read there)
