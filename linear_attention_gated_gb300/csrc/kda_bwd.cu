@@ -277,7 +277,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     {
       const float gck = sm.gC[kl];
       float4 racc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
+#pragma unroll 2
       for (int q = 0; q < 4; ++q) {
         const int c0 = 64 * hv + 16 * q;
         float g16[16], x16[16];
@@ -418,10 +418,16 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       float acc[kChunk], pbv[kChunk];
       tc::tmem_ld16(tl + kColDW, acc);  // dW (rows v)
       // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
+      float bsv[kChunk], upv[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        bsv[i] = sm.bs[i];
+        upv[i] = sm.Up[i * kLds + vv];
+      }
 #pragma unroll
       for (int i = kChunk - 1; i >= 0; --i) {
         const float ei = acc[i];
-        const float du = sm.bs[i] * ei;
+        const float du = bsv[i] * ei;
         acc[i] = du;  // keep dV in place
         float arow[kChunk];
 #pragma unroll
@@ -431,7 +437,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         }
 #pragma unroll
         for (int m = 0; m < i; ++m) acc[m] = fmaf(-arow[m], du, acc[m]);
-        pbv[i] = ei * sm.Up[i * kLds + vv];
+        pbv[i] = ei * upv[i];
       }
       // dbeta partial sums over the warp's 32 value rows: halving butterfly
       // (16 shuffles); lane l ends with the sum for token 8 b4 + 4 b3 + 2 b2 + b1
