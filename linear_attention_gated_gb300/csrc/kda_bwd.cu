@@ -38,7 +38,8 @@
 // staged checkpoint is itself the shared-memory A operand S0^T; it is rounded
 // to TF32 in place after sum_v Gd * S0 has been taken from it in FP32. Gd is
 // read by the tensor core at TF32 (truncated); Gd^T W^T adds the product of
-// Gd^T's truncated-away low part, so it is split TF32 on both sides. The
+// Gd^T's truncated-away low part, so it is split TF32 on both sides. dO W^T
+// (dO exact in TF32, W split) also runs on the tensor core. The
 // forward's FP32 A and B of each sub-chunk are reused. The next sub-chunk's
 // token tiles, u, A/B and state checkpoint are prefetched with cp.async into
 // buffers freed earlier in the current sub-chunk. The 16x16 intra-chunk
@@ -48,6 +49,8 @@
 // the epilogue (flashinfer.kda_backward.recurrent_kda_backward, description:
 // gradients with respect to the raw gate and raw beta logits, Q/K normalised
 // with eps 1e-6).
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "tc.cuh"
 
@@ -64,6 +67,7 @@ constexpr uint32_t kColDW = 384;  // Gd (k^ / gamma)^T : lanes v, 16 columns
 constexpr uint32_t kColQ = 400;   // S0^T dO^T : lanes k, 16 columns
 constexpr uint32_t kColR = 416;   // S0^T dV^T : lanes k, 16 columns
 constexpr uint32_t kColWG = 432;  // Gd^T [W_hi; W_lo]^T : lanes k, 32 columns
+constexpr uint32_t kColM1 = 464;  // dO [W_hi; W_lo]^T : lanes 0..15 (token i), 32 columns
 
 struct BwdSmem {
   // chunk-start state as saved (ckpt_index layout, cp.async staging): S0^T,
@@ -91,7 +95,7 @@ struct BwdSmem {
   __nv_bfloat16 dOp[kChunk * kDim];
   float As[kChunk][kChunk];               // A and B^T of the sub-chunk, from the forward (cp.async
   float BsT[kChunk][kChunk];              // staging); As and BsT must stay contiguous
-  float M1[kChunk][kChunk];               // dO W^T
+  float M1[kChunk][kChunk];               // dO W^T (W = diag(beta) U)
   float M2[kChunk][kChunk];               // dV W^T
   float M1T[kChunk][kChunk];
   float M2T[kChunk][kChunk];
@@ -385,29 +389,36 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
           tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
+        // dO W^T: the A tile is read as 128 rows from dOU on; rows 0..15 are dO
+        // and the rest (other shared-memory tiles) only fill D lanes 16..127,
+        // which are never read
+#pragma unroll
+        for (int st = 0; st < kDim / 8; ++st)
+          tc::mma_ss(tbase + kColM1, tc::kdesc(dou, st, kDim), tc::kdesc(wt, st, kDim), i32, st > 0);
         tc::mma_commit(mb1);
       }
       __syncwarp();
     }
     if (warp >= 4) {
-      // dO W^T with W = beta u, in FP32
-      {
-        const int t2 = tid - 128;
+      // dO W^T = dO (W_hi + W_lo)^T from tensor memory (dO is exact in TF32)
+      ok = ok && tc::mbar_wait(mb1, ph);
+      tc::fence_after();
+      if (warp == 4) {
+        float hi16[16], lo16[16];
+        tc::tmem_ld16_nowait(tl + kColM1, hi16);
+        tc::tmem_ld16_nowait(tl + kColM1 + 16, lo16);
+        tc::tmem_wait_ld2(hi16, lo16);
+        if (lane < kChunk) {
 #pragma unroll
-        for (int rep = 0; rep < 2; ++rep) {
-          const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
-          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-          for (int vv = 0; vv < kDim; vv += 8) {
-            float d8[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.dOp + i * kDim + vv), d8);
-            fma4(a4, make_float4(d8[0], d8[1], d8[2], d8[3]), *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
-            fma4(a4, make_float4(d8[4], d8[5], d8[6], d8[7]),
-                 *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv + 4));
+          for (int j = 0; j < kChunk; ++j) {
+            const float m = hi16[j] + lo16[j];
+            sm.M1T[j][lane] = m;
+            hi16[j] = m;
           }
-          const float acc = hsum4(a4);
-          sm.M1[i][j] = acc * sm.bs[j];
-          sm.M1T[j][i] = acc * sm.bs[j];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<float4*>(&sm.M1[lane][4 * q4]) =
+                make_float4(hi16[4 * q4], hi16[4 * q4 + 1], hi16[4 * q4 + 2], hi16[4 * q4 + 3]);
         }
       }
     } else {
@@ -545,63 +556,72 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       prefetch_late(c - 1);
       prefetch_state(c - 1);
     }
-    // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows 8 hv .. 8 hv + 7)
+    // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows i0 .. i0 + 7 with
+    // i0 = 8 hv a compile-time constant, so the triangular masks drop whole terms)
     {
-      float* dQh = cmb;
-      float* dKh = cmb + kTileF;
-      float* tv = cmb + 2 * kTileF;
-      float qd[8], rd[8], wh[8], wl[8];
-      tc::tmem_ld8(tl + kColQ + 8 * hv, qd);
-      tc::tmem_ld8(tl + kColR + 8 * hv, rd);
-      tc::tmem_ld8(tl + kColWG + 8 * hv, wh);
-      tc::tmem_ld8(tl + kColWG + 16 + 8 * hv, wl);
-      const int k = kl, i0 = 8 * hv;
-      float kic[kChunk], qtc[kChunk], ktc[kChunk];
-#pragma unroll
-      for (int j = 0; j < kChunk; ++j) {
-        kic[j] = sm.Kip[j * kLds + k];
-        qtc[j] = sm.Qtp[j * kLds + k];
-        ktc[j] = sm.Ktp[j * kLds + k];
-      }
-      float rp = 0.f;
-#pragma unroll
-      for (int ii = 0; ii < 8; ++ii) {
-        // rows of this thread: i = i0 + ii (i0 is 0 or 8; the masks below compare with it)
-        const int i = i0 + ii;
-        const float gam = sm.Pa[i * kLds + k];
-        const float inv = __fdividef(1.0f, gam);
-        const float wg = wh[ii] + wl[ii];
-        float pq = qd[ii], pr = rd[ii], pw = wg;
-        float kii = 0.f, qti = 0.f, kti = 0.f;
-        float m1r[kChunk], m2r[kChunk], m1c[kChunk], m2c[kChunk];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(&sm.M1[i][4 * q4]);
-          const float4 b4 = *reinterpret_cast<const float4*>(&sm.M2[i][4 * q4]);
-          const float4 c4 = *reinterpret_cast<const float4*>(&sm.M1T[i][4 * q4]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&sm.M2T[i][4 * q4]);
-          m1r[4 * q4] = a4.x; m1r[4 * q4 + 1] = a4.y; m1r[4 * q4 + 2] = a4.z; m1r[4 * q4 + 3] = a4.w;
-          m2r[4 * q4] = b4.x; m2r[4 * q4 + 1] = b4.y; m2r[4 * q4 + 2] = b4.z; m2r[4 * q4 + 3] = b4.w;
-          m1c[4 * q4] = c4.x; m1c[4 * q4 + 1] = c4.y; m1c[4 * q4 + 2] = c4.z; m1c[4 * q4 + 3] = c4.w;
-          m2c[4 * q4] = d4.x; m2c[4 * q4 + 1] = d4.y; m2c[4 * q4 + 2] = d4.z; m2c[4 * q4 + 3] = d4.w;
-        }
+      auto combine = [&](auto i0c) {
+        constexpr int i0 = decltype(i0c)::value;
+        float* dQh = cmb;
+        float* dKh = cmb + kTileF;
+        float* tv = cmb + 2 * kTileF;
+        float qd[8], rd[8], wh[8], wl[8];
+        tc::tmem_ld8(tl + kColQ + i0, qd);
+        tc::tmem_ld8(tl + kColR + i0, rd);
+        tc::tmem_ld8(tl + kColWG + i0, wh);
+        tc::tmem_ld8(tl + kColWG + 16 + i0, wl);
+        const int k = kl;
+        float kic[kChunk], qtc[kChunk], ktc[kChunk];
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          if (j == i) { kii = kic[j]; qti = qtc[j]; kti = ktc[j]; }
-          if (j <= i) pq = fmaf(m1r[j], kic[j], pq);
-          if (j < i) pr = fmaf(m2r[j], kic[j], pr);
-          if (j >= i) pw = fmaf(s * m1c[j], qtc[j], pw);
-          if (j > i) pw = fmaf(-m2c[j], ktc[j], pw);
+          kic[j] = sm.Kip[j * kLds + k];
+          qtc[j] = sm.Qtp[j * kLds + k];
+          ktc[j] = sm.Ktp[j * kLds + k];
         }
-        rp = fmaf(kii, wg, rp);
-        const float dq_ = s * gam * pq;
-        const float dkr = -gam * pr;
-        const float dkw = inv * pw;
-        dQh[i * kLds + k] = dq_;
-        dKh[i * kLds + k] = dkr + dkw;
-        tv[i * kLds + k] = qti * inv * dq_ + kti * inv * (dkr - dkw);
-      }
-      sm.rho2[hv][k] = rp;
+        float rp = 0.f;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          const int i = i0 + ii;
+          const float gam = sm.Pa[i * kLds + k];
+          const float inv = __fdividef(1.0f, gam);
+          const float wg = wh[ii] + wl[ii];
+          float pq = qd[ii], pr = rd[ii], pw = wg;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            if (4 * q4 <= i) {  // tril(M1) and stril(M2) rows
+              const float4 a4 = *reinterpret_cast<const float4*>(&sm.M1[i][4 * q4]);
+              const float4 b4 = *reinterpret_cast<const float4*>(&sm.M2[i][4 * q4]);
+              const float m1r[4] = {a4.x, a4.y, a4.z, a4.w}, m2r[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * q4 + e;
+                if (j <= i) pq = fmaf(m1r[e], kic[j], pq);
+                if (j < i) pr = fmaf(m2r[e], kic[j], pr);
+              }
+            }
+            if (4 * q4 + 3 >= i) {  // triu(M1^T) and striu(M2^T) rows
+              const float4 c4 = *reinterpret_cast<const float4*>(&sm.M1T[i][4 * q4]);
+              const float4 d4 = *reinterpret_cast<const float4*>(&sm.M2T[i][4 * q4]);
+              const float m1c[4] = {c4.x, c4.y, c4.z, c4.w}, m2c[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * q4 + e;
+                if (j >= i) pw = fmaf(s * m1c[e], qtc[j], pw);
+                if (j > i) pw = fmaf(-m2c[e], ktc[j], pw);
+              }
+            }
+          }
+          rp = fmaf(kic[i], wg, rp);
+          const float dq_ = s * gam * pq;
+          const float dkr = -gam * pr;
+          const float dkw = inv * pw;
+          dQh[i * kLds + k] = dq_;
+          dKh[i * kLds + k] = dkr + dkw;
+          tv[i * kLds + k] = qtc[i] * inv * dq_ + ktc[i] * inv * (dkr - dkw);
+        }
+        sm.rho2[i0 / 8][k] = rp;
+      };
+      if (hv == 0) combine(std::integral_constant<int, 0>{});
+      else combine(std::integral_constant<int, 8>{});
     }
     __syncthreads();
     // ---- P8: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
