@@ -31,6 +31,8 @@
 // and sigmoid of each token are computed on chip (the fused prologue). The
 // state at the start of every checkpoint interval is stored for the backward
 // (transposed, in the layout the backward's tensor-core products read).
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "tc.cuh"
 
@@ -301,8 +303,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       for (int t = 0; t < kChunk; ++t) acc[t] = sm.Vs[t * kLds + sv] - yp[t];
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
-        w[j] = sm.bs[j] * acc[j];
-        if ((j >> 3) == ch && j < nt) P.utape[((tc0 + j) * P.Hv + h) * kDim + sv] = acc[j];  // u_j for the backward
+        w[j] = sm.bs[j] * acc[j];  // acc[j] is final here: u_j
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           if (4 * q4 + 3 <= j) continue;
@@ -313,30 +314,39 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
             if (4 * q4 + e > j) acc[4 * q4 + e] = fmaf(-ar[e], w[j], acc[4 * q4 + e]);
         }
       }
+      // this warp's half of the tokens (compile-time, so B's zero upper triangle
+      // drops out): u tape, output, and one TF32 part of W
+      auto emit = [&](auto chc) {
+        constexpr int c_h = decltype(chc)::value;
 #pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        const int t = 8 * ch + tt;
-        float o = ch ? op[8 + tt] : op[tt];
+        for (int tt = 0; tt < 8; ++tt) {
+          const int t = 8 * c_h + tt;
+          if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
+          float o = op[t];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 x = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * q4]);
-          o = fmaf(x.x, w[4 * q4], o);  // B is zero above the diagonal
-          o = fmaf(x.y, w[4 * q4 + 1], o);
-          o = fmaf(x.z, w[4 * q4 + 2], o);
-          o = fmaf(x.w, w[4 * q4 + 3], o);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            if (4 * q4 > t) continue;
+            const float4 x = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * q4]);
+            const float br[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * q4 + e <= t) o = fmaf(br[e], w[4 * q4 + e], o);
+          }
+          if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o);
         }
-        if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o);
-      }
 #pragma unroll
-      for (int t4 = 0; t4 < 4; ++t4) {
-        float x[4];
+        for (int t4 = 0; t4 < 4; ++t4) {
+          float x[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float hi = tc::round_tf32(w[4 * t4 + e]);
-          x[e] = ch == 0 ? hi : tc::round_tf32(w[4 * t4 + e] - hi);
+          for (int e = 0; e < 4; ++e) {
+            const float hi = tc::round_tf32(w[4 * t4 + e]);
+            x[e] = c_h == 0 ? hi : tc::round_tf32(w[4 * t4 + e] - hi);
+          }
+          *reinterpret_cast<float4*>(sm.Wa[c_h] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(x[0], x[1], x[2], x[3]);
         }
-        *reinterpret_cast<float4*>(sm.Wa[ch] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(x[0], x[1], x[2], x[3]);
-      }
+      };
+      if (ch == 0) emit(std::integral_constant<int, 0>{});
+      else emit(std::integral_constant<int, 1>{});
     }
     tc::tmem_wait_st();
     tc::fence_async_smem();
