@@ -523,10 +523,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           tc::mma_ss(tbase + kColG, tc::kdesc(douv, st, 32), tc::kdesc(qkt, st, 32), i128, 1);
         }
 #pragma unroll
-        for (int st = 0; st < 2; ++st) {  // -k^g (columns 16..31 of QKT) with the dV lo part
+        for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) with the dV lo part, for G^T only:
+          // G (lanes v) is only ever read truncated to TF32, as the A operand of Gd (k^/g)^T
           tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
-          tc::mma_ss(tbase + kColG, tc::kdesc(dul, st, kChunk), tc::kdesc(qkt, 2 + st, 32), i128, 1);
-        }
         tc::mma_commit(mb2);
       }
       __syncwarp();
