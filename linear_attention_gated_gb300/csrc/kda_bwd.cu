@@ -57,7 +57,8 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;             // compute threads
+constexpr int kBlock = kThreads + 32;      // plus the MMA-issuing warp
 constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // G, FP32 accumulator (lanes v, columns k)
@@ -106,11 +107,23 @@ struct BwdSmem {
   float rho0[2][kDim];                    // halves of sum_v Gd * S0
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
   float dbp[4][kChunk];                   // per-warp partial dbeta
-  unsigned long long mbar[3];
+  unsigned long long mbar[5];
   uint32_t tmem_base;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Barrier among the compute warps only (the MMA-issuing warp does not take part).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ bool csync_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 1, %2, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(kThreads)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kBlock, 1)
 kda_bwd_kernel(const Problem P, const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
@@ -128,7 +141,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 3; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), 1);
+    for (int i = 0; i < 5; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), 1);
   }
   tc::fence_before();
   __syncthreads();
@@ -137,6 +150,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   const uint32_t tl = tbase + lane_off;
   const uint32_t mbD = tc::smem_u32(&sm.mbar[0]), mb1 = tc::smem_u32(&sm.mbar[1]);
   const uint32_t mb2 = tc::smem_u32(&sm.mbar[2]);
+  const uint32_t rdy1 = tc::smem_u32(&sm.mbar[3]), rdy2 = tc::smem_u32(&sm.mbar[4]);  // compute -> MMA warp
   uint32_t ph = 0;  // every barrier completes once per sub-chunk
   bool ok = true;
   bool aborted = false;
@@ -180,546 +194,556 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     tc::cp_async_commit();
   };
 
-  // G <- dfinal_state (lanes v) and G^T (lanes k)
-  {
-    const float* src = a.d_hT + (n * P.Hv + h) * kDim * kDim;
+  if (warp == kThreads / 32) {
+    // The MMA-issuing warp: one elected lane issues both groups of every
+    // sub-chunk once the compute warps signal that the operands are in place,
+    // so no compute warp is held by the tensor pipe's queue.
+    if (tc::elect_one()) {
+      uint32_t mph = 0;
+      for (int64_t c = nchunks - 1; c >= 0; --c) {
+        if (!tc::mbar_wait(rdy1, mph)) break;
+        tc::fence_after();
+        {
+          const uint32_t ki = tc::smem_u32(sm.Ki), s0 = tc::smem_u32(sm.S0s);
+          const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
+          const uint32_t douv = tc::smem_u32(sm.dOUv);
+          const uint32_t bsc[2] = {tc::smem_u32(sm.Bsc[0]), tc::smem_u32(sm.Bsc[1])};
+          const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
+#pragma unroll
+          for (int st = 0; st < kDim / 8; ++st)
+            tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, tc::kdesc(ki, st, kDim), i16, st > 0);
+#pragma unroll
+          for (int p = 0; p < 2; ++p)  // dO (rows v, exact in TF32) with scale B^T hi and lo
+#pragma unroll
+            for (int st = 0; st < 2; ++st)
+              tc::mma_ss(tbase + kColDW, tc::kdesc(douv, st, 32), tc::kdesc(bsc[p], st, kChunk), i16, 1);
+          tc::mma_commit(mbD);
+#pragma unroll
+          for (int st = 0; st < kDim / 8; ++st) {
+            tc::mma_ss(tbase + kColQ, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
+                       st > 0);
+            tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
+          }
+#pragma unroll
+          for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
+            tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
+          // dO W^T: the A tile is read as 128 rows from dOU on; rows 0..15 are dO
+          // and the rest (other shared-memory tiles) only fill D lanes 16..127,
+          // which are never read
+#pragma unroll
+          for (int st = 0; st < kDim / 8; ++st)
+            tc::mma_ss(tbase + kColM1, tc::kdesc(dou, st, kDim), tc::kdesc(wt, st, kDim), i32, st > 0);
+          tc::mma_commit(mb1);
+        }
+        if (!tc::mbar_wait(rdy2, mph)) break;
+        tc::fence_after();
+        {
+          const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
+          const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
+          const uint32_t s0 = tc::smem_u32(sm.S0s);
+          const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
+#pragma unroll
+          for (int st = 0; st < kDim / 8; ++st)
+            tc::mma_ss(tbase + kColR, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
+                       st > 0);
+#pragma unroll
+          for (int st = 0; st < 4; ++st) {
+            tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
+            tc::mma_ss(tbase + kColG, tc::kdesc(douv, st, 32), tc::kdesc(qkt, st, 32), i128, 1);
+          }
+#pragma unroll
+          for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) with the dV lo part, for G^T only:
+            // G (lanes v) is only ever read truncated to TF32, as the A operand of Gd (k^/g)^T
+            tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
+          tc::mma_commit(mb2);
+        }
+        mph ^= 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // G <- dfinal_state (lanes v) and G^T (lanes k)
+    {
+      const float* src = a.d_hT + (n * P.Hv + h) * kDim * kDim;
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int c0 = 64 * hv + 16 * q;
-      float x[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) x[j] = src[(c0 + j) * kDim + kl];
-      tc::tmem_st16(tl + kColGT + c0, x);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 y = *reinterpret_cast<const float4*>(src + kl * kDim + c0 + 4 * m);
-        x[4 * m] = y.x; x[4 * m + 1] = y.y; x[4 * m + 2] = y.z; x[4 * m + 3] = y.w;
-      }
-      tc::tmem_st16(tl + kColG + c0, x);
-    }
-    tc::tmem_wait_st();
-  }
-  prefetch_qkg(nchunks - 1);
-  prefetch_late(nchunks - 1);
-  prefetch_state(nchunks - 1);
-
-  const int ti = tid >> 4;
-  const int c8 = (tid & 15) * 8;
-  const float ea = expf(P.A_log[h]);
-  float dtb[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) dtb[e] = P.dt_bias[h * kDim + c8 + e];
-  float ddt_acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ddt_acc[e] = 0.f;
-  float dA_acc = 0.f;
-  float* cmb = reinterpret_cast<float*>(sm.Wt[0]);  // d q^, d k^, gauge / da tiles (after the MMAs)
-  const int ot = tid & 15, oq = tid >> 4;           // operand-tile mapping: token ot, quads oq, oq + 16
-
-  for (int64_t c = nchunks - 1; c >= 0; --c) {
-    const int64_t tc0 = si.t0 + c * kChunk;
-    const int nt = rows_of(c);
-    tc::cp_async_wait_all();
-    __syncthreads();
-    // ---- P0: prologue (token row ti, columns c8..c8+7): L2 norm, gate, sigmoid beta
-    float qhat[8], khat[8], zz[8], rq, rk;
-    {
-      float qv[8], kv[8], gv[8];
-      const bool valid = ti < nt;
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sq + ti * kDim + c8), qv);
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sk + ti * kDim + c8), kv);
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sg + ti * kDim + c8), gv);
-      float sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
-      sq = row16_sum(sq);
-      sk = row16_sum(sk);
-      rq = valid ? inv_norm_of(sq) : 0.f;
-      rk = valid ? inv_norm_of(sk) : 0.f;
-      float la[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        qhat[e] = qv[e] * rq;
-        khat[e] = kv[e] * rk;
-        zz[e] = ea * (gv[e] + dtb[e]);
-        la[e] = valid ? log_decay_of(P.lb, zz[e]) : 0.f;
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int o = 4 * hh;
-        *reinterpret_cast<float4*>(sm.Qtp + ti * kLds + c8 + o) = make_float4(qhat[o], qhat[o + 1], qhat[o + 2], qhat[o + 3]);
-        *reinterpret_cast<float4*>(sm.Ktp + ti * kLds + c8 + o) = make_float4(khat[o], khat[o + 1], khat[o + 2], khat[o + 3]);
-        *reinterpret_cast<float4*>(sm.Pa + ti * kLds + c8 + o) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
-      }
-      if (tid < kChunk) {
-        const float bl = __bfloat162float(nb);
-        sm.braw[tid] = bl;
-        sm.bs[tid] = (tid < nt) ? sigmoid_of(bl) : 0.f;
-      }
-    }
-    __syncthreads();
-    // ---- P1: cumulative decay (one key column per thread); the next q, k, g are fetched meanwhile
-    if (c > 0) prefetch_qkg(c - 1);
-    if (tid < kDim) {
-      float av[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) av[i] = sm.Pa[i * kLds + tid];
-      float G = 0.f;
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        G += av[i];
-        av[i] = expf(G);
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
-      sm.gC[tid] = av[kChunk - 1];
-    }
-    __syncthreads();
-    // ---- P2: decay of the adjoint, G <- G diag(gamma_C) (lanes v) and G^T <- diag(gamma_C) G^T
-    // (lanes k), with sum_v Gd * S0 from the FP32 checkpoint, the low part of Gd^T for the
-    // split Gd^T W^T, and S0 rounded to TF32 in place for the tensor core; then the operand tiles
-    {
-      const float gck = sm.gC[kl];
-      float4 racc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
       for (int q = 0; q < 4; ++q) {
         const int c0 = 64 * hv + 16 * q;
-        float g16[16], x16[16];
-        tc::tmem_ld16_nowait(tl + kColGT + c0, g16);
-        tc::tmem_ld16_nowait(tl + kColG + c0, x16);
-        float4 s4[4];
+        float x[16];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) s4[b] = *reinterpret_cast<const float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4);
-        tc::tmem_wait_ld2(g16, x16);
-        float lo16[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          g16[j] *= gck;
-          lo16[j] = g16[j] - __uint_as_float(__float_as_uint(g16[j]) & 0xFFFFE000u);
-        }
+        for (int j = 0; j < 16; ++j) x[j] = src[(c0 + j) * kDim + kl];
+        tc::tmem_st16(tl + kColGT + c0, x);
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          const float4 y = *reinterpret_cast<const float4*>(sm.gC + c0 + 4 * m);
-          x16[4 * m] *= y.x; x16[4 * m + 1] *= y.y; x16[4 * m + 2] *= y.z; x16[4 * m + 3] *= y.w;
+          const float4 y = *reinterpret_cast<const float4*>(src + kl * kDim + c0 + 4 * m);
+          x[4 * m] = y.x; x[4 * m + 1] = y.y; x[4 * m + 2] = y.z; x[4 * m + 3] = y.w;
         }
-        tc::tmem_st16(tl + kColGT + c0, g16);
-        tc::tmem_st16(tl + kColGL + c0, lo16);
-        tc::tmem_st16(tl + kColG + c0, x16);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          fma4(racc, make_float4(g16[4 * b], g16[4 * b + 1], g16[4 * b + 2], g16[4 * b + 3]), s4[b]);
-          *reinterpret_cast<float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4) =
-              make_float4(tc::round_tf32(s4[b].x), tc::round_tf32(s4[b].y), tc::round_tf32(s4[b].z),
-                          tc::round_tf32(s4[b].w));
-        }
+        tc::tmem_st16(tl + kColG + c0, x);
       }
-      sm.rho0[hv][kl] = hsum4(racc);
+      tc::tmem_wait_st();
     }
+    prefetch_qkg(nchunks - 1);
+    prefetch_late(nchunks - 1);
+    prefetch_state(nchunks - 1);
+
+    const int ti = tid >> 4;
+    const int c8 = (tid & 15) * 8;
+    const float ea = expf(P.A_log[h]);
+    float dtb[8];
 #pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int k0 = 4 * (oq + 16 * rep);
-      const float4 qh4 = *reinterpret_cast<const float4*>(sm.Qtp + ot * kLds + k0);
-      const float4 kh4 = *reinterpret_cast<const float4*>(sm.Ktp + ot * kLds + k0);
-      const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + ot * kLds + k0);
-      const float4 u4 = *reinterpret_cast<const float4*>(sm.Up + ot * kLds + k0);
-      const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
-      const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ua[4] = {u4.x, u4.y, u4.z, u4.w};
-      const float bt = sm.bs[ot];
-      float kt[4], qt[4], ki[4], whi[4], wlo[4], dof[4];
+    for (int e = 0; e < 8; ++e) dtb[e] = P.dt_bias[h * kDim + c8 + e];
+    float ddt_acc[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float inv = __fdividef(1.0f, ga[e]);  // gamma is in [e^-80, 1]
-        kt[e] = ka[e] * ga[e];
-        qt[e] = qa[e] * ga[e];
-        ki[e] = ka[e] * inv;
-        const float w = bt * ua[e];
-        whi[e] = tc::round_tf32(w);
-        wlo[e] = tc::round_tf32(w - whi[e]);
-        dof[e] = __bfloat162float(sm.dOp[ot * kDim + k0 + e]);
-        *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(k0 + e, ot, 32)) = dof[e];
-        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, ot, 32)) = tc::round_tf32(s * qt[e]);
-        *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, 16 + ot, 32)) = tc::round_tf32(-kt[e]);
-      }
-      *reinterpret_cast<float4*>(sm.Ktp + ot * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
-      *reinterpret_cast<float4*>(sm.Qtp + ot * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
-      *reinterpret_cast<float4*>(sm.Kip + ot * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
-      *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ot, k0, kDim)) =
-          make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
-      *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ot, k0, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
-      *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ot, k0, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
-      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ot, k0, kDim)) = make_float4(dof[0], dof[1], dof[2], dof[3]);
-    }
-    {  // scale B^T as rows t, K = j (B[j][t] is BsT[t][j]), split into TF32 hi + lo
-      const int t = tid >> 4, j = tid & 15;
-      const float x = s * sm.BsT[t][j];
-      const float hi = tc::round_tf32(x);
-      *reinterpret_cast<float*>(sm.Bsc[0] + tc::kmaj(t, j, kChunk)) = hi;
-      *reinterpret_cast<float*>(sm.Bsc[1] + tc::kmaj(t, j, kChunk)) = tc::round_tf32(x - hi);
-    }
-    tc::tmem_wait_st();
-    tc::fence_async_smem();
-    tc::fence_before();
-    __syncthreads();
-    // ---- MMA group 1: dW = Gd (k^/g)^T + scale dO^T B first (the dV chain needs it), then S0^T dO^T
-    // and Gd^T W^T
-    // (issued from warp 4, whose next work, dO W^T, is not needed until the combination)
-    if (warp == 4) {
-      if (tc::elect_one()) {
-        tc::fence_after();
-        const uint32_t ki = tc::smem_u32(sm.Ki), s0 = tc::smem_u32(sm.S0s);
-        const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
-        const uint32_t douv = tc::smem_u32(sm.dOUv);
-        const uint32_t bsc[2] = {tc::smem_u32(sm.Bsc[0]), tc::smem_u32(sm.Bsc[1])};
-        const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
-#pragma unroll
-        for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, tc::kdesc(ki, st, kDim), i16, st > 0);
-#pragma unroll
-        for (int p = 0; p < 2; ++p)  // dO (rows v, exact in TF32) with scale B^T hi and lo
-#pragma unroll
-          for (int st = 0; st < 2; ++st)
-            tc::mma_ss(tbase + kColDW, tc::kdesc(douv, st, 32), tc::kdesc(bsc[p], st, kChunk), i16, 1);
-        tc::mma_commit(mbD);
-#pragma unroll
-        for (int st = 0; st < kDim / 8; ++st) {
-          tc::mma_ss(tbase + kColQ, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
-                     st > 0);
-          tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
-        }
-#pragma unroll
-        for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
-          tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
-        // dO W^T: the A tile is read as 128 rows from dOU on; rows 0..15 are dO
-        // and the rest (other shared-memory tiles) only fill D lanes 16..127,
-        // which are never read
-#pragma unroll
-        for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ss(tbase + kColM1, tc::kdesc(dou, st, kDim), tc::kdesc(wt, st, kDim), i32, st > 0);
-        tc::mma_commit(mb1);
-      }
-      __syncwarp();
-    }
-    if (warp >= 4) {
-      // dO W^T = dO (W_hi + W_lo)^T from tensor memory (dO is exact in TF32)
-      ok = ok && tc::mbar_wait(mb1, ph);
-      tc::fence_after();
-      if (warp == 4) {
-        float hi16[16], lo16[16];
-        tc::tmem_ld16_nowait(tl + kColM1, hi16);
-        tc::tmem_ld16_nowait(tl + kColM1 + 16, lo16);
-        tc::tmem_wait_ld2(hi16, lo16);
-        if (lane < kChunk) {
-#pragma unroll
-          for (int j = 0; j < kChunk; ++j) {
-            const float m = hi16[j] + lo16[j];
-            sm.M1T[j][lane] = m;
-            hi16[j] = m;
-          }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<float4*>(&sm.M1[lane][4 * q4]) =
-                make_float4(hi16[4 * q4], hi16[4 * q4 + 1], hi16[4 * q4 + 2], hi16[4 * q4 + 3]);
-        }
-      }
-    } else {
-      ok = ok && tc::mbar_wait(mbD, ph);
-      tc::fence_after();
-      // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
-      const int vv = kl;
-      float acc[kChunk], pbv[kChunk];
-      tc::tmem_ld16(tl + kColDW, acc);  // dW (rows v)
-      // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
-      float bsv[kChunk], upv[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        bsv[i] = sm.bs[i];
-        upv[i] = sm.Up[i * kLds + vv];
-      }
-#pragma unroll
-      for (int i = kChunk - 1; i >= 0; --i) {
-        const float ei = acc[i];
-        const float du = bsv[i] * ei;
-        acc[i] = du;  // keep dV in place
-        float arow[kChunk];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 x = *reinterpret_cast<const float4*>(&sm.As[i][4 * q4]);
-          arow[4 * q4] = x.x; arow[4 * q4 + 1] = x.y; arow[4 * q4 + 2] = x.z; arow[4 * q4 + 3] = x.w;
-        }
-#pragma unroll
-        for (int m = 0; m < i; ++m) acc[m] = fmaf(-arow[m], du, acc[m]);
-        pbv[i] = ei * upv[i];
-      }
-      // dbeta partial sums over the warp's 32 value rows: halving butterfly
-      // (16 shuffles); lane l ends with the sum for token 8 b4 + 4 b3 + 2 b2 + b1
+    for (int e = 0; e < 8; ++e) ddt_acc[e] = 0.f;
+    float dA_acc = 0.f;
+    float* cmb = reinterpret_cast<float*>(sm.Wt[0]);  // d q^, d k^, gauge / da tiles (after the MMAs)
+    const int ot = tid & 15, oq = tid >> 4;           // operand-tile mapping: token ot, quads oq, oq + 16
+
+    for (int64_t c = nchunks - 1; c >= 0; --c) {
+      const int64_t tc0 = si.t0 + c * kChunk;
+      const int nt = rows_of(c);
+      tc::cp_async_wait_all();
+      csync();
+      // ---- P0: prologue (token row ti, columns c8..c8+7): L2 norm, gate, sigmoid beta
+      float qhat[8], khat[8], zz[8], rq, rk;
       {
-        float y8[8], y4[4], y2[2];
-        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+        float qv[8], kv[8], gv[8];
+        const bool valid = ti < nt;
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sq + ti * kDim + c8), qv);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sk + ti * kDim + c8), kv);
+        unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sg + ti * kDim + c8), gv);
+        float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float send = b4 ? pbv[j] : pbv[j + 8], keep = b4 ? pbv[j + 8] : pbv[j];
-          y8[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float send = b3 ? y8[j] : y8[j + 4], keep = b3 ? y8[j + 4] : y8[j];
-          y4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float send = b2 ? y4[j] : y4[j + 2], keep = b2 ? y4[j + 2] : y4[j];
-          y2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        const float send = b1 ? y2[0] : y2[1], keep = b1 ? y2[1] : y2[0];
-        float y1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-        if ((lane & 1) == 0) sm.dbp[warp][(b4 ? 8 : 0) + (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0)] = y1;
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(acc[i]);
-        sm.DUp[i * kLds + vv] = acc[i];
-      }
-#pragma unroll
-      for (int a4 = 0; a4 < 4; ++a4) {
-        float hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          hi[e] = tc::round_tf32(acc[4 * a4 + e]);
-          lo[e] = tc::round_tf32(acc[4 * a4 + e] - hi[e]);
-        }
-        *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(vv, 16 + 4 * a4, 32)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<float4*>(sm.dUlo + tc::kmaj(vv, 4 * a4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-    tc::fence_before();
-    __syncthreads();
-    // dV rows of the S0^T dV^T operand (token ot, quads oq and oq + 16)
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int k0 = 4 * (oq + 16 * rep);
-      const float4 d4 = *reinterpret_cast<const float4*>(sm.DUp + ot * kLds + k0);
-      *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(16 + ot, k0, kDim)) =
-          make_float4(tc::round_tf32(d4.x), tc::round_tf32(d4.y), tc::round_tf32(d4.z), tc::round_tf32(d4.w));
-    }
-    tc::fence_async_smem();
-    tc::fence_before();
-    __syncthreads();
-    // ---- MMA group 2: S0^T dV^T and the adjoint update of G and G^T
-    if (warp == 0) {
-      if (tc::elect_one()) {
-        tc::fence_after();
-        const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
-        const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
-        const uint32_t s0 = tc::smem_u32(sm.S0s);
-        const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
-#pragma unroll
-        for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ss(tbase + kColR, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
-                     st > 0);
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
-          tc::mma_ss(tbase + kColG, tc::kdesc(douv, st, 32), tc::kdesc(qkt, st, 32), i128, 1);
-        }
-#pragma unroll
-        for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) with the dV lo part, for G^T only:
-          // G (lanes v) is only ever read truncated to TF32, as the A operand of Gd (k^/g)^T
-          tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
-        tc::mma_commit(mb2);
-      }
-      __syncwarp();
-    }
-    if (warp >= 4) {  // dV W^T in FP32
-      const int t2 = tid - 128;
-#pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
-        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int vv = 0; vv < kDim; vv += 4)
-          fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
-               *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
-        const float acc = hsum4(a4);
-        sm.M2[i][j] = acc * sm.bs[j];
-        sm.M2T[j][i] = acc * sm.bs[j];
-      }
-    } else if (tid < kChunk) {
-      sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
-    }
-    ok = ok && tc::mbar_wait(mb1, ph);
-    ok = ok && tc::mbar_wait(mb2, ph);
-    tc::fence_after();
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
-    if (c > 0) {  // dO, u, A/B and S0 of this sub-chunk are no longer read
-      prefetch_late(c - 1);
-      prefetch_state(c - 1);
-    }
-    // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows i0 .. i0 + 7 with
-    // i0 = 8 hv a compile-time constant, so the triangular masks drop whole terms)
-    {
-      auto combine = [&](auto i0c) {
-        constexpr int i0 = decltype(i0c)::value;
-        float* dQh = cmb;
-        float* dKh = cmb + kTileF;
-        float* tv = cmb + 2 * kTileF;
-        float qd[8], rd[8], wh[8], wl[8];
-        tc::tmem_ld8(tl + kColQ + i0, qd);
-        tc::tmem_ld8(tl + kColR + i0, rd);
-        tc::tmem_ld8(tl + kColWG + i0, wh);
-        tc::tmem_ld8(tl + kColWG + 16 + i0, wl);
-        const int k = kl;
-        float kic[kChunk], qtc[kChunk], ktc[kChunk];
-#pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          kic[j] = sm.Kip[j * kLds + k];
-          qtc[j] = sm.Qtp[j * kLds + k];
-          ktc[j] = sm.Ktp[j * kLds + k];
-        }
-        float rp = 0.f;
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii) {
-          const int i = i0 + ii;
-          const float gam = sm.Pa[i * kLds + k];
-          const float inv = __fdividef(1.0f, gam);
-          const float wg = wh[ii] + wl[ii];
-          float pq = qd[ii], pr = rd[ii], pw = wg;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            if (4 * q4 <= i) {  // tril(M1) and stril(M2) rows
-              const float4 a4 = *reinterpret_cast<const float4*>(&sm.M1[i][4 * q4]);
-              const float4 b4 = *reinterpret_cast<const float4*>(&sm.M2[i][4 * q4]);
-              const float m1r[4] = {a4.x, a4.y, a4.z, a4.w}, m2r[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int j = 4 * q4 + e;
-                if (j <= i) pq = fmaf(m1r[e], kic[j], pq);
-                if (j < i) pr = fmaf(m2r[e], kic[j], pr);
-              }
-            }
-            if (4 * q4 + 3 >= i) {  // triu(M1^T) and striu(M2^T) rows
-              const float4 c4 = *reinterpret_cast<const float4*>(&sm.M1T[i][4 * q4]);
-              const float4 d4 = *reinterpret_cast<const float4*>(&sm.M2T[i][4 * q4]);
-              const float m1c[4] = {c4.x, c4.y, c4.z, c4.w}, m2c[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int j = 4 * q4 + e;
-                if (j >= i) pw = fmaf(s * m1c[e], qtc[j], pw);
-                if (j > i) pw = fmaf(-m2c[e], ktc[j], pw);
-              }
-            }
-          }
-          rp = fmaf(kic[i], wg, rp);
-          const float dq_ = s * gam * pq;
-          const float dkr = -gam * pr;
-          const float dkw = inv * pw;
-          dQh[i * kLds + k] = dq_;
-          dKh[i * kLds + k] = dkr + dkw;
-          tv[i * kLds + k] = qtc[i] * inv * dq_ + ktc[i] * inv * (dkr - dkw);
-        }
-        sm.rho2[i0 / 8][k] = rp;
-      };
-      if (hv == 0) combine(std::integral_constant<int, 0>{});
-      else combine(std::integral_constant<int, 8>{});
-    }
-    __syncthreads();
-    // ---- P8: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
-    if (tid < kDim) {
-      float* tv = cmb + 2 * kTileF;
-      float run = sm.rho0[0][tid] + sm.rho0[1][tid] + sm.rho2[0][tid] + sm.rho2[1][tid];
-#pragma unroll
-      for (int i = kChunk - 1; i >= 0; --i) {
-        run += tv[i * kLds + tid];
-        tv[i * kLds + tid] = run;
-      }
-    }
-    __syncthreads();
-    // ---- P9: epilogue: gate / sigmoid / L2-norm backward and stores
-    {
-      const float* dQh = cmb;
-      const float* dKh = cmb + kTileF;
-      const float* da = cmb + 2 * kTileF;
-      const bool valid = ti < nt;
-      const int64_t t = tc0 + ti;
-      float dg8[8], dq8[8], dk8[8];
-      float pq = 0.f, pk = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        // sigmoid'(z) = sigmoid(z) sigmoid(-z) = e / (1 + e)^2 with e = exp(-|z|) (no cancellation)
-        const float ex = __expf(-fabsf(zz[e]));
-        const float den = __fdividef(1.0f, 1.0f + ex);
-        const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * ex * den * den : 0.f;
-        dg8[e] = dz * ea;
-        ddt_acc[e] += dg8[e];
-        dA_acc += dz * zz[e];
-        dq8[e] = dQh[ti * kLds + c8 + e];
-        dk8[e] = dKh[ti * kLds + c8 + e];
-        pq += qhat[e] * dq8[e];
-        pk += khat[e] * dk8[e];
-      }
-      if (P.r == 1) {
-        pq = row16_sum(pq);
-        pk = row16_sum(pk);
+        for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+        sq = row16_sum(sq);
+        sk = row16_sum(sk);
+        rq = valid ? inv_norm_of(sq) : 0.f;
+        rk = valid ? inv_norm_of(sk) : 0.f;
+        float la[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          dq8[e] = rq * (dq8[e] - qhat[e] * pq);
-          dk8[e] = rk * (dk8[e] - khat[e] * pk);
+          qhat[e] = qv[e] * rq;
+          khat[e] = kv[e] * rk;
+          zz[e] = ea * (gv[e] + dtb[e]);
+          la[e] = valid ? log_decay_of(P.lb, zz[e]) : 0.f;
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int o = 4 * hh;
+          *reinterpret_cast<float4*>(sm.Qtp + ti * kLds + c8 + o) = make_float4(qhat[o], qhat[o + 1], qhat[o + 2], qhat[o + 3]);
+          *reinterpret_cast<float4*>(sm.Ktp + ti * kLds + c8 + o) = make_float4(khat[o], khat[o + 1], khat[o + 2], khat[o + 3]);
+          *reinterpret_cast<float4*>(sm.Pa + ti * kLds + c8 + o) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
+        }
+        if (tid < kChunk) {
+          const float bl = __bfloat162float(nb);
+          sm.braw[tid] = bl;
+          sm.bs[tid] = (tid < nt) ? sigmoid_of(bl) : 0.f;
         }
       }
-      if (valid) {
-        store_bf16x8(a.dg + (t * P.Hv + h) * kDim + c8, dg8);
+      csync();
+      // ---- P1: cumulative decay (one key column per thread); the next q, k, g are fetched meanwhile
+      if (c > 0) prefetch_qkg(c - 1);
+      if (tid < kDim) {
+        float av[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) av[i] = sm.Pa[i * kLds + tid];
+        float G = 0.f;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+          G += av[i];
+          av[i] = expf(G);
+        }
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
+        sm.gC[tid] = av[kChunk - 1];
+      }
+      csync();
+      // ---- P2: decay of the adjoint, G <- G diag(gamma_C) (lanes v) and G^T <- diag(gamma_C) G^T
+      // (lanes k), with sum_v Gd * S0 from the FP32 checkpoint, the low part of Gd^T for the
+      // split Gd^T W^T, and S0 rounded to TF32 in place for the tensor core; then the operand tiles
+      {
+        const float gck = sm.gC[kl];
+        float4 racc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+        for (int q = 0; q < 4; ++q) {
+          const int c0 = 64 * hv + 16 * q;
+          float g16[16], x16[16];
+          tc::tmem_ld16_nowait(tl + kColGT + c0, g16);
+          tc::tmem_ld16_nowait(tl + kColG + c0, x16);
+          float4 s4[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) s4[b] = *reinterpret_cast<const float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4);
+          tc::tmem_wait_ld2(g16, x16);
+          float lo16[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            g16[j] *= gck;
+            lo16[j] = g16[j] - __uint_as_float(__float_as_uint(g16[j]) & 0xFFFFE000u);
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 y = *reinterpret_cast<const float4*>(sm.gC + c0 + 4 * m);
+            x16[4 * m] *= y.x; x16[4 * m + 1] *= y.y; x16[4 * m + 2] *= y.z; x16[4 * m + 3] *= y.w;
+          }
+          tc::tmem_st16(tl + kColGT + c0, g16);
+          tc::tmem_st16(tl + kColGL + c0, lo16);
+          tc::tmem_st16(tl + kColG + c0, x16);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            fma4(racc, make_float4(g16[4 * b], g16[4 * b + 1], g16[4 * b + 2], g16[4 * b + 3]), s4[b]);
+            *reinterpret_cast<float4*>(sm.S0s + ckpt_index(c0 + 4 * b, kl) * 4) =
+                make_float4(tc::round_tf32(s4[b].x), tc::round_tf32(s4[b].y), tc::round_tf32(s4[b].z),
+                            tc::round_tf32(s4[b].w));
+          }
+        }
+        sm.rho0[hv][kl] = hsum4(racc);
+      }
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int k0 = 4 * (oq + 16 * rep);
+        const float4 qh4 = *reinterpret_cast<const float4*>(sm.Qtp + ot * kLds + k0);
+        const float4 kh4 = *reinterpret_cast<const float4*>(sm.Ktp + ot * kLds + k0);
+        const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + ot * kLds + k0);
+        const float4 u4 = *reinterpret_cast<const float4*>(sm.Up + ot * kLds + k0);
+        const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
+        const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ua[4] = {u4.x, u4.y, u4.z, u4.w};
+        const float bt = sm.bs[ot];
+        float kt[4], qt[4], ki[4], whi[4], wlo[4], dof[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float inv = __fdividef(1.0f, ga[e]);  // gamma is in [e^-80, 1]
+          kt[e] = ka[e] * ga[e];
+          qt[e] = qa[e] * ga[e];
+          ki[e] = ka[e] * inv;
+          const float w = bt * ua[e];
+          whi[e] = tc::round_tf32(w);
+          wlo[e] = tc::round_tf32(w - whi[e]);
+          dof[e] = __bfloat162float(sm.dOp[ot * kDim + k0 + e]);
+          *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(k0 + e, ot, 32)) = dof[e];
+          *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, ot, 32)) = tc::round_tf32(s * qt[e]);
+          *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, 16 + ot, 32)) = tc::round_tf32(-kt[e]);
+        }
+        *reinterpret_cast<float4*>(sm.Ktp + ot * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
+        *reinterpret_cast<float4*>(sm.Qtp + ot * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
+        *reinterpret_cast<float4*>(sm.Kip + ot * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
+        *reinterpret_cast<float4*>(sm.Ki + tc::kmaj(ot, k0, kDim)) =
+            make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
+        *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ot, k0, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
+        *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ot, k0, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
+        *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ot, k0, kDim)) = make_float4(dof[0], dof[1], dof[2], dof[3]);
+      }
+      {  // scale B^T as rows t, K = j (B[j][t] is BsT[t][j]), split into TF32 hi + lo
+        const int t = tid >> 4, j = tid & 15;
+        const float x = s * sm.BsT[t][j];
+        const float hi = tc::round_tf32(x);
+        *reinterpret_cast<float*>(sm.Bsc[0] + tc::kmaj(t, j, kChunk)) = hi;
+        *reinterpret_cast<float*>(sm.Bsc[1] + tc::kmaj(t, j, kChunk)) = tc::round_tf32(x - hi);
+      }
+      tc::tmem_wait_st();
+      tc::fence_async_smem();
+      tc::fence_before();
+      csync();
+      // ---- MMA group 1 (issued by the MMA warp): dW = Gd (k^/g)^T + scale dO^T B first (the dV
+      // chain needs it), then S0^T dO^T, Gd^T W^T and dO W^T
+      if (tid == 0) tc::mbar_arrive(rdy1);  // operands of the first MMA group are in place
+      if (warp >= 4) {
+        // dO W^T = dO (W_hi + W_lo)^T from tensor memory (dO is exact in TF32)
+        ok = ok && tc::mbar_wait(mb1, ph);
+        tc::fence_after();
+        if (warp == 4) {
+          float hi16[16], lo16[16];
+          tc::tmem_ld16_nowait(tl + kColM1, hi16);
+          tc::tmem_ld16_nowait(tl + kColM1 + 16, lo16);
+          tc::tmem_wait_ld2(hi16, lo16);
+          if (lane < kChunk) {
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+              const float m = hi16[j] + lo16[j];
+              sm.M1T[j][lane] = m;
+              hi16[j] = m;
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<float4*>(&sm.M1[lane][4 * q4]) =
+                  make_float4(hi16[4 * q4], hi16[4 * q4 + 1], hi16[4 * q4 + 2], hi16[4 * q4 + 3]);
+          }
+        }
+      } else {
+        ok = ok && tc::mbar_wait(mbD, ph);
+        tc::fence_after();
+        // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
+        const int vv = kl;
+        float acc[kChunk], pbv[kChunk];
+        tc::tmem_ld16(tl + kColDW, acc);  // dW (rows v)
+        // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
+        float bsv[kChunk], upv[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+          bsv[i] = sm.bs[i];
+          upv[i] = sm.Up[i * kLds + vv];
+        }
+#pragma unroll
+        for (int i = kChunk - 1; i >= 0; --i) {
+          const float ei = acc[i];
+          const float du = bsv[i] * ei;
+          acc[i] = du;  // keep dV in place
+          float arow[kChunk];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 x = *reinterpret_cast<const float4*>(&sm.As[i][4 * q4]);
+            arow[4 * q4] = x.x; arow[4 * q4 + 1] = x.y; arow[4 * q4 + 2] = x.z; arow[4 * q4 + 3] = x.w;
+          }
+#pragma unroll
+          for (int m = 0; m < i; ++m) acc[m] = fmaf(-arow[m], du, acc[m]);
+          pbv[i] = ei * upv[i];
+        }
+        // dbeta partial sums over the warp's 32 value rows: halving butterfly
+        // (16 shuffles); lane l ends with the sum for token 8 b4 + 4 b3 + 2 b2 + b1
+        {
+          float y8[8], y4[4], y2[2];
+          const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float send = b4 ? pbv[j] : pbv[j + 8], keep = b4 ? pbv[j + 8] : pbv[j];
+            y8[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float send = b3 ? y8[j] : y8[j + 4], keep = b3 ? y8[j + 4] : y8[j];
+            y4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float send = b2 ? y4[j] : y4[j + 2], keep = b2 ? y4[j + 2] : y4[j];
+            y2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+          }
+          const float send = b1 ? y2[0] : y2[1], keep = b1 ? y2[1] : y2[0];
+          float y1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+          y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+          if ((lane & 1) == 0) sm.dbp[warp][(b4 ? 8 : 0) + (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0)] = y1;
+        }
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+          if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(acc[i]);
+          sm.DUp[i * kLds + vv] = acc[i];
+        }
+#pragma unroll
+        for (int a4 = 0; a4 < 4; ++a4) {
+          float hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = tc::round_tf32(acc[4 * a4 + e]);
+            lo[e] = tc::round_tf32(acc[4 * a4 + e] - hi[e]);
+          }
+          *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(vv, 16 + 4 * a4, 32)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<float4*>(sm.dUlo + tc::kmaj(vv, 4 * a4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      tc::fence_before();
+      csync();
+      // dV rows of the S0^T dV^T operand (token ot, quads oq and oq + 16)
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int k0 = 4 * (oq + 16 * rep);
+        const float4 d4 = *reinterpret_cast<const float4*>(sm.DUp + ot * kLds + k0);
+        *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(16 + ot, k0, kDim)) =
+            make_float4(tc::round_tf32(d4.x), tc::round_tf32(d4.y), tc::round_tf32(d4.z), tc::round_tf32(d4.w));
+      }
+      tc::fence_async_smem();
+      tc::fence_before();
+      csync();
+      // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T
+      if (tid == 0) tc::mbar_arrive(rdy2);  // operands of the second MMA group are in place
+      if (warp >= 4) {  // dV W^T in FP32
+        const int t2 = tid - 128;
+#pragma unroll
+        for (int rep = 0; rep < 2; ++rep) {
+          const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
+          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+          for (int vv = 0; vv < kDim; vv += 4)
+            fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
+                 *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
+          const float acc = hsum4(a4);
+          sm.M2[i][j] = acc * sm.bs[j];
+          sm.M2T[j][i] = acc * sm.bs[j];
+        }
+      } else if (tid < kChunk) {
+        sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
+      }
+      ok = ok && tc::mbar_wait(mb1, ph);
+      ok = ok && tc::mbar_wait(mb2, ph);
+      tc::fence_after();
+      if (csync_or(!ok)) { aborted = true; break; }
+      if (c > 0) {  // dO, u, A/B and S0 of this sub-chunk are no longer read
+        prefetch_late(c - 1);
+        prefetch_state(c - 1);
+      }
+      // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows i0 .. i0 + 7 with
+      // i0 = 8 hv a compile-time constant, so the triangular masks drop whole terms)
+      {
+        auto combine = [&](auto i0c) {
+          constexpr int i0 = decltype(i0c)::value;
+          float* dQh = cmb;
+          float* dKh = cmb + kTileF;
+          float* tv = cmb + 2 * kTileF;
+          float qd[8], rd[8], wh[8], wl[8];
+          tc::tmem_ld8(tl + kColQ + i0, qd);
+          tc::tmem_ld8(tl + kColR + i0, rd);
+          tc::tmem_ld8(tl + kColWG + i0, wh);
+          tc::tmem_ld8(tl + kColWG + 16 + i0, wl);
+          const int k = kl;
+          float kic[kChunk], qtc[kChunk], ktc[kChunk];
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) {
+            kic[j] = sm.Kip[j * kLds + k];
+            qtc[j] = sm.Qtp[j * kLds + k];
+            ktc[j] = sm.Ktp[j * kLds + k];
+          }
+          float rp = 0.f;
+#pragma unroll
+          for (int ii = 0; ii < 8; ++ii) {
+            const int i = i0 + ii;
+            const float gam = sm.Pa[i * kLds + k];
+            const float inv = __fdividef(1.0f, gam);
+            const float wg = wh[ii] + wl[ii];
+            float pq = qd[ii], pr = rd[ii], pw = wg;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              if (4 * q4 <= i) {  // tril(M1) and stril(M2) rows
+                const float4 a4 = *reinterpret_cast<const float4*>(&sm.M1[i][4 * q4]);
+                const float4 b4 = *reinterpret_cast<const float4*>(&sm.M2[i][4 * q4]);
+                const float m1r[4] = {a4.x, a4.y, a4.z, a4.w}, m2r[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 4 * q4 + e;
+                  if (j <= i) pq = fmaf(m1r[e], kic[j], pq);
+                  if (j < i) pr = fmaf(m2r[e], kic[j], pr);
+                }
+              }
+              if (4 * q4 + 3 >= i) {  // triu(M1^T) and striu(M2^T) rows
+                const float4 c4 = *reinterpret_cast<const float4*>(&sm.M1T[i][4 * q4]);
+                const float4 d4 = *reinterpret_cast<const float4*>(&sm.M2T[i][4 * q4]);
+                const float m1c[4] = {c4.x, c4.y, c4.z, c4.w}, m2c[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 4 * q4 + e;
+                  if (j >= i) pw = fmaf(s * m1c[e], qtc[j], pw);
+                  if (j > i) pw = fmaf(-m2c[e], ktc[j], pw);
+                }
+              }
+            }
+            rp = fmaf(kic[i], wg, rp);
+            const float dq_ = s * gam * pq;
+            const float dkr = -gam * pr;
+            const float dkw = inv * pw;
+            dQh[i * kLds + k] = dq_;
+            dKh[i * kLds + k] = dkr + dkw;
+            tv[i * kLds + k] = qtc[i] * inv * dq_ + ktc[i] * inv * (dkr - dkw);
+          }
+          sm.rho2[i0 / 8][k] = rp;
+        };
+        if (hv == 0) combine(std::integral_constant<int, 0>{});
+        else combine(std::integral_constant<int, 8>{});
+      }
+      csync();
+      // ---- P8: da = rho + reverse cumulative sum of the gauge term within the sub-chunk
+      if (tid < kDim) {
+        float* tv = cmb + 2 * kTileF;
+        float run = sm.rho0[0][tid] + sm.rho0[1][tid] + sm.rho2[0][tid] + sm.rho2[1][tid];
+#pragma unroll
+        for (int i = kChunk - 1; i >= 0; --i) {
+          run += tv[i * kLds + tid];
+          tv[i * kLds + tid] = run;
+        }
+      }
+      csync();
+      // ---- P9: epilogue: gate / sigmoid / L2-norm backward and stores
+      {
+        const float* dQh = cmb;
+        const float* dKh = cmb + kTileF;
+        const float* da = cmb + 2 * kTileF;
+        const bool valid = ti < nt;
+        const int64_t t = tc0 + ti;
+        float dg8[8], dq8[8], dk8[8];
+        float pq = 0.f, pk = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          // sigmoid'(z) = sigmoid(z) sigmoid(-z) = e / (1 + e)^2 with e = exp(-|z|) (no cancellation)
+          const float ex = __expf(-fabsf(zz[e]));
+          const float den = __fdividef(1.0f, 1.0f + ex);
+          const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * ex * den * den : 0.f;
+          dg8[e] = dz * ea;
+          ddt_acc[e] += dg8[e];
+          dA_acc += dz * zz[e];
+          dq8[e] = dQh[ti * kLds + c8 + e];
+          dk8[e] = dKh[ti * kLds + c8 + e];
+          pq += qhat[e] * dq8[e];
+          pk += khat[e] * dk8[e];
+        }
         if (P.r == 1) {
-          store_bf16x8(a.dq + (t * P.Hqk + qh) * kDim + c8, dq8);
-          store_bf16x8(a.dk + (t * P.Hqk + qh) * kDim + c8, dk8);
-        } else {
-          float* dst = a.dqk_part + ((t * P.Hv + h) * 2) * kDim + c8;
-          *reinterpret_cast<float4*>(dst) = make_float4(dq8[0], dq8[1], dq8[2], dq8[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(dq8[4], dq8[5], dq8[6], dq8[7]);
-          *reinterpret_cast<float4*>(dst + kDim) = make_float4(dk8[0], dk8[1], dk8[2], dk8[3]);
-          *reinterpret_cast<float4*>(dst + kDim + 4) = make_float4(dk8[4], dk8[5], dk8[6], dk8[7]);
+          pq = row16_sum(pq);
+          pk = row16_sum(pk);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            dq8[e] = rq * (dq8[e] - qhat[e] * pq);
+            dk8[e] = rk * (dk8[e] - khat[e] * pk);
+          }
+        }
+        if (valid) {
+          store_bf16x8(a.dg + (t * P.Hv + h) * kDim + c8, dg8);
+          if (P.r == 1) {
+            store_bf16x8(a.dq + (t * P.Hqk + qh) * kDim + c8, dq8);
+            store_bf16x8(a.dk + (t * P.Hqk + qh) * kDim + c8, dk8);
+          } else {
+            float* dst = a.dqk_part + ((t * P.Hv + h) * 2) * kDim + c8;
+            *reinterpret_cast<float4*>(dst) = make_float4(dq8[0], dq8[1], dq8[2], dq8[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(dq8[4], dq8[5], dq8[6], dq8[7]);
+            *reinterpret_cast<float4*>(dst + kDim) = make_float4(dk8[0], dk8[1], dk8[2], dk8[3]);
+            *reinterpret_cast<float4*>(dst + kDim + 4) = make_float4(dk8[4], dk8[5], dk8[6], dk8[7]);
+          }
+        }
+        if (tid < nt) {
+          const float bn = sigmoid_of(-sm.braw[tid]);
+          a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
         }
       }
-      if (tid < nt) {
-        const float bn = sigmoid_of(-sm.braw[tid]);
-        a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
-      }
+      ph ^= 1;
+      tc::fence_before();
     }
-    ph ^= 1;
-    tc::fence_before();
-  }
-  tc::cp_async_wait_all();
-  __syncthreads();
-  if (!aborted) {
-    // dinitial_state = G (from its transposed copy, for coalesced stores)
-    float* dst = a.dh0 + (n * P.Hv + h) * kDim * kDim;
-    tc::fence_after();
+    tc::cp_async_wait_all();
+    csync();
+    if (!aborted) {
+      // dinitial_state = G (from its transposed copy, for coalesced stores)
+      float* dst = a.dh0 + (n * P.Hv + h) * kDim * kDim;
+      tc::fence_after();
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      const int v0 = 64 * hv + 16 * q;
-      float x[16];
-      tc::tmem_ld16(tl + kColGT + v0, x);
+      for (int q = 0; q < 4; ++q) {
+        const int v0 = 64 * hv + 16 * q;
+        float x[16];
+        tc::tmem_ld16(tl + kColGT + v0, x);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) dst[(v0 + j) * kDim + kl] = x[j];
-    }
-    // per-unit parameter-gradient partials, reduced in a fixed order
-    float* red = sm.Qtp;  // [16 rows][128] + [256]: spans Qtp and Ktp
+        for (int j = 0; j < 16; ++j) dst[(v0 + j) * kDim + kl] = x[j];
+      }
+      // per-unit parameter-gradient partials, reduced in a fixed order
+      float* red = sm.Qtp;  // [16 rows][128] + [256]: spans Qtp and Ktp
 #pragma unroll
-    for (int e = 0; e < 8; ++e) red[ti * kDim + c8 + e] = ddt_acc[e];
-    red[kChunk * kDim + tid] = dA_acc;
-    __syncthreads();
-    float* pp = a.par_part + (int64_t)unit * kParStride;
-    if (tid < kDim) {
-      float acc = 0.f;
-      for (int i = 0; i < kChunk; ++i) acc += red[i * kDim + tid];
-      pp[tid] = acc;
+      for (int e = 0; e < 8; ++e) red[ti * kDim + c8 + e] = ddt_acc[e];
+      red[kChunk * kDim + tid] = dA_acc;
+      csync();
+      float* pp = a.par_part + (int64_t)unit * kParStride;
+      if (tid < kDim) {
+        float acc = 0.f;
+        for (int i = 0; i < kChunk; ++i) acc += red[i * kDim + tid];
+        pp[tid] = acc;
+      }
+      if (tid == 0) {
+        float acc = 0.f;
+        for (int i = 0; i < kThreads; ++i) acc += red[kChunk * kDim + i];
+        pp[kDim] = acc;
+      }
+    } else if (tid == 0) {
+      atomicExch(P.status, 1);
     }
-    if (tid == 0) {
-      float acc = 0.f;
-      for (int i = 0; i < kThreads; ++i) acc += red[kChunk * kDim + i];
-      pp[kDim] = acc;
-    }
-  } else if (tid == 0) {
-    atomicExch(P.status, 1);
   }
   tc::fence_before();
   __syncthreads();
@@ -789,7 +813,7 @@ cudaError_t launch_backward(const Problem& P, const BwdArgs& a, int64_t units, i
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  kda_bwd_kernel<<<(unsigned)units, kThreads, smem, s>>>(P, a);
+  kda_bwd_kernel<<<(unsigned)units, kBlock, smem, s>>>(P, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   kda_param_reduce_kernel<<<(unsigned)P.Hv, kDim + 1, 0, s>>>(a.par_part, P.N, P.Hv, dA_log, ddt_bias);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -88,6 +88,11 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
 
 // Bounded wait for the given phase parity (about two seconds of SM clock);
 // false if it gave up.
+// Plain arrive (release at CTA scope) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
   const long long t0 = clock64();
   while (true) {
