@@ -44,14 +44,18 @@ constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 256;  // two CTAs per SM share the 512 columns
 constexpr uint32_t kColS = 0;        // FP32 state S (lane = value row v, column = key k)
 constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns
+constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T : lanes 0..31, 16 columns (A and B)
 
 struct FwdSmem {
-  unsigned char KQ[32 * kDim * 4];         // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128)
+  // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128). As the A operand of the A/B
+  // product it is read as 128 rows: rows 32..127 fall on the tiles below and only fill TMEM
+  // lanes that are never read.
+  unsigned char KQ[32 * kDim * 4];
+  unsigned char KiT[kChunk * kDim * 4];    // k^ / gamma rows t, TF32 (K-major, K = 128)
   unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo (K = 16)
   unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo                     (K = 16)
-  float Pq[kTileF];                        // q^, then q^ gamma
-  float Pk[kTileF];                        // k^, then k^ gamma
-  float Pi[kTileF];                        // k^ / gamma
+  float Pq[kTileF];                        // q^
+  float Pk[kTileF];                        // k^
   float Pa[kTileF];                        // log decay, then gamma
   float Vs[kTileF];                        // v
   float AsT[kChunk][kChunk];               // A transposed: AsT[j][t] = A[t][j]
@@ -216,51 +220,62 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
             make_float4(tc::round_tf32(kt[0]), tc::round_tf32(kt[1]), tc::round_tf32(kt[2]), tc::round_tf32(kt[3]));
         *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(16 + t, k0, kDim)) =
             make_float4(tc::round_tf32(qt[0]), tc::round_tf32(qt[1]), tc::round_tf32(qt[2]), tc::round_tf32(qt[3]));
-        // plain FP32 copies for the 16x16 A and B (overwriting q^ / k^ of the same elements)
-        *reinterpret_cast<float4*>(sm.Pk + t * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
-        *reinterpret_cast<float4*>(sm.Pq + t * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
-        *reinterpret_cast<float4*>(sm.Pi + t * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
+        *reinterpret_cast<float4*>(sm.KiT + tc::kmaj(t, k0, kDim)) =
+            make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
       }
     }
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- tensor cores: S0 [k^g; q^g]^T with the state read from tensor memory
+    // ---- tensor cores: S0 [k^g; q^g]^T with the state read from tensor memory, and the 16x16
+    // A_ij = (k^g)_i . (k^/g)_j, B_ij = (q^g)_i . (k^/g)_j (TF32 operands, FP32 accumulation)
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
-        const uint32_t kq = tc::smem_u32(sm.KQ);
+        const uint32_t kq = tc::smem_u32(sm.KQ), kit = tc::smem_u32(sm.KiT);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
           tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, tc::kdesc(kq, st, kDim), tc::idesc_tf32(128, 32), st > 0);
+#pragma unroll
+        for (int st = 0; st < kDim / 8; ++st)
+          tc::mma_ss(tbase + kColAB, tc::kdesc(kq, st, kDim), tc::kdesc(kit, st, kDim), tc::idesc_tf32(128, 16), st > 0);
         tc::mma_commit(mbar);
       }
       __syncwarp();
     }
-    // ---- meanwhile, A_ij = (k^g)_i . (k^/g)_j (j < i) and B_ij = (q^g)_i . (k^/g)_j (j <= i) in FP32
-    {
-      const int mat = tid >> 7, i = (tid & 127) >> 3, j0 = tid & 7;
-      const float* X = mat ? sm.Pq : sm.Pk;
-#pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int j = j0 + 8 * rep;
-        float acc = 0.f;
-        if (j < i || (mat && j == i)) {
-          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-          for (int kk = 0; kk < kDim; kk += 4)
-            fma4(a4, *reinterpret_cast<const float4*>(X + i * kLds + kk),
-                 *reinterpret_cast<const float4*>(sm.Pi + j * kLds + kk));
-          acc = hsum4(a4);
-        }
-        if (mat) sm.Bs[i][j] = acc; else sm.AsT[j][i] = acc;
-        // for the backward: A row-major, B transposed (its columns are read there)
-        P.abtape[((si.ch_base + c) * P.Hv + h) * 512 + (mat ? 256 + j * 16 + i : i * 16 + j)] = acc;
-      }
-    }
     ok = ok && tc::mbar_wait(mbar, parity);
     parity ^= 1;
     tc::fence_after();
+    if (warp == 0) {
+      // A (lanes 0..15, strictly lower) and B (lanes 16..31, lower) from tensor memory; for
+      // the backward the tape holds A row-major and B transposed (its columns are read there)
+      float d16[16];
+      tc::tmem_ld16(tl + kColAB, d16);
+      float* tape = P.abtape + ((si.ch_base + c) * P.Hv + h) * 512;
+      if (lane < kChunk) {
+        const int i = lane;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          d16[j] = j < i ? d16[j] : 0.f;
+          sm.AsT[j][i] = d16[j];
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<float4*>(tape + i * 16 + 4 * q4) =
+              make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
+      } else {
+        const int i = lane - kChunk;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          d16[j] = j <= i ? d16[j] : 0.f;
+          tape[256 + j * 16 + i] = d16[j];
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<float4*>(&sm.Bs[i][4 * q4]) =
+              make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
+      }
+    }
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     // ---- state checkpoint and decay S <- S0 diag(gamma_C) in tensor memory
     {
