@@ -43,7 +43,7 @@ constexpr int kThreads = 256;
 constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 256;  // two CTAs per SM share the 512 columns
 constexpr uint32_t kColS = 0;        // FP32 state S (lane = value row v, column = key k)
-constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns
+constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns; the last 16 then also take + W^T B^T
 constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T : lanes 0..31, 16 columns (A and B)
 
 struct FwdSmem {
@@ -52,6 +52,7 @@ struct FwdSmem {
   // lanes that are never read.
   unsigned char KQ[32 * kDim * 4];
   unsigned char KiT[kChunk * kDim * 4];    // k^ / gamma rows t, TF32 (K-major, K = 128)
+  unsigned char Bt[kChunk * kChunk * 4];   // B rows t, TF32 (K-major, K = 16): O += W^T B^T
   unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo (K = 16)
   unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo                     (K = 16)
   float Pq[kTileF];                        // q^
@@ -59,7 +60,6 @@ struct FwdSmem {
   float Pa[kTileF];                        // log decay, then gamma
   float Vs[kTileF];                        // v
   float AsT[kChunk][kChunk];               // A transposed: AsT[j][t] = A[t][j]
-  float Bs[kChunk][kChunk];
   float bs[kChunk];
   float gC[kDim];
   unsigned long long mbar;
@@ -271,9 +271,11 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
           tape[256 + j * 16 + i] = d16[j];
         }
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<float4*>(&sm.Bs[i][4 * q4]) =
-              make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          *reinterpret_cast<float4*>(sm.Bt + tc::kmaj(i, 4 * q4, kChunk)) =
+              make_float4(tc::round_tf32(d16[4 * q4]), tc::round_tf32(d16[4 * q4 + 1]), tc::round_tf32(d16[4 * q4 + 2]),
+                          tc::round_tf32(d16[4 * q4 + 3]));
+        }
       }
     }
     if (__syncthreads_or(!ok)) { aborted = true; break; }
@@ -305,12 +307,12 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
         tc::tmem_st16(tl + kColS + col, x);
       }
     }
-    // ---- W by forward substitution and the output: both warps of a state row
-    // solve for W; each then writes half of the tokens and one TF32 part of W
+    // ---- W by forward substitution: both warps of a state row solve for W; each then
+    // writes the u tape of half of the tokens and one TF32 part of W (the output's B W term
+    // is added by the tensor core with the state update)
     {
-      float yp[16], op[16];
+      float yp[16];
       tc::tmem_ld16(tl + kColYO, yp);
-      tc::tmem_ld16(tl + kColYO + 16, op);
       // right-looking substitution: once w_j is known it is removed from every
       // later row, so the dependent chain is one FMA per token
       float w[kChunk], acc[kChunk];
@@ -329,25 +331,13 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
             if (4 * q4 + e > j) acc[4 * q4 + e] = fmaf(-ar[e], w[j], acc[4 * q4 + e]);
         }
       }
-      // this warp's half of the tokens (compile-time, so B's zero upper triangle
-      // drops out): u tape, output, and one TF32 part of W
+      // this warp's half of the tokens (compile-time): u tape and one TF32 part of W
       auto emit = [&](auto chc) {
         constexpr int c_h = decltype(chc)::value;
 #pragma unroll
         for (int tt = 0; tt < 8; ++tt) {
           const int t = 8 * c_h + tt;
           if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
-          float o = op[t];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            if (4 * q4 > t) continue;
-            const float4 x = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * q4]);
-            const float br[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (4 * q4 + e <= t) o = fmaf(br[e], w[4 * q4 + e], o);
-          }
-          if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o);
         }
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
@@ -367,12 +357,14 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
-    // ---- tensor cores: S += W^T (k^ gamma_C / gamma) in split TF32 (hi hi + lo hi + hi lo)
+    // ---- tensor cores: S += W^T (k^ gamma_C / gamma) in split TF32 (hi hi + lo hi + hi lo), and
+    // the output's W^T B^T added to S0 (q^ gamma)^T (W split, B in TF32)
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
         const uint32_t wa[2] = {tc::smem_u32(sm.Wa[0]), tc::smem_u32(sm.Wa[1])};
         const uint32_t kb[2] = {tc::smem_u32(sm.KbT[0]), tc::smem_u32(sm.KbT[1])};
+        const uint32_t bt = tc::smem_u32(sm.Bt);
         const int pa[3] = {0, 1, 0}, pb[3] = {0, 0, 1};
 #pragma unroll
         for (int p = 0; p < 3; ++p)
@@ -380,6 +372,12 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
           for (int st = 0; st < kChunk / 8; ++st)
             tc::mma_ss(tbase + kColS, tc::kdesc(wa[pa[p]], st, kChunk), tc::kdesc(kb[pb[p]], st, kChunk),
                        tc::idesc_tf32(128, 128), 1);
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+          for (int st = 0; st < kChunk / 8; ++st)
+            tc::mma_ss(tbase + kColYO + 16, tc::kdesc(wa[p], st, kChunk), tc::kdesc(bt, st, kChunk),
+                       tc::idesc_tf32(128, 16), 1);
         tc::mma_commit(mbar);
       }
       __syncwarp();
@@ -389,6 +387,15 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     ok = ok && tc::mbar_wait(mbar, parity);
     parity ^= 1;
     tc::fence_after();
+    {  // the output of this warp's half of the tokens: o = scale (S0 (q^ gamma)^T + W^T B^T)
+      float o8[8];
+      tc::tmem_ld8(tl + kColYO + 16 + 8 * ch, o8);
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) {
+        const int t = 8 * ch + tt;
+        if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o8[tt]);
+      }
+    }
     if (__syncthreads_or(!ok)) { aborted = true; break; }
   }
   if (!aborted) {
