@@ -298,48 +298,54 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     float* cmb = reinterpret_cast<float*>(sm.Wt[0]);  // d q^, d k^, gauge / da tiles (after the MMAs)
     const int ot = tid & 15, oq = tid >> 4;           // operand-tile mapping: token ot, quads oq, oq + 16
 
+    // P0, the prologue of sub-chunk cc (token row ti, columns c8..c8+7): L2 norm, gate,
+    // sigmoid beta. It runs in the same barrier interval as the previous (later) sub-chunk's
+    // epilogue, with which it shares no data, so the two latency chains interleave.
+    float qhat[8], khat[8], zz[8], rq = 0.f, rk = 0.f;
+    auto prologue = [&](int64_t cc) {
+      const int ntc = rows_of(cc);
+        {
+          float qv[8], kv[8], gv[8];
+          const bool valid = ti < ntc;
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sq + ti * kDim + c8), qv);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sk + ti * kDim + c8), kv);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sg + ti * kDim + c8), gv);
+          float sq = 0.f, sk = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+          sq = row16_sum(sq);
+          sk = row16_sum(sk);
+          rq = valid ? inv_norm_of(sq) : 0.f;
+          rk = valid ? inv_norm_of(sk) : 0.f;
+          float la[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            qhat[e] = qv[e] * rq;
+            khat[e] = kv[e] * rk;
+            zz[e] = ea * (gv[e] + dtb[e]);
+            la[e] = valid ? log_decay_of(P.lb, zz[e]) : 0.f;
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int o = 4 * hh;
+            *reinterpret_cast<float4*>(sm.Qtp + ti * kLds + c8 + o) = make_float4(qhat[o], qhat[o + 1], qhat[o + 2], qhat[o + 3]);
+            *reinterpret_cast<float4*>(sm.Ktp + ti * kLds + c8 + o) = make_float4(khat[o], khat[o + 1], khat[o + 2], khat[o + 3]);
+            *reinterpret_cast<float4*>(sm.Pa + ti * kLds + c8 + o) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
+          }
+          if (tid < kChunk) {
+            const float bl = __bfloat162float(nb);
+            sm.braw[tid] = bl;
+            sm.bs[tid] = (tid < ntc) ? sigmoid_of(bl) : 0.f;
+          }
+        }
+    };
+    tc::cp_async_wait<2>();  // q, k, g of the first sub-chunk (dO/u/A/B and the state may be in flight)
+    csync();
+    prologue(nchunks - 1);
     for (int64_t c = nchunks - 1; c >= 0; --c) {
       const int64_t tc0 = si.t0 + c * kChunk;
       const int nt = rows_of(c);
-      tc::cp_async_wait_all();
-      csync();
-      // ---- P0: prologue (token row ti, columns c8..c8+7): L2 norm, gate, sigmoid beta
-      float qhat[8], khat[8], zz[8], rq, rk;
-      {
-        float qv[8], kv[8], gv[8];
-        const bool valid = ti < nt;
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sq + ti * kDim + c8), qv);
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sk + ti * kDim + c8), kv);
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(sm.Sg + ti * kDim + c8), gv);
-        float sq = 0.f, sk = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
-        sq = row16_sum(sq);
-        sk = row16_sum(sk);
-        rq = valid ? inv_norm_of(sq) : 0.f;
-        rk = valid ? inv_norm_of(sk) : 0.f;
-        float la[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qhat[e] = qv[e] * rq;
-          khat[e] = kv[e] * rk;
-          zz[e] = ea * (gv[e] + dtb[e]);
-          la[e] = valid ? log_decay_of(P.lb, zz[e]) : 0.f;
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int o = 4 * hh;
-          *reinterpret_cast<float4*>(sm.Qtp + ti * kLds + c8 + o) = make_float4(qhat[o], qhat[o + 1], qhat[o + 2], qhat[o + 3]);
-          *reinterpret_cast<float4*>(sm.Ktp + ti * kLds + c8 + o) = make_float4(khat[o], khat[o + 1], khat[o + 2], khat[o + 3]);
-          *reinterpret_cast<float4*>(sm.Pa + ti * kLds + c8 + o) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
-        }
-        if (tid < kChunk) {
-          const float bl = __bfloat162float(nb);
-          sm.braw[tid] = bl;
-          sm.bs[tid] = (tid < nt) ? sigmoid_of(bl) : 0.f;
-        }
-      }
-      csync();
+      csync();  // the prologue of this sub-chunk is in place
       // ---- P1: cumulative decay (one key column per thread); the next q, k, g are fetched meanwhile
       if (c > 0) prefetch_qkg(c - 1);
       if (tid < kDim) {
@@ -356,6 +362,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
         sm.gC[tid] = av[kChunk - 1];
       }
+      if (c > 0) tc::cp_async_wait<1>();  // dO, u, A/B and the state of this sub-chunk (the next q, k, g may be in flight)
+      else tc::cp_async_wait_all();
       csync();
       // ---- P2: decay of the adjoint, G <- G diag(gamma_C) (lanes v) and G^T <- diag(gamma_C) G^T
       // (lanes k), with sum_v Gd * S0 from the FP32 checkpoint, the low part of Gd^T for the
@@ -656,6 +664,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           tv[i * kLds + tid] = run;
         }
       }
+      if (c > 0) tc::cp_async_wait<2>();  // q, k, g of the next sub-chunk, for its prologue below
       csync();
       // ---- P9: epilogue: gate / sigmoid / L2-norm backward and stores
       {
@@ -707,6 +716,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
         }
       }
+      if (c > 0) prologue(c - 1);
       ph ^= 1;
       tc::fence_before();
     }

@@ -140,6 +140,9 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uin
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Wait until at most N of this thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Issue a 16-column TMEM load without waiting; tmem_wait_ld() completes it.
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
