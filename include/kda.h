@@ -178,6 +178,18 @@ kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16*
                            kda_bf16* dbeta, float* dA_log, float* ddt_bias, float* dh0,
                            struct CUstream_st* stream);
 
+/* Self-test of the device-side timeout path (no counterpart on the pages: the
+ * kernels' own failure handling). Launches one CTA of 32 threads on `stream`
+ * whose mbarrier wait can never complete, because nothing arrives on the
+ * barrier. The wait is the same bounded wait the kernels use, with a limit of
+ * 2^21 SM clock cycles (about 1 ms), after which the CTA writes a device status
+ * word and exits; the call synchronises the stream and reads the word.
+ * Returns KDA_ERR_DEVICE_TIMEOUT when the wait gave up (the expected outcome),
+ * KDA_OK if it did not, KDA_ERR_UNSUPPORTED on a device that is not sm_103,
+ * KDA_ERR_CUDA on a launch or copy error. Nothing faults, traps or hangs, and
+ * the device and any contexts stay usable. Not for use inside stream capture. */
+kda_status kda_selftest_device_timeout(struct CUstream_st* stream);
+
 /* Internal tiling, for tooling and tests: sub-chunk length in tokens and the
  * checkpoint interval in tokens. */
 int32_t kda_chunk_tokens(void);

@@ -13,6 +13,7 @@
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
+#include "tc.cuh"
 
 using kda::SeqInfo;
 
@@ -156,6 +157,22 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 void kda::set_last_error(const char* msg) { g_last_error = msg; }
 
+namespace {
+
+__device__ int32_t g_selftest_status;
+
+// One CTA waits on an mbarrier that nothing arrives at; the bounded wait must
+// give up after `limit` cycles and the CTA records that in the status word.
+__global__ void kda_selftest_timeout_kernel(long long limit) {
+  __shared__ unsigned long long mbar;
+  if (threadIdx.x == 0) kda::tc::mbar_init(kda::tc::smem_u32(&mbar), 1);
+  __syncthreads();
+  const bool completed = kda::tc::mbar_wait(kda::tc::smem_u32(&mbar), 0, limit);
+  if (threadIdx.x == 0) g_selftest_status = completed ? 0 : 1;
+}
+
+}  // namespace
+
 struct kda_ctx {
   Shape shape;
   Layout layout;
@@ -187,6 +204,24 @@ const char* kda_status_string(kda_status st) {
 }
 
 const char* kda_last_error_message(void) { return g_last_error.c_str(); }
+
+kda_status kda_selftest_device_timeout(struct CUstream_st* stream) {
+  int dev = -1;
+  kda_status st = check_device(&dev);
+  if (st != KDA_OK) return st;
+  const int32_t unset = -1;
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_selftest_status, &unset, sizeof(unset), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test status reset");
+  kda_selftest_timeout_kernel<<<1, 32, 0, stream>>>(1ll << 21);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "self-test launch");
+  int32_t status = -1;
+  e = cudaMemcpyFromSymbolAsync(&status, g_selftest_status, sizeof(status), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test status read");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "self-test synchronise");
+  if (status == 1) return fail(KDA_ERR_DEVICE_TIMEOUT, "self-test: the device-side wait gave up as designed");
+  if (status == 0) return KDA_OK;
+  return fail(KDA_ERR_CUDA, "self-test: status word not written");
+}
 
 int32_t kda_chunk_tokens(void) { return kda::kChunk; }
 int32_t kda_checkpoint_tokens(void) { return kda::kCkTokens; }

@@ -93,7 +93,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+// Bounded wait for the phase with the given parity: gives up (returns false)
+// after `limit` SM clock cycles, ~2 s at the default.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long long limit = 1ll << 32) {
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
@@ -104,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
         : "r"(mbar), "r"(parity)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > (1ll << 32)) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 

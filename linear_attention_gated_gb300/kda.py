@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_last_error_message.restype = ctypes.c_char_p
     lib.kda_bwd_noalloc.argtypes = [P] * 8 + [P, P, I, I, I, I, I, I, F, F] + [P] * 10 + [P]
     lib.kda_bwd_noalloc.restype = ctypes.c_int
+    lib.kda_selftest_device_timeout.argtypes = [P]
+    lib.kda_selftest_device_timeout.restype = ctypes.c_int
     lib.kda_chunk_tokens.argtypes = []
     lib.kda_chunk_tokens.restype = ctypes.c_int32
     lib.kda_checkpoint_tokens.argtypes = []
@@ -273,6 +275,17 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_
                              ctypes.c_void_p(stream.cuda_stream))
     _check(rc)
     return tuple(out)
+
+
+def selftest_device_timeout(device=None) -> int:
+    """Run the device-side timeout self-test on the current stream of `device`:
+    one CTA waits on an mbarrier nothing arrives at and must give up after
+    about 1 ms. Returns the status code (KDA_ERR_DEVICE_TIMEOUT is the expected
+    outcome) without raising."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib.kda_selftest_device_timeout(_stream_handle(dev)))
 
 
 recurrent_kda_training_forward = kda_fwd
