@@ -234,8 +234,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="named workload of kda_inputs.WORKLOADS (default: the packed 8 x 1024, 96-head one)")
+    ap.add_argument("--decode", type=int, default=0, metavar="N",
+                    help="instead of the training step, time decode steps (T = 1) of N sequences x 96 heads")
+    ap.add_argument("--decode-state", default="bf16", choices=["bf16", "fp32"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.decode:
+        bench_decode(args)
+        return
 
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -344,6 +350,61 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def bench_decode(args):
+    """Decode steps of N sequences x 96 value heads (one token each) against one
+    state pool, updated in place; prints one JSON line with HBM roofline."""
+    import torch
+
+    from linear_attention_gated_gb300 import build as cuda_build
+    from linear_attention_gated_gb300 import kda_decode, load_library
+
+    cuda_build.build()
+    load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, H = args.decode, 96
+    gen = torch.Generator("cpu").manual_seed(7)
+    def bf(*shape):
+        return torch.randn(shape, generator=gen).to(torch.bfloat16).to(dev)
+    q, k, v, g, beta = bf(N, 1, H, DIM), bf(N, 1, H, DIM), bf(N, 1, H, DIM), bf(N, 1, H, DIM), bf(N, 1, H)
+    A_log = (torch.rand((H,), generator=gen) * math.log(16.0)).to(dev)
+    dt_bias = (0.1 * torch.randn((H, DIM), generator=gen)).to(dev)
+    sdt = torch.bfloat16 if args.decode_state == "bf16" else torch.float32
+    state = (0.05 * torch.randn((N, H, DIM, DIM), generator=gen)).to(sdt).to(dev)
+    o = torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        kda_decode(q, k, v, g, beta, A_log, dt_bias, state, out=o)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        kda_decode(q, k, v, g, beta, A_log, dt_bias, state, out=o)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    sec = t0.elapsed_time(t1) / 1e3 / args.steps
+    esz = 2 if sdt == torch.bfloat16 else 4
+    # per unit: the state read and written once, q, k (its query/key head), v, g read, o written, beta
+    bytes_step = N * H * (2 * esz * DIM * DIM + 4 * 2 * DIM + 2 * DIM + 2)
+    peaks = read_peaks()
+    achieved = bytes_step / sec / 1e9
+    line = {"metric": "KDA decode token\u00b7heads/s (1 GB300)", "value": N * H / sec, "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec,
+            "higher_is_better": True, "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": f"decode_{N}x{H}", "sequences": N, "Hqk": H, "Hv": H, "head_dim": DIM,
+                       "state_dtype": args.decode_state,
+                       "l2": f"state pool {N * H * DIM * DIM * esz / 1e6:.0f} MB > 129 MB, no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "kda_decode_kernel",
+                         "peak_src": peaks["src"], "algorithmic_bytes_per_launch": bytes_step},
+            "gpu_launches": args.steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
 
 
 def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=5):

@@ -178,6 +178,41 @@ kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16*
                            kda_bf16* dbeta, float* dA_log, float* ddt_bias, float* dh0,
                            struct CUstream_st* stream);
 
+/* State element types for kda_decode. */
+enum { KDA_STATE_BF16 = 0, KDA_STATE_FP32 = 1 };
+
+/* One decode step, T = 1 (flashinfer.kda.recurrent_kda, description and the
+ * parameters q ("T=1 selects decode"), initial_state ("Updated in-place") and
+ * ssm_state_indices): for every sequence n and value head h, with the state S
+ * of pool slot state_indices[n] (slot n when state_indices is NULL),
+ *   S' = S diag(d),  u = v - S' k^,  S <- S' + beta u k^^T,  o = scale S q^
+ * with q^, k^ L2-normalised in the kernel (eps 1e-6), the gate computed in the
+ * kernel, d = exp(lower_bound * sigmoid(exp(A_log[h]) * (g + dt_bias[h]))),
+ * and beta = sigmoid(logit). Arithmetic is FP32; a BF16 state is read, updated
+ * in FP32 and written back rounded to nearest even.
+ *   q, k            BF16 [N, 1, Hqk, 128]
+ *   v, g            BF16 [N, 1, Hv, 128]; beta BF16 [N, 1, Hv] (logits)
+ *   A_log           FP32 [Hv]; dt_bias FP32 [Hv, 128]
+ *   state           [num_slots, Hv, 128, 128] value-first, KDA_STATE_BF16 or
+ *                   KDA_STATE_FP32 per state_dtype; read and written in place
+ *   state_indices   device int32 [N] and its trusted host mirror
+ *                   state_indices_host (both NULL, or both set); every index in
+ *                   [0, num_slots) and no slot used twice
+ *   o               BF16 [N, 1, Hv, 128], overwritten
+ * Hv must be a multiple of Hqk (value head h reads query/key head h / (Hv/Hqk));
+ * head_dim 128; scale NaN or 1/sqrt(128); lower_bound -5. Device pointers are
+ * caller-owned, 16-byte aligned for the token and state tensors; the state,
+ * o and the inputs must not overlap. Validation errors return before any
+ * launch (KDA_ERR_INVALID_ARGUMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_ALIASING);
+ * otherwise the step is enqueued on `stream` and KDA_OK returned (KDA_ERR_CUDA
+ * on a launch error). Nothing is allocated. */
+kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                      const kda_bf16* beta, const float* A_log, const float* dt_bias, void* state,
+                      int32_t state_dtype, const int32_t* state_indices,
+                      const int32_t* state_indices_host, int64_t num_slots, int64_t N, int64_t Hqk,
+                      int64_t Hv, int64_t head_dim, float scale, float lower_bound, kda_bf16* o,
+                      struct CUstream_st* stream);
+
 /* Self-test of the device-side timeout path (no counterpart on the pages: the
  * kernels' own failure handling). Launches one CTA of 32 threads on `stream`
  * whose mbarrier wait can never complete, because nothing arrives on the

@@ -1,7 +1,8 @@
 """GB300 (sm_103a) recurrent KDA training forward + backward behind a C ABI.
 
 ``kda_fwd`` / ``kda_bwd`` (and the aliases ``recurrent_kda_training_forward`` /
-``recurrent_kda_training_backward``) call libkda.so; see include/kda.h.
+``recurrent_kda_training_backward``) and the single-token ``kda_decode`` call
+libkda.so; see include/kda.h.
 """
 
 from .kda import (  # noqa: F401
@@ -11,6 +12,7 @@ from .kda import (  # noqa: F401
     KdaError,
     kda_bwd,
     kda_bwd_noalloc,
+    kda_decode,
     kda_fwd,
     load_library,
     recurrent_kda_training_backward,

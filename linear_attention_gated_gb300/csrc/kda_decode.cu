@@ -1,0 +1,240 @@
+// kda_decode.cu -- one decode step (T = 1) of the recurrent KDA recurrence
+// (flashinfer.kda.recurrent_kda, description and parameters: "T=1 selects
+// decode"; the state is updated in place, optionally through state-cache slot
+// indices).
+//
+// For every (sequence n, value head h) the 128x128 state S (value-first, the
+// slot state_indices[n] of the state pool) is read once, decayed per key
+// column, delta-corrected and written back, and the output token produced:
+//   S' = S diag(d),  u = v - S' k^,  S <- S' + beta u k^^T,  o = s S q^
+// with q^, k^ L2-normalised, d = exp(lb sigmoid(exp(A_log) (g + dt_bias)))
+// and beta = sigmoid(logit). Since S q^ = S' q^ + beta u (k^ . q^), each state
+// row needs two dot products with the decayed row and one rank-1 update.
+//
+// The step moves the state through HBM once in each direction and does 8 flops
+// per state element, so it is bandwidth-bound: one CTA of 256 threads per
+// unit, a half-warp per state row (8 keys per lane), all eight rows of a
+// thread loaded before any is used so that a CTA keeps 4 KiB (BF16 state) or
+// 8 KiB (FP32 state) per warp in flight, several CTAs per SM.
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+
+#include <cmath>
+#include <unordered_set>
+
+namespace kda {
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kRowsPerPass = kDecThreads / 16;     // 16 rows: two per warp
+constexpr int kPasses = kDim / kRowsPerPass;       // 8
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;     // [N, Hqk, 128]
+  const __nv_bfloat16* k;     // [N, Hqk, 128]
+  const __nv_bfloat16* v;     // [N, Hv, 128]
+  const __nv_bfloat16* g;     // [N, Hv, 128]
+  const __nv_bfloat16* beta;  // [N, Hv] (logits)
+  const float* A_log;         // [Hv]
+  const float* dt_bias;       // [Hv, 128]
+  void* state;                // [num_slots, Hv, 128, 128], BF16 or FP32
+  const int32_t* idx;         // [N] slot per sequence, or null (slot n)
+  __nv_bfloat16* o;           // [N, Hv, 128]
+  int64_t Hqk, Hv, r;
+  float scale, lb;
+};
+
+// 8 consecutive state elements of one row <-> FP32 registers
+template <typename T>
+struct Row8;
+template <>
+struct Row8<__nv_bfloat16> {
+  using Raw = uint4;
+  static __device__ __forceinline__ Raw load(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+  static __device__ __forceinline__ void unpack(const Raw& r, float* x) { unpack_bf16x8(r, x); }
+  static __device__ __forceinline__ void store(void* p, const float* x) {
+    store_bf16x8(reinterpret_cast<__nv_bfloat16*>(p), x);
+  }
+};
+template <>
+struct Row8<float> {
+  struct Raw {
+    float4 a, b;
+  };
+  static __device__ __forceinline__ Raw load(const void* p) {
+    const float4* f = reinterpret_cast<const float4*>(p);
+    return Raw{f[0], f[1]};
+  }
+  static __device__ __forceinline__ void unpack(const Raw& r, float* x) {
+    x[0] = r.a.x; x[1] = r.a.y; x[2] = r.a.z; x[3] = r.a.w;
+    x[4] = r.b.x; x[5] = r.b.y; x[6] = r.b.z; x[7] = r.b.w;
+  }
+  static __device__ __forceinline__ void store(void* p, const float* x) {
+    float4* f = reinterpret_cast<float4*>(p);
+    f[0] = make_float4(x[0], x[1], x[2], x[3]);
+    f[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+};
+
+template <typename StateT>
+__global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeArgs a) {
+  const int64_t unit = blockIdx.x;
+  const int64_t n = unit / a.Hv, h = unit % a.Hv, qh = h / a.r;
+  const int64_t slot = a.idx ? a.idx[n] : n;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hl = lane & 15, half = lane >> 4;  // keys 8 hl .. 8 hl + 7 of row 2 warp + half (+16 per pass)
+  StateT* S = reinterpret_cast<StateT*>(a.state) + ((slot * a.Hv + h) * kDim) * kDim + 8 * hl;
+
+  // the state rows first: they are the bandwidth
+  typename Row8<StateT>::Raw raw[kPasses];
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) raw[p] = Row8<StateT>::load(S + (kRowsPerPass * p + 2 * warp + half) * kDim);
+
+  // the token's vectors (every half-warp holds all 128 keys)
+  float qv[8], kv[8], gv[8];
+  load_bf16x8(a.q + (n * a.Hqk + qh) * kDim + 8 * hl, qv);
+  load_bf16x8(a.k + (n * a.Hqk + qh) * kDim + 8 * hl, kv);
+  load_bf16x8(a.g + (n * a.Hv + h) * kDim + 8 * hl, gv);
+  float sq = 0.f, sk = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+  sq = row16_sum(sq);
+  sk = row16_sum(sk);
+  const float rq = inv_norm_of(sq), rk = inv_norm_of(sk);
+  const float ea = expf(a.A_log[h]);
+  float d[8], kq = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    qv[e] *= rq;
+    kv[e] *= rk;
+    kq += kv[e] * qv[e];
+    d[e] = expf(log_decay_of(a.lb, ea * (gv[e] + a.dt_bias[h * kDim + 8 * hl + e])));
+  }
+  kq = row16_sum(kq);
+  const float bt = sigmoid_of(__bfloat162float(a.beta[n * a.Hv + h]));
+  const __nv_bfloat16* vrow = a.v + (n * a.Hv + h) * kDim;
+  __nv_bfloat16* orow = a.o + (n * a.Hv + h) * kDim;
+
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const int row = kRowsPerPass * p + 2 * warp + half;
+    float s[8];
+    Row8<StateT>::unpack(raw[p], s);
+    float pk = 0.f, pq = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s[e] *= d[e];
+      pk = fmaf(s[e], kv[e], pk);
+      pq = fmaf(s[e], qv[e], pq);
+    }
+    pk = row16_sum(pk);
+    pq = row16_sum(pq);
+    const float u = __bfloat162float(vrow[row]) - pk;
+    const float bu = bt * u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] = fmaf(bu, kv[e], s[e]);
+    Row8<StateT>::store(S + row * kDim, s);
+    if (hl == 0) orow[row] = __float2bfloat16_rn(a.scale * (pq + bu * kq));
+  }
+}
+
+}  // namespace
+}  // namespace kda
+
+namespace {
+
+kda_status dfail(kda_status st, const char* msg) {
+  kda::set_last_error(msg);
+  return st;
+}
+
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+
+bool overlap(const Span& a, const Span& b) {
+  const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+  return a.bytes && b.bytes && a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+}  // namespace
+
+extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                                 const kda_bf16* beta, const float* A_log, const float* dt_bias, void* state,
+                                 int32_t state_dtype, const int32_t* state_indices,
+                                 const int32_t* state_indices_host, int64_t num_slots, int64_t N, int64_t Hqk,
+                                 int64_t Hv, int64_t head_dim, float scale, float lower_bound, kda_bf16* o,
+                                 struct CUstream_st* stream) {
+  if (N < 1 || Hqk < 1 || Hv < 1) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: N, Hqk and Hv must be positive");
+  if (Hv % Hqk != 0) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: Hv must be a multiple of Hqk");
+  if (head_dim != kda::kDim) return dfail(KDA_ERR_UNSUPPORTED, "decode: head_dim must be 128");
+  const float s_def = 1.0f / std::sqrt((float)kda::kDim);
+  if (!std::isnan(scale) && scale != s_def)
+    return dfail(KDA_ERR_UNSUPPORTED, "decode: scale must be 1/sqrt(128) (NaN selects it)");
+  if (lower_bound != -5.0f) return dfail(KDA_ERR_UNSUPPORTED, "decode: lower_bound must be -5");
+  if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32)
+    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_dtype must be KDA_STATE_BF16 or KDA_STATE_FP32");
+  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !state || !o)
+    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: null tensor pointer");
+  if ((state_indices == nullptr) != (state_indices_host == nullptr))
+    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_indices needs its host mirror (and the reverse)");
+  if (state_indices_host) {
+    std::unordered_set<int32_t> seen;
+    for (int64_t i = 0; i < N; ++i) {
+      const int32_t s = state_indices_host[i];
+      if (s < 0 || s >= num_slots) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state index out of range");
+      if (!seen.insert(s).second)
+        return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: two sequences share a state slot");
+    }
+  } else if (num_slots < N) {
+    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: without state_indices the pool needs a slot per sequence");
+  }
+  const void* ptrs[] = {q, k, v, g, state, o};
+  for (const void* p : ptrs)
+    if ((uintptr_t)p & 15u) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: token and state tensors must be 16-byte aligned");
+  const size_t esz = state_dtype == KDA_STATE_BF16 ? 2 : 4;
+  const Span st{state, esz * (size_t)num_slots * Hv * kda::kDim * kda::kDim};
+  const Span out{o, 2 * (size_t)N * Hv * kda::kDim};
+  const Span ins[] = {{q, 2 * (size_t)N * Hqk * kda::kDim}, {k, 2 * (size_t)N * Hqk * kda::kDim},
+                      {v, 2 * (size_t)N * Hv * kda::kDim},  {g, 2 * (size_t)N * Hv * kda::kDim},
+                      {beta, 2 * (size_t)N * Hv},           {A_log, 4 * (size_t)Hv},
+                      {dt_bias, 4 * (size_t)Hv * kda::kDim}};
+  for (const Span& in : ins)
+    if (overlap(in, st) || overlap(in, out)) return dfail(KDA_ERR_ALIASING, "decode: an input overlaps the state or o");
+  if (overlap(st, out)) return dfail(KDA_ERR_ALIASING, "decode: o overlaps the state");
+  if (state_indices && overlap(Span{state_indices, 4 * (size_t)N}, st))
+    return dfail(KDA_ERR_ALIASING, "decode: state_indices overlaps the state");
+
+  int dev = -1, major = 0, minor = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
+  if (major != 10 || minor != 3) return dfail(KDA_ERR_UNSUPPORTED, "decode: kernels are built for sm_103a");
+
+  kda::DecodeArgs a{};
+  a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  a.k = reinterpret_cast<const __nv_bfloat16*>(k);
+  a.v = reinterpret_cast<const __nv_bfloat16*>(v);
+  a.g = reinterpret_cast<const __nv_bfloat16*>(g);
+  a.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+  a.A_log = A_log;
+  a.dt_bias = dt_bias;
+  a.state = state;
+  a.idx = state_indices;
+  a.o = reinterpret_cast<__nv_bfloat16*>(o);
+  a.Hqk = Hqk;
+  a.Hv = Hv;
+  a.r = Hv / Hqk;
+  a.scale = s_def;
+  a.lb = lower_bound;
+  const unsigned grid = (unsigned)(N * Hv);
+  if (state_dtype == KDA_STATE_BF16)
+    kda::kda_decode_kernel<__nv_bfloat16><<<grid, kda::kDecThreads, 0, stream>>>(a);
+  else
+    kda::kda_decode_kernel<float><<<grid, kda::kDecThreads, 0, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
+  return KDA_OK;
+}

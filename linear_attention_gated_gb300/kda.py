@@ -30,7 +30,7 @@ _STATUS = {
 
 EXPORTED = ("kda_ctx_workspace_bytes", "kda_fwd", "kda_bwd", "kda_ctx_status", "kda_ctx_destroy",
             "kda_status_string", "kda_last_error_message", "kda_chunk_tokens",
-            "kda_checkpoint_tokens", "kda_bwd_noalloc")
+            "kda_checkpoint_tokens", "kda_bwd_noalloc", "kda_decode", "kda_selftest_device_timeout")
 
 
 class KdaError(RuntimeError):
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_last_error_message.restype = ctypes.c_char_p
     lib.kda_bwd_noalloc.argtypes = [P] * 8 + [P, P, I, I, I, I, I, I, F, F] + [P] * 10 + [P]
     lib.kda_bwd_noalloc.restype = ctypes.c_int
+    lib.kda_decode.argtypes = [P] * 8 + [ctypes.c_int32, P, P, I, I, I, I, I, F, F, P, P]
+    lib.kda_decode.restype = ctypes.c_int
     lib.kda_selftest_device_timeout.argtypes = [P]
     lib.kda_selftest_device_timeout.restype = ctypes.c_int
     lib.kda_chunk_tokens.argtypes = []
@@ -275,6 +277,52 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_
                              ctypes.c_void_p(stream.cuda_stream))
     _check(rc)
     return tuple(out)
+
+
+def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scale=None, lower_bound=-5.0,
+               out=None):
+    """One decode step (T = 1): updates ``state`` in place and returns o.
+
+    q, k [N, 1, Hqk, 128] and v, g [N, 1, Hv, 128] BF16, beta [N, 1, Hv] BF16
+    logits, A_log [Hv] and dt_bias [Hv, 128] FP32; state [num_slots, Hv, 128,
+    128] BF16 or FP32 (value-first), read and written at slot state_indices[n]
+    (int32 [N], on the device; slot n when None). Argument marshalling only: the
+    step is one launch of the library's decode kernel."""
+    lib = load_library()
+    N, T, Hqk, K = q.shape
+    Hv = v.shape[2]
+    if T != 1:
+        raise ValueError("decode takes one token per sequence (T = 1)")
+    _want(q, "q", torch.bfloat16); _want(k, "k", torch.bfloat16, q.shape)
+    _want(v, "v", torch.bfloat16); _want(g, "g", torch.bfloat16, v.shape)
+    _want(beta, "beta", torch.bfloat16, (N, 1, Hv))
+    _want(A_log, "A_log", torch.float32, (Hv,)); _want(dt_bias, "dt_bias", torch.float32, (Hv, K))
+    if state.dtype == torch.bfloat16:
+        sdt = 0
+    elif state.dtype == torch.float32:
+        sdt = 1
+    else:
+        raise TypeError("state must be bfloat16 or float32")
+    if state.dim() != 4 or tuple(state.shape[1:]) != (Hv, K, K) or not state.is_contiguous():
+        raise ValueError(f"state must be contiguous [num_slots, {Hv}, {K}, {K}]")
+    if out is None:
+        out = torch.empty_like(v)
+    _want(out, "out", torch.bfloat16, v.shape)
+    idx_dev = idx_host = None
+    if state_indices is not None:
+        if state_indices.dtype != torch.int32 or state_indices.shape != (N,):
+            raise ValueError("state_indices must be int32 [N]")
+        idx_dev = state_indices.contiguous()
+        idx_host = idx_dev.cpu()
+    dev = q.device
+    with torch.cuda.device(dev):
+        rc = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                            _ptr(state), sdt, _ptr(idx_dev) if idx_dev is not None else None,
+                            ctypes.c_void_p(idx_host.data_ptr()) if idx_host is not None else None,
+                            state.shape[0], N, Hqk, Hv, K, float("nan") if scale is None else float(scale),
+                            float(lower_bound), _ptr(out), _stream_handle(dev))
+    _check(rc)
+    return out
 
 
 def selftest_device_timeout(device=None) -> int:
