@@ -12,12 +12,15 @@
 // row needs two dot products with the decayed row and one rank-1 update.
 //
 // The step moves the state through HBM once in each direction and does 8 flops
-// per state element, so it is bandwidth-bound: one CTA of 256 threads per
-// unit, a half-warp per state row (8 keys per lane), all eight rows of a
-// thread loaded before any is used so that a CTA keeps 4 KiB (BF16 state) or
-// 8 KiB (FP32 state) per warp in flight, several CTAs per SM.
+// per state element, so it is bandwidth-bound. One CTA of 256 threads per unit
+// starts the state's loads first: a BF16 state (32 KiB) is staged into shared
+// memory with cp.async, an FP32 state (64 KiB) is loaded into registers, eight
+// rows' slices per thread; meanwhile it computes the token's vectors. Then a
+// half-warp updates one state row at a time (8 keys per lane) and writes it
+// straight back.
 #include "../../include/kda.h"
 #include "kda_common.cuh"
+#include "tc.cuh"
 
 #include <cmath>
 #include <unordered_set>
@@ -76,19 +79,38 @@ struct Row8<float> {
   }
 };
 
+// A BF16 state is staged through shared memory (bytes in flight bounded by
+// shared memory, four CTAs per SM); an FP32 state, twice the bytes per row, is
+// loaded straight into registers, all eight rows of a thread at once.
 template <typename StateT>
-__global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeArgs a) {
+constexpr bool kStaged = sizeof(StateT) == 2;
+template <typename StateT>
+constexpr int kDecMinBlocks = kStaged<StateT> ? 4 : 2;
+
+template <typename StateT>
+__global__ void __launch_bounds__(kDecThreads, kDecMinBlocks<StateT>) kda_decode_kernel(const DecodeArgs a) {
   const int64_t unit = blockIdx.x;
   const int64_t n = unit / a.Hv, h = unit % a.Hv, qh = h / a.r;
   const int64_t slot = a.idx ? a.idx[n] : n;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hl = lane & 15, half = lane >> 4;  // keys 8 hl .. 8 hl + 7 of row 2 warp + half (+16 per pass)
-  StateT* S = reinterpret_cast<StateT*>(a.state) + ((slot * a.Hv + h) * kDim) * kDim + 8 * hl;
+  StateT* S = reinterpret_cast<StateT*>(a.state) + ((slot * a.Hv + h) * kDim) * kDim;
+  extern __shared__ __align__(16) unsigned char st_smem[];
+  StateT* Ss = reinterpret_cast<StateT*>(st_smem);
 
-  // the state rows first: they are the bandwidth
-  typename Row8<StateT>::Raw raw[kPasses];
+  // the state first: it is the bandwidth
+  typename Row8<StateT>::Raw raw[kStaged<StateT> ? 1 : kPasses];
+  if constexpr (kStaged<StateT>) {
+    constexpr int kPieces = kDim * kDim * (int)sizeof(StateT) / 16;
+#pragma unroll 4
+    for (int i = tid; i < kPieces; i += kDecThreads)
+      tc::cp_async16(st_smem + 16 * i, reinterpret_cast<const unsigned char*>(S) + 16 * i, 16u);
+    tc::cp_async_commit();
+  } else {
 #pragma unroll
-  for (int p = 0; p < kPasses; ++p) raw[p] = Row8<StateT>::load(S + (kRowsPerPass * p + 2 * warp + half) * kDim);
+    for (int p = 0; p < kPasses; ++p)
+      raw[p] = Row8<StateT>::load(S + (kRowsPerPass * p + 2 * warp + half) * kDim + 8 * hl);
+  }
 
   // the token's vectors (every half-warp holds all 128 keys)
   float qv[8], kv[8], gv[8];
@@ -114,12 +136,17 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeArg
   const float bt = sigmoid_of(__bfloat162float(a.beta[n * a.Hv + h]));
   const __nv_bfloat16* vrow = a.v + (n * a.Hv + h) * kDim;
   __nv_bfloat16* orow = a.o + (n * a.Hv + h) * kDim;
+  if constexpr (kStaged<StateT>) {
+    tc::cp_async_wait_all();
+    __syncthreads();
+  }
 
 #pragma unroll
   for (int p = 0; p < kPasses; ++p) {
     const int row = kRowsPerPass * p + 2 * warp + half;
     float s[8];
-    Row8<StateT>::unpack(raw[p], s);
+    if constexpr (kStaged<StateT>) Row8<StateT>::unpack(Row8<StateT>::load(Ss + row * kDim + 8 * hl), s);
+    else Row8<StateT>::unpack(raw[p], s);
     float pk = 0.f, pq = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -133,7 +160,7 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode_kernel(const DecodeArg
     const float bu = bt * u;
 #pragma unroll
     for (int e = 0; e < 8; ++e) s[e] = fmaf(bu, kv[e], s[e]);
-    Row8<StateT>::store(S + row * kDim, s);
+    Row8<StateT>::store(S + row * kDim + 8 * hl, s);
     if (hl == 0) orow[row] = __float2bfloat16_rn(a.scale * (pq + bu * kq));
   }
 }
@@ -230,10 +257,15 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
   a.scale = s_def;
   a.lb = lower_bound;
   const unsigned grid = (unsigned)(N * Hv);
-  if (state_dtype == KDA_STATE_BF16)
-    kda::kda_decode_kernel<__nv_bfloat16><<<grid, kda::kDecThreads, 0, stream>>>(a);
-  else
-    kda::kda_decode_kernel<float><<<grid, kda::kDecThreads, 0, stream>>>(a);
+  const size_t smem = state_dtype == KDA_STATE_BF16 ? esz * kda::kDim * kda::kDim : 0;
+  if (state_dtype == KDA_STATE_BF16) {
+    e = cudaFuncSetAttribute(kda::kda_decode_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) kda::kda_decode_kernel<__nv_bfloat16><<<grid, kda::kDecThreads, smem, stream>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(kda::kda_decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) kda::kda_decode_kernel<float><<<grid, kda::kDecThreads, smem, stream>>>(a);
+  }
+  if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
   e = cudaGetLastError();
   if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
   return KDA_OK;
