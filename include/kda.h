@@ -213,6 +213,45 @@ kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, c
                       int64_t Hv, int64_t head_dim, float scale, float lower_bound, kda_bf16* o,
                       struct CUstream_st* stream);
 
+/* Inference prefill over whole sequences from a state pool (flashinfer.kda.
+ * recurrent_kda, parameters initial_state "Updated in-place",
+ * ssm_state_indices, state_checkpoints, checkpoint_cu_starts and
+ * checkpoint_every_n_tokens): the forward recurrence of kda_fwd for every
+ * sequence n and value head h, starting from the state of pool slot
+ * state_indices[n] (slot n when NULL) and writing the final state back to it,
+ * with the output o, and nothing saved for a backward. Same layouts, head
+ * mapping, gate, beta, scale and lower_bound rules as kda_fwd (fixed layout
+ * with cu_seqlens NULL; packed with B = 1, device cu_seqlens and its trusted
+ * host mirror). Arithmetic as in kda_fwd; a BF16 pool is read, carried in FP32
+ * and written back rounded to nearest even.
+ *   state            [num_slots, Hv, 128, 128] value-first, state_dtype
+ *                    KDA_STATE_BF16 or KDA_STATE_FP32, read and written in place
+ *   state_indices    device int32 [N] and its host mirror (both NULL, or both
+ *                    set); in range, no slot used twice
+ *   o                BF16 [B, T, Hv, 128]
+ *   checkpoints      optional BF16 [num_checkpoints, Hv, 128, 128] value-first:
+ *                    for each sequence, rows checkpoint_cu_starts[n] + j hold
+ *                    the state before token j * checkpoint_every_n_tokens
+ *                    (row 0 is the initial state), j < ceil(len_n / N); the
+ *                    device checkpoint_cu_starts [N + 1] and its host mirror must
+ *                    hold those cumulative counts, ending at num_checkpoints.
+ *                    checkpoint_every_n_tokens: a positive multiple of 16 (0
+ *                    with checkpoints NULL).
+ *   device_status    optional device int32, set to 1 if a bounded device wait
+ *                    gave up (then o and the pool are incomplete); NULL uses a
+ *                    word inside the library.
+ * Units run in index order. Validation errors return before any launch;
+ * otherwise the work is enqueued on `stream`. Nothing is allocated. */
+kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                       const kda_bf16* beta, const float* A_log, const float* dt_bias,
+                       const int64_t* cu_seqlens, const int64_t* cu_seqlens_host, int64_t num_seqs,
+                       int64_t B, int64_t T, int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
+                       float lower_bound, void* state, int32_t state_dtype, const int32_t* state_indices,
+                       const int32_t* state_indices_host, int64_t num_slots, kda_bf16* o,
+                       kda_bf16* checkpoints, int64_t num_checkpoints, const int64_t* checkpoint_cu_starts,
+                       const int64_t* checkpoint_cu_starts_host, int64_t checkpoint_every_n_tokens,
+                       int32_t* device_status, struct CUstream_st* stream);
+
 /* Self-test of the device-side timeout path (no counterpart on the pages: the
  * kernels' own failure handling). Launches one CTA of 32 threads on `stream`
  * whose mbarrier wait can never complete, because nothing arrives on the

@@ -1,8 +1,8 @@
 """GB300 (sm_103a) recurrent KDA training forward + backward behind a C ABI.
 
 ``kda_fwd`` / ``kda_bwd`` (and the aliases ``recurrent_kda_training_forward`` /
-``recurrent_kda_training_backward``) and the single-token ``kda_decode`` call
-libkda.so; see include/kda.h.
+``recurrent_kda_training_backward``), the inference ``kda_prefill`` and the
+single-token ``kda_decode`` call libkda.so; see include/kda.h.
 """
 
 from .kda import (  # noqa: F401
@@ -14,6 +14,7 @@ from .kda import (  # noqa: F401
     kda_bwd_noalloc,
     kda_decode,
     kda_fwd,
+    kda_prefill,
     load_library,
     recurrent_kda_training_backward,
     recurrent_kda_training_forward,

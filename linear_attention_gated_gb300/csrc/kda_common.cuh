@@ -49,6 +49,20 @@ struct FwdOut {
   float* hT;
 };
 
+// Inference prefill (the forward without tapes or training checkpoints): the
+// initial state comes from a state-pool slot and the final state goes back to
+// it; optional BF16 state checkpoints every ck_every_chunks sub-chunks.
+struct PrefillArgs {
+  const int64_t* cu;           // device cu_seqlens [N + 1], or null for B sequences of T tokens
+  int64_t T;                   // tokens per sequence in the fixed layout
+  const int32_t* slots;        // pool slot per sequence, or null (slot n)
+  void* pool;                  // [num_slots, Hv, 128, 128] value-first, BF16 or FP32, in place
+  int pool_bf16;               // 1: BF16 pool, 0: FP32 pool
+  __nv_bfloat16* ck;           // [C, Hv, 128, 128] BF16 value-first, or null
+  const int64_t* ck_starts;    // [N + 1] first checkpoint row of each sequence
+  int ck_every_chunks;         // checkpoint interval in sub-chunks
+};
+
 struct BwdArgs {
   const __nv_bfloat16* d_o;
   const float* d_hT;
@@ -136,6 +150,8 @@ void set_last_error(const char* msg);
 
 // Launchers (defined in kda_fwd.cu / kda_bwd.cu).
 cudaError_t launch_forward(const Problem& P, const FwdOut& out, int64_t units, cudaStream_t s);
+cudaError_t launch_prefill(const Problem& P, const FwdOut& out, const PrefillArgs& pf, int64_t units,
+                           cudaStream_t s);
 cudaError_t launch_backward(const Problem& P, const BwdArgs& a, int64_t units, int64_t Ttot,
                             float* dA_log, float* ddt_bias, cudaStream_t s);
 

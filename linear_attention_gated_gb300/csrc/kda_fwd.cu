@@ -66,16 +66,29 @@ struct FwdSmem {
   uint32_t tmem_base;
 };
 
+// kPf = false: the training forward (tapes and checkpoints for the backward,
+// h0 in, h_T out). kPf = true: inference prefill (PrefillArgs; units in index
+// order, sequence offsets from the device cu_seqlens, no tapes).
+template <bool kPf>
 __global__ void __launch_bounds__(kThreads, 2)
-kda_fwd_kernel(const Problem P, const FwdOut out) {
+kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = P.order[blockIdx.x];
+  const int unit = kPf ? (int)blockIdx.x : P.order[blockIdx.x];
   const int64_t n = unit / P.Hv;
   const int64_t h = unit % P.Hv;
   const int64_t qh = h / P.r;
-  const SeqInfo si = P.seq[n];
+  SeqInfo si;
+  if constexpr (kPf) {
+    si.t0 = pf.cu ? pf.cu[n] : n * pf.T;
+    si.len = pf.cu ? pf.cu[n + 1] - si.t0 : pf.T;
+    si.ck_base = 0;
+    si.ch_base = 0;
+  } else {
+    si = P.seq[n];
+  }
+  const int64_t slot = kPf ? (pf.slots ? pf.slots[n] : n) : 0;
 
   const int sv = 32 * (warp & 3) + lane;  // state row (TMEM lane) of this thread
   const int ch = warp >> 2;               // column half [64 ch, 64 ch + 64)
@@ -91,16 +104,23 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
   bool ok = true;
   bool aborted = false;
 
-  // S <- h0
+  // S <- h0 (prefill: the pool slot)
   {
-    const float* src = P.h0 + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
+    const int64_t row = ((kPf ? slot : n) * P.Hv + h) * kDim + sv;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       float x[16];
+      if (kPf && pf.pool_bf16) {
+        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(pf.pool) + row * kDim + 64 * ch + 16 * q;
+        load_bf16x8(src, x);
+        load_bf16x8(src + 8, x + 8);
+      } else {
+        const float* src = (kPf ? reinterpret_cast<const float*>(pf.pool) : P.h0) + row * kDim + 64 * ch + 16 * q;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 y = *reinterpret_cast<const float4*>(src + 16 * q + 4 * m);
-        x[4 * m] = y.x; x[4 * m + 1] = y.y; x[4 * m + 2] = y.z; x[4 * m + 3] = y.w;
+        for (int m = 0; m < 4; ++m) {
+          const float4 y = *reinterpret_cast<const float4*>(src + 4 * m);
+          x[4 * m] = y.x; x[4 * m + 1] = y.y; x[4 * m + 2] = y.z; x[4 * m + 3] = y.w;
+        }
       }
       tc::tmem_st16(tl + kColS + 64 * ch + 16 * q, x);
     }
@@ -251,7 +271,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
       // the backward the tape holds A row-major and B transposed (its columns are read there)
       float d16[16];
       tc::tmem_ld16(tl + kColAB, d16);
-      float* tape = P.abtape + ((si.ch_base + c) * P.Hv + h) * 512;
+      float* tape = kPf ? nullptr : P.abtape + ((si.ch_base + c) * P.Hv + h) * 512;
       if (lane < kChunk) {
         const int i = lane;
 #pragma unroll
@@ -259,16 +279,18 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
           d16[j] = j < i ? d16[j] : 0.f;
           sm.AsT[j][i] = d16[j];
         }
+        if constexpr (!kPf) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<float4*>(tape + i * 16 + 4 * q4) =
-              make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<float4*>(tape + i * 16 + 4 * q4) =
+                make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
+        }
       } else {
         const int i = lane - kChunk;
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
           d16[j] = j <= i ? d16[j] : 0.f;
-          tape[256 + j * 16 + i] = d16[j];
+          if constexpr (!kPf) tape[256 + j * 16 + i] = d16[j];
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -281,13 +303,22 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     if (__syncthreads_or(!ok)) { aborted = true; break; }
     // ---- state checkpoint and decay S <- S0 diag(gamma_C) in tensor memory
     {
-      const bool ck = (c % ck_every) == 0;
-      float* dst = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
+      const bool ck = !kPf && (c % ck_every) == 0;
+      float* dst = kPf ? nullptr : P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
+      // prefill: BF16 checkpoint (value-first) of the state before this sub-chunk
+      const bool pck = kPf && pf.ck != nullptr && (c % pf.ck_every_chunks) == 0;
+      __nv_bfloat16* pdst = pck ? pf.ck + ((pf.ck_starts[n] + c / pf.ck_every_chunks) * P.Hv + h) * kDim * kDim +
+                                      (int64_t)sv * kDim + 64 * ch
+                                : nullptr;
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         const int col = 64 * ch + 16 * q;
         float x[16];
         tc::tmem_ld16(tl + kColS + col, x);
+        if (pck) {
+          store_bf16x8(pdst + 16 * q, x);
+          store_bf16x8(pdst + 16 * q + 8, x + 8);
+        }
         if (ck) {
           // 4x4 blocks transposed across each lane quad: lane (quad base + j)
           // then holds the four values of key col + 4 m + j
@@ -337,7 +368,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 #pragma unroll
         for (int tt = 0; tt < 8; ++tt) {
           const int t = 8 * c_h + tt;
-          if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
+          if (!kPf && t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
         }
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
@@ -399,14 +430,21 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
     if (__syncthreads_or(!ok)) { aborted = true; break; }
   }
   if (!aborted) {
-    float* dst = out.hT + ((n * P.Hv + h) * kDim + sv) * kDim + 64 * ch;
+    const int64_t row = ((kPf ? slot : n) * P.Hv + h) * kDim + sv;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       float x[16];
       tc::tmem_ld16(tl + kColS + 64 * ch + 16 * q, x);
+      if (kPf && pf.pool_bf16) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(pf.pool) + row * kDim + 64 * ch + 16 * q;
+        store_bf16x8(dst, x);
+        store_bf16x8(dst + 8, x + 8);
+      } else {
+        float* dst = (kPf ? reinterpret_cast<float*>(pf.pool) : out.hT) + row * kDim + 64 * ch + 16 * q;
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<float4*>(dst + 16 * q + 4 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+        for (int m = 0; m < 4; ++m)
+          *reinterpret_cast<float4*>(dst + 4 * m) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+      }
     }
   } else if (tid == 0) {
     atomicExch(P.status, 1);
@@ -423,9 +461,18 @@ kda_fwd_kernel(const Problem P, const FwdOut out) {
 
 cudaError_t launch_forward(const Problem& P, const FwdOut& out, int64_t units, cudaStream_t s) {
   const size_t smem = sizeof(FwdSmem);
-  cudaError_t e = cudaFuncSetAttribute(kda_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kda_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kda_fwd_kernel<<<(unsigned)units, kThreads, smem, s>>>(P, out);
+  kda_fwd_kernel<false><<<(unsigned)units, kThreads, smem, s>>>(P, out, PrefillArgs{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const Problem& P, const FwdOut& out, const PrefillArgs& pf, int64_t units,
+                           cudaStream_t s) {
+  const size_t smem = sizeof(FwdSmem);
+  cudaError_t e = cudaFuncSetAttribute(kda_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kda_fwd_kernel<true><<<(unsigned)units, kThreads, smem, s>>>(P, out, pf);
   return cudaGetLastError();
 }
 

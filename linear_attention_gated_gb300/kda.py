@@ -30,7 +30,8 @@ _STATUS = {
 
 EXPORTED = ("kda_ctx_workspace_bytes", "kda_fwd", "kda_bwd", "kda_ctx_status", "kda_ctx_destroy",
             "kda_status_string", "kda_last_error_message", "kda_chunk_tokens",
-            "kda_checkpoint_tokens", "kda_bwd_noalloc", "kda_decode", "kda_selftest_device_timeout")
+            "kda_checkpoint_tokens", "kda_bwd_noalloc", "kda_decode", "kda_prefill",
+            "kda_selftest_device_timeout")
 
 
 class KdaError(RuntimeError):
@@ -71,6 +72,9 @@ def load_library(path: str = LIB_PATH):
     lib.kda_bwd_noalloc.restype = ctypes.c_int
     lib.kda_decode.argtypes = [P] * 8 + [ctypes.c_int32, P, P, I, I, I, I, I, F, F, P, P]
     lib.kda_decode.restype = ctypes.c_int
+    lib.kda_prefill.argtypes = [P] * 7 + [P, P, I, I, I, I, I, I, F, F, P, ctypes.c_int32, P, P, I, P, P, I, P, P,
+                                          I, P, P]
+    lib.kda_prefill.restype = ctypes.c_int
     lib.kda_selftest_device_timeout.argtypes = [P]
     lib.kda_selftest_device_timeout.restype = ctypes.c_int
     lib.kda_chunk_tokens.argtypes = []
@@ -321,6 +325,52 @@ def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scal
                             ctypes.c_void_p(idx_host.data_ptr()) if idx_host is not None else None,
                             state.shape[0], N, Hqk, Hv, K, float("nan") if scale is None else float(scale),
                             float(lower_bound), _ptr(out), _stream_handle(dev))
+    _check(rc)
+    return out
+
+
+def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_indices=None, checkpoints=None,
+                checkpoint_cu_starts=None, checkpoint_every_n_tokens=0, scale=None, lower_bound=-5.0, out=None,
+                device_status=None):
+    """Inference prefill from a state pool: returns o; the final state of every
+    sequence is written back to its slot of ``state`` (BF16 or FP32, [num_slots,
+    Hv, 128, 128]); optional BF16 ``checkpoints`` [C, Hv, 128, 128] every
+    ``checkpoint_every_n_tokens`` tokens, counted by the int64 device tensor
+    ``checkpoint_cu_starts`` [N + 1]. Layouts as for kda_fwd. Argument
+    marshalling only: one launch of the library's forward kernel."""
+    lib = load_library()
+    B, T, Hqk, K = q.shape
+    Hv = v.shape[2]
+    _want(q, "q", torch.bfloat16); _want(k, "k", torch.bfloat16, q.shape)
+    _want(v, "v", torch.bfloat16); _want(g, "g", torch.bfloat16, v.shape)
+    _want(beta, "beta", torch.bfloat16, (B, T, Hv))
+    _want(A_log, "A_log", torch.float32, (Hv,)); _want(dt_bias, "dt_bias", torch.float32, (Hv, K))
+    sdt = {torch.bfloat16: 0, torch.float32: 1}.get(state.dtype)
+    if sdt is None:
+        raise TypeError("state must be bfloat16 or float32")
+    if state.dim() != 4 or tuple(state.shape[1:]) != (Hv, K, K) or not state.is_contiguous():
+        raise ValueError(f"state must be contiguous [num_slots, {Hv}, {K}, {K}]")
+    if out is None:
+        out = torch.empty_like(v)
+    _want(out, "out", torch.bfloat16, v.shape)
+    cu_host = cu_seqlens.cpu() if cu_seqlens is not None else None
+    N = (cu_host.numel() - 1) if cu_host is not None else B
+    idx_host = state_indices.cpu() if state_indices is not None else None
+    cks_host = checkpoint_cu_starts.cpu() if checkpoint_cu_starts is not None else None
+    n_ck = 0
+    if checkpoints is not None:
+        _want(checkpoints, "checkpoints", torch.bfloat16)
+        n_ck = checkpoints.shape[0]
+    def host(t):
+        return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    dev = q.device
+    with torch.cuda.device(dev):
+        rc = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                             _ptr(cu_seqlens), host(cu_host), N, B, T, Hqk, Hv, K,
+                             float("nan") if scale is None else float(scale), float(lower_bound), _ptr(state), sdt,
+                             _ptr(state_indices), host(idx_host), state.shape[0], _ptr(out), _ptr(checkpoints), n_ck,
+                             _ptr(checkpoint_cu_starts), host(cks_host), int(checkpoint_every_n_tokens),
+                             _ptr(device_status), _stream_handle(dev))
     _check(rc)
     return out
 
