@@ -69,6 +69,9 @@ def _load():
             D = ctypes.c_double
             lib.kda_oracle_forward.argtypes = [I, P, I, I, I, I] + [P] * 8 + [D, D, P, P, P]
             lib.kda_oracle_forward.restype = ctypes.c_int
+            lib.kda_oracle_forward_modes.argtypes = ([I, P, I, I, I, I] + [P] * 8 +
+                                                     [D, D, ctypes.c_int, ctypes.c_int, P, P])
+            lib.kda_oracle_forward_modes.restype = ctypes.c_int
             lib.kda_oracle_forward_chunked.argtypes = [I, P, I, I, I, I] + [P] * 8 + [D, D, I, P, P]
             lib.kda_oracle_forward_chunked.restype = ctypes.c_int
             lib.kda_oracle_backward.argtypes = ([I, P, I, I, I, I] + [P] * 10 + [D, D, P] + [P] * 8)
@@ -148,16 +151,27 @@ def _nan(shape):
 
 
 def forward(q, k, v, g, beta, A_log, dt_bias, h0, cu_seqlens=None, scale=None,
-            lower_bound=-5.0, heads=None):
+            lower_bound=-5.0, heads=None, log_space_g=False, presigmoid_beta=False):
     """Sequential FP64 forward. Returns (o [B,T,Hv,DV], final_state [N,Hv,DV,DK]).
 
     ``heads``: optional iterable of query/key heads to compute (with all their
     value heads); entries of other heads are NaN.
+
+    Gate modes of "flashinfer.kda.recurrent_kda" (parameters g and beta):
+    ``log_space_g`` takes g as the per-key log decay (decay exp(g); A_log,
+    dt_bias and lower_bound unused); ``presigmoid_beta`` takes beta as the
+    learning rate itself rather than its logit.
     """
     p = _Problem(q, k, v, g, beta, A_log, dt_bias, h0, cu_seqlens, scale, lower_bound, heads)
     o = _nan((p.B * p.T, p.hv, p.dv))
     hT = _nan((p.nseq, p.hv, p.dv, p.dk))
-    rc = _load().kda_oracle_forward(*p.common(), p.scale, p.lb, _ptr(p.mask), _ptr(o), _ptr(hT))
+    if log_space_g or presigmoid_beta:
+        if heads is not None:
+            raise ValueError("oracle forward: head selection is not offered with the gate modes")
+        rc = _load().kda_oracle_forward_modes(*p.common(), p.scale, p.lb, int(bool(log_space_g)),
+                                              int(bool(presigmoid_beta)), _ptr(o), _ptr(hT))
+    else:
+        rc = _load().kda_oracle_forward(*p.common(), p.scale, p.lb, _ptr(p.mask), _ptr(o), _ptr(hT))
     if rc:
         raise ValueError("oracle forward rejected its arguments")
     return o.reshape(p.token_shape(p.hv, p.dv)), hT

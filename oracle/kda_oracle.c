@@ -17,7 +17,10 @@
  *    value-first FP32 state [N, Hv, V, K]; v, g, beta and the state carry Hv
  *    heads, q and k carry Hqk heads with Hv an integer multiple of Hqk.
  *  - "flashinfer.kda.recurrent_kda", parameter `lower_bound`: the same gate
- *    formula lower_bound * sigmoid(exp(A_log) * (g + dt_bias)).
+ *    formula lower_bound * sigmoid(exp(A_log) * (g + dt_bias)); parameters g
+ *    and beta: g may come precomputed in log space (the decay is then exp(g))
+ *    and beta may come already passed through the sigmoid. Those two inference
+ *    modes are kda_oracle_forward_modes below.
  * The pages name the method (a gated delta rule with per-key-dimension decay)
  * but print no update equations. This file takes the plain reading, per token:
  *     S' = S diag(d);  u = v - S' k^;  S = S' + beta u k^T;  o = scale S q^
@@ -67,6 +70,11 @@ typedef struct {
   int64_t hqk, hv, dk, dv;
   const double *q, *k, *v, *g, *beta, *A_log, *dt_bias, *h0;
   double scale, lb;
+  /* inference gate modes (flashinfer.kda.recurrent_kda, parameters g and beta):
+   * 0 (the default) computes the gate in the kernel and passes beta through a
+   * sigmoid; log_space_g = 1 takes g as the log decay itself, presigmoid_beta =
+   * 1 takes beta as already passed through the sigmoid */
+  int log_space_g, presigmoid_beta;
 } problem;
 
 /* Per-token quantities shared by the forward and backward steps. */
@@ -81,12 +89,20 @@ static void token_prepare(const problem* P, int64_t t, int64_t h, token_terms* t
   const int64_t DK = P->dk;
   tt->rq = l2norm(P->q + (t * P->hqk + qh) * DK, DK, tt->qhat);
   tt->rk = l2norm(P->k + (t * P->hqk + qh) * DK, DK, tt->khat);
-  const double ea = exp(P->A_log[h]);
-  for (int64_t j = 0; j < DK; ++j) {
-    tt->z[j] = ea * (P->g[(t * P->hv + h) * DK + j] + P->dt_bias[h * DK + j]);
-    tt->d[j] = exp(P->lb * sigmoid(tt->z[j]));
+  if (P->log_space_g) {
+    for (int64_t j = 0; j < DK; ++j) {
+      tt->z[j] = 0.0;
+      tt->d[j] = exp(P->g[(t * P->hv + h) * DK + j]);
+    }
+  } else {
+    const double ea = exp(P->A_log[h]);
+    for (int64_t j = 0; j < DK; ++j) {
+      tt->z[j] = ea * (P->g[(t * P->hv + h) * DK + j] + P->dt_bias[h * DK + j]);
+      tt->d[j] = exp(P->lb * sigmoid(tt->z[j]));
+    }
   }
-  tt->b = sigmoid(P->beta[t * P->hv + h]);
+  const double braw = P->beta[t * P->hv + h];
+  tt->b = P->presigmoid_beta ? braw : sigmoid(braw);
 }
 
 static void token_alloc(const problem* P, token_terms* tt) {
@@ -128,13 +144,37 @@ static int head_selected(const problem* P, const uint8_t* qk_mask, int64_t h) {
   return qk_mask == NULL || qk_mask[h / (P->hv / P->hqk)];
 }
 
+static int forward_impl(const problem* PP, const uint8_t* qk_mask, double* o, double* hT);
+
 int kda_oracle_forward(int64_t nseq, const int64_t* cu, int64_t hqk, int64_t hv, int64_t dk,
                        int64_t dv, const double* q, const double* k, const double* v,
                        const double* g, const double* beta, const double* A_log,
                        const double* dt_bias, const double* h0, double scale, double lower_bound,
                        const uint8_t* qk_mask, double* o, double* hT) {
   if (nseq <= 0 || hqk <= 0 || hv <= 0 || hv % hqk != 0 || dk <= 0 || dv <= 0) return 1;
-  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound};
+  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound, 0, 0};
+  return forward_impl(&P, qk_mask, o, hT);
+}
+
+/* The same forward with the inference page's gate modes: log_space_g = 1 reads
+ * g as the per-key log decay (d = exp(g); A_log, dt_bias and lower_bound are
+ * not used), presigmoid_beta = 1 reads beta as the learning rate itself. */
+int kda_oracle_forward_modes(int64_t nseq, const int64_t* cu, int64_t hqk, int64_t hv, int64_t dk,
+                             int64_t dv, const double* q, const double* k, const double* v,
+                             const double* g, const double* beta, const double* A_log,
+                             const double* dt_bias, const double* h0, double scale, double lower_bound,
+                             int log_space_g, int presigmoid_beta, double* o, double* hT) {
+  if (nseq <= 0 || hqk <= 0 || hv <= 0 || hv % hqk != 0 || dk <= 0 || dv <= 0) return 1;
+  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound,
+               log_space_g != 0, presigmoid_beta != 0};
+  return forward_impl(&P, NULL, o, hT);
+}
+
+static int forward_impl(const problem* PP, const uint8_t* qk_mask, double* o, double* hT) {
+  const problem P = *PP;
+  const int64_t nseq = P.nseq, hv = P.hv, dk = P.dk, dv = P.dv;
+  const int64_t* cu = P.cu;
+  const double* h0 = P.h0;
   const int64_t units = nseq * hv;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t un = 0; un < units; ++un) {
@@ -175,7 +215,7 @@ int kda_oracle_forward_chunked(int64_t nseq, const int64_t* cu, int64_t hqk, int
                                double scale, double lower_bound, int64_t chunk, double* o,
                                double* hT) {
   if (nseq <= 0 || hqk <= 0 || hv <= 0 || hv % hqk != 0 || chunk <= 0) return 1;
-  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound};
+  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound, 0, 0};
   const int64_t units = nseq * hv;
   const int64_t C = chunk;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -278,7 +318,7 @@ int kda_oracle_backward(int64_t nseq, const int64_t* cu, int64_t hqk, int64_t hv
                         double* dg, double* dbeta, double* dA_log, double* ddt_bias,
                         double* dh0) {
   if (nseq <= 0 || hqk <= 0 || hv <= 0 || hv % hqk != 0 || dk <= 0 || dv <= 0) return 1;
-  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound};
+  problem P = {nseq, cu, hqk, hv, dk, dv, q, k, v, g, beta, A_log, dt_bias, h0, scale, lower_bound, 0, 0};
   const int64_t r = hv / hqk;
   const int64_t DK = dk, DV = dv;
   const int64_t SZ = DV * DK;

@@ -359,3 +359,67 @@ def test_head_subset_matches_full_run():
     np.testing.assert_array_equal(part[5][2:4], full[5][2:4])
     np.testing.assert_array_equal(part[7][:, 2:4], full[7][:, 2:4])
     assert np.all(np.isnan(part[2][:, :, 0:2]))
+
+
+# ------------------------------------------------- inference gate modes
+# "flashinfer.kda.recurrent_kda", parameters g ("log-space if pre-computed") and
+# beta ("pre-sigmoided unless beta_is_logit"): with the gate precomputed the
+# decay is exp(g) per key dimension; with beta presigmoided it is the learning
+# rate itself.
+
+def test_log_space_gate_scales_key_columns_and_ignores_gate_parameters():
+    """log_space_g with g = ln(m / (m + 1)) per key dim m and presigmoided beta
+    = 0 (no write): S_T = h0 diag(prod_t m/(m+1)). A_log and dt_bias are NaN,
+    so reading either would poison the result."""
+    T, dk, dv = 3, 6, 4
+    m = np.arange(1, dk + 1, dtype=np.float64)
+    rng = np.random.default_rng(40)
+    p = dict(q=rng.standard_normal((1, T, 1, dk)), k=rng.standard_normal((1, T, 1, dk)),
+             v=rng.standard_normal((1, T, 1, dv)),
+             g=np.broadcast_to(np.log(m / (m + 1)), (1, T, 1, dk)).copy(),
+             beta=np.zeros((1, T, 1)), A_log=np.array([np.nan]), dt_bias=np.full((1, dk), np.nan),
+             h0=rng.standard_normal((1, 1, dv, dk)))
+    o, hT = fwd(p, log_space_g=True, presigmoid_beta=True, lower_bound=np.nan)
+    np.testing.assert_allclose(hT[0, 0], p["h0"][0, 0] * ((m / (m + 1)) ** T)[None, :], rtol=1e-13)
+    assert np.isfinite(o).all()
+
+
+def test_presigmoid_beta_first_token_closed_form():
+    """First token, no decay (log-space g = 0), presigmoided beta b, q = k:
+    o = scale (h0 k^ (1 - b |k^|^2) + b |k^|^2 v)."""
+    dk, dv, b = 8, 5, 0.3
+    rng = np.random.default_rng(41)
+    k = rng.standard_normal((1, 1, 1, dk))
+    khat = k[0, 0, 0] / math.sqrt(float(np.sum(k * k)) + 1e-6)
+    kk = float(khat @ khat)
+    p = dict(q=k.copy(), k=k, v=rng.standard_normal((1, 1, 1, dv)), g=np.zeros((1, 1, 1, dk)),
+             beta=np.full((1, 1, 1), b), A_log=np.array([0.0]), dt_bias=np.zeros((1, dk)),
+             h0=rng.standard_normal((1, 1, dv, dk)))
+    o, _ = fwd(p, scale=1.0, log_space_g=True, presigmoid_beta=True)
+    want = p["h0"][0, 0] @ khat * (1 - b * kk) + b * kk * p["v"][0, 0, 0]
+    np.testing.assert_allclose(o[0, 0, 0], want, rtol=1e-13)
+    # beta = 1 presigmoided overwrites the memory at the key: o = scale v |k^|^2 + h0 k^ (1 - |k^|^2)
+    p["beta"][:] = 1.0
+    o1, _ = fwd(p, scale=1.0, log_space_g=True, presigmoid_beta=True)
+    np.testing.assert_allclose(o1[0, 0, 0], p["v"][0, 0, 0], rtol=0, atol=1e-6 * np.abs(p["v"]).max()
+                               + 1e-6 * np.abs(p["h0"]).max())
+
+
+def test_gate_modes_agree_with_in_kernel_gate_on_transformed_inputs():
+    """Feeding the precomputed log decay lb sigmoid(exp(A_log)(g + dt_bias))
+    and the presigmoided beta to the modes reproduces the default forward, one
+    mode at a time and both together (packed, GQA)."""
+    p = rand_problem(42, [7, 12, 3], 2, 4, 16, 12)
+    o_ref, s_ref = fwd(p)
+    lb = -5.0
+    z = np.exp(p["A_log"])[None, None, :, None] * (p["g"] + p["dt_bias"][None, None])
+    g_log = lb / (1.0 + np.exp(-z))
+    b_sig = 1.0 / (1.0 + np.exp(-p["beta"]))
+    for lg, pb in [(True, False), (False, True), (True, True)]:
+        x = dict(p)
+        if lg:
+            x["g"] = g_log
+        if pb:
+            x["beta"] = b_sig
+        o, s = fwd(x, log_space_g=lg, presigmoid_beta=pb)
+        assert rel(o, o_ref) < 1e-13 and rel(s, s_ref) < 1e-13, (lg, pb)
