@@ -376,7 +376,7 @@ def bench_decode(args):
     o = torch.empty_like(v)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
-        kda_decode(q, k, v, g, beta, A_log, dt_bias, state, out=o)
+        kda_decode(q, k, v, g, beta, A_log, dt_bias, state, out=o, use_gate_in_kernel=True, beta_is_logit=True)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(0)
     sampler.start()
@@ -384,7 +384,7 @@ def bench_decode(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        kda_decode(q, k, v, g, beta, A_log, dt_bias, state, out=o)
+        kda_decode(q, k, v, g, beta, A_log, dt_bias, state, out=o, use_gate_in_kernel=True, beta_is_logit=True)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()

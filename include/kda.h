@@ -181,18 +181,33 @@ kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16*
 /* State element types for kda_decode. */
 enum { KDA_STATE_BF16 = 0, KDA_STATE_FP32 = 1 };
 
+/* Gate modes of kda_decode and kda_prefill (flashinfer.kda.recurrent_kda,
+ * parameters g, beta, A_log, use_gate_in_kernel, lower_bound and
+ * beta_is_logit):
+ *   use_gate_in_kernel = 1: the decay is computed in the kernel,
+ *       d = exp(lower_bound * sigmoid(exp(A_log[h]) * (g + dt_bias[h]))),
+ *       with lower_bound -5 (the sigmoid-bounded formula; the softplus gate
+ *       the page names without a formula is not offered: KDA_ERR_UNSUPPORTED
+ *       for any other lower_bound);
+ *   use_gate_in_kernel = 0: g is already the log decay, d = exp(g); A_log and
+ *       dt_bias may be NULL and lower_bound is ignored;
+ *   beta_is_logit = 1: the learning rate is sigmoid(beta);
+ *   beta_is_logit = 0: beta is the learning rate itself (already sigmoided).
+ * The training entry points kda_fwd / kda_bwd always use the in-kernel gate
+ * and beta logits. */
+
 /* One decode step, T = 1 (flashinfer.kda.recurrent_kda, description and the
  * parameters q ("T=1 selects decode"), initial_state ("Updated in-place") and
  * ssm_state_indices): for every sequence n and value head h, with the state S
  * of pool slot state_indices[n] (slot n when state_indices is NULL),
  *   S' = S diag(d),  u = v - S' k^,  S <- S' + beta u k^^T,  o = scale S q^
- * with q^, k^ L2-normalised in the kernel (eps 1e-6), the gate computed in the
- * kernel, d = exp(lower_bound * sigmoid(exp(A_log[h]) * (g + dt_bias[h]))),
- * and beta = sigmoid(logit). Arithmetic is FP32; a BF16 state is read, updated
+ * with q^, k^ L2-normalised in the kernel (eps 1e-6) and d and beta as the
+ * gate modes above say. Arithmetic is FP32; a BF16 state is read, updated
  * in FP32 and written back rounded to nearest even.
  *   q, k            BF16 [N, 1, Hqk, 128]
- *   v, g            BF16 [N, 1, Hv, 128]; beta BF16 [N, 1, Hv] (logits)
- *   A_log           FP32 [Hv]; dt_bias FP32 [Hv, 128]
+ *   v, g            BF16 [N, 1, Hv, 128]; beta BF16 [N, 1, Hv]
+ *   A_log           FP32 [Hv]; dt_bias FP32 [Hv, 128] (may be NULL when
+ *                   use_gate_in_kernel is 0)
  *   state           [num_slots, Hv, 128, 128] value-first, KDA_STATE_BF16 or
  *                   KDA_STATE_FP32 per state_dtype; read and written in place
  *   state_indices   device int32 [N] and its trusted host mirror
@@ -210,7 +225,8 @@ kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, c
                       const kda_bf16* beta, const float* A_log, const float* dt_bias, void* state,
                       int32_t state_dtype, const int32_t* state_indices,
                       const int32_t* state_indices_host, int64_t num_slots, int64_t N, int64_t Hqk,
-                      int64_t Hv, int64_t head_dim, float scale, float lower_bound, kda_bf16* o,
+                      int64_t Hv, int64_t head_dim, float scale, float lower_bound,
+                      int32_t use_gate_in_kernel, int32_t beta_is_logit, kda_bf16* o,
                       struct CUstream_st* stream);
 
 /* Inference prefill over whole sequences from a state pool (flashinfer.kda.
@@ -220,10 +236,16 @@ kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, c
  * sequence n and value head h, starting from the state of pool slot
  * state_indices[n] (slot n when NULL) and writing the final state back to it,
  * with the output o, and nothing saved for a backward. Same layouts, head
- * mapping, gate, beta, scale and lower_bound rules as kda_fwd (fixed layout
- * with cu_seqlens NULL; packed with B = 1, device cu_seqlens and its trusted
- * host mirror). Arithmetic as in kda_fwd; a BF16 pool is read, carried in FP32
- * and written back rounded to nearest even.
+ * mapping and scale rules as kda_fwd (fixed layout with cu_seqlens NULL;
+ * packed with B = 1, device cu_seqlens and its trusted host mirror); d and
+ * beta as the gate modes above say. With use_gate_in_kernel = 1 and
+ * beta_is_logit = 1 the arithmetic is that of kda_fwd, bit for bit. A BF16 pool
+ * is read, carried in FP32 and written back rounded to nearest even.
+ * With use_gate_in_kernel = 0, every g must lie in [-5, 0], the range of the
+ * in-kernel gate: the chunked evaluation scales keys by the inverse of the
+ * decay accumulated over up to 16 tokens, which leaves FP32 range below about
+ * -5.4 per token. The kernel checks this; a value outside the range (or NaN)
+ * sets bit 1 (value 2) of device_status and o and the pool are then unspecified.
  *   state            [num_slots, Hv, 128, 128] value-first, state_dtype
  *                    KDA_STATE_BF16 or KDA_STATE_FP32, read and written in place
  *   state_indices    device int32 [N] and its host mirror (both NULL, or both
@@ -237,16 +259,18 @@ kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, c
  *                    hold those cumulative counts, ending at num_checkpoints.
  *                    checkpoint_every_n_tokens: a positive multiple of 16 (0
  *                    with checkpoints NULL).
- *   device_status    optional device int32, set to 1 if a bounded device wait
- *                    gave up (then o and the pool are incomplete); NULL uses a
- *                    word inside the library.
+ *   device_status    optional device int32: bit 0 (value 1) is set if a
+ *                    bounded device wait gave up (then o and the pool are
+ *                    incomplete), bit 1 (value 2) as said above; bits are only
+ *                    ever set, never cleared. NULL uses a word inside the library.
  * Units run in index order. Validation errors return before any launch;
  * otherwise the work is enqueued on `stream`. Nothing is allocated. */
 kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
                        const kda_bf16* beta, const float* A_log, const float* dt_bias,
                        const int64_t* cu_seqlens, const int64_t* cu_seqlens_host, int64_t num_seqs,
                        int64_t B, int64_t T, int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
-                       float lower_bound, void* state, int32_t state_dtype, const int32_t* state_indices,
+                       float lower_bound, int32_t use_gate_in_kernel, int32_t beta_is_logit,
+                       void* state, int32_t state_dtype, const int32_t* state_indices,
                        const int32_t* state_indices_host, int64_t num_slots, kda_bf16* o,
                        kda_bf16* checkpoints, int64_t num_checkpoints, const int64_t* checkpoint_cu_starts,
                        const int64_t* checkpoint_cu_starts_host, int64_t checkpoint_every_n_tokens,

@@ -13,6 +13,10 @@ Recipe (one ``torch.Generator('cpu')`` per workload, seeded, draws in this order
   7. dfinal_state = 0.05 * randn      (float32, same shape as h0)
 The distributions are those of the five named workloads below; the draw order
 is this module's choice (the workloads fix distributions and seeds only).
+
+Inference gate modes (``precomputed_gate_inputs``, a generator of its own):
+a log-space gate g = bfloat16(-5 * rand), in [-5, 0], and an already
+sigmoided beta = bfloat16(rand), in [0, 1].
 """
 
 from __future__ import annotations
@@ -100,6 +104,16 @@ def make_inputs(B: int, T: int, hqk: int, hv: int, seed: int, lengths=None,
     dfinal_state = 0.05 * torch.randn((nseq, hv, dim, dim), generator=gen, dtype=torch.float32)
     return dict(q=q, k=k, v=v, g=g, beta=beta, A_log=A_log, dt_bias=dt_bias, h0=h0, do=do,
                 dfinal_state=dfinal_state, cu_seqlens=cu)
+
+
+def precomputed_gate_inputs(x: dict, seed: int) -> dict:
+    """Copy of ``x`` whose g is drawn as a log-space gate in [-5, 0] and whose
+    beta is drawn as a learning rate in [0, 1] (same shapes, bfloat16)."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    y = dict(x)
+    y["g"] = (-5.0 * torch.rand(x["g"].shape, generator=gen, dtype=torch.float32)).to(torch.bfloat16)
+    y["beta"] = torch.rand(x["beta"].shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    return y
 
 
 def _cumsum(xs):

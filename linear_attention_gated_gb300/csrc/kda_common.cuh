@@ -38,7 +38,8 @@ struct Problem {
   float* utape;           // [Ttot, Hv, 128]: u_t = v_t - S'_t k^_t of every token (forward -> backward)
   float* abtape;          // [n_sub_chunks, Hv, 2, 16, 16]: the FP32 A (strictly lower) and B (lower)
                           // matrices of every sub-chunk (forward -> backward)
-  int32_t* status;        // device status word: non-zero when a bounded device wait gave up
+  int32_t* status;        // device status word: bit 0 when a bounded device wait gave up, bit 1
+                          // when a prefill log-space gate value is outside [-5, 0]
   int64_t N, Hqk, Hv;
   int32_t r;              // Hv / Hqk
   float scale, lb;
@@ -61,6 +62,8 @@ struct PrefillArgs {
   __nv_bfloat16* ck;           // [C, Hv, 128, 128] BF16 value-first, or null
   const int64_t* ck_starts;    // [N + 1] first checkpoint row of each sequence
   int ck_every_chunks;         // checkpoint interval in sub-chunks
+  int gate_in_kernel;          // 1: d = exp(lb sigmoid(exp(A_log)(g + dt_bias))); 0: g is log d, in [-5, 0]
+  int beta_logit;              // 1: beta = sigmoid(input); 0: the input is beta
 };
 
 struct BwdArgs {

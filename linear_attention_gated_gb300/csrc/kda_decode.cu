@@ -8,7 +8,8 @@
 // column, delta-corrected and written back, and the output token produced:
 //   S' = S diag(d),  u = v - S' k^,  S <- S' + beta u k^^T,  o = s S q^
 // with q^, k^ L2-normalised, d = exp(lb sigmoid(exp(A_log) (g + dt_bias)))
-// and beta = sigmoid(logit). Since S q^ = S' q^ + beta u (k^ . q^), each state
+// (or d = exp(g) with the gate precomputed in log space) and beta = sigmoid(
+// logit) (or beta as given, already sigmoided). Since S q^ = S' q^ + beta u (k^ . q^), each state
 // row needs two dot products with the decayed row and one rank-1 update.
 //
 // The step moves the state through HBM once in each direction and does 8 flops
@@ -37,7 +38,7 @@ struct DecodeArgs {
   const __nv_bfloat16* k;     // [N, Hqk, 128]
   const __nv_bfloat16* v;     // [N, Hv, 128]
   const __nv_bfloat16* g;     // [N, Hv, 128]
-  const __nv_bfloat16* beta;  // [N, Hv] (logits)
+  const __nv_bfloat16* beta;  // [N, Hv] (logits when beta_logit)
   const float* A_log;         // [Hv]
   const float* dt_bias;       // [Hv, 128]
   void* state;                // [num_slots, Hv, 128, 128], BF16 or FP32
@@ -45,6 +46,8 @@ struct DecodeArgs {
   __nv_bfloat16* o;           // [N, Hv, 128]
   int64_t Hqk, Hv, r;
   float scale, lb;
+  int gate_in_kernel;         // 1: d = exp(lb sigmoid(exp(A_log)(g + dt_bias))); 0: d = exp(g)
+  int beta_logit;             // 1: beta = sigmoid(input); 0: the input is beta
 };
 
 // 8 consecutive state elements of one row <-> FP32 registers
@@ -123,17 +126,19 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks<StateT>) kda_decode
   sq = row16_sum(sq);
   sk = row16_sum(sk);
   const float rq = inv_norm_of(sq), rk = inv_norm_of(sk);
-  const float ea = expf(a.A_log[h]);
+  const float ea = a.gate_in_kernel ? expf(a.A_log[h]) : 0.f;
   float d[8], kq = 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     qv[e] *= rq;
     kv[e] *= rk;
     kq += kv[e] * qv[e];
-    d[e] = expf(log_decay_of(a.lb, ea * (gv[e] + a.dt_bias[h * kDim + 8 * hl + e])));
+    d[e] = a.gate_in_kernel ? expf(log_decay_of(a.lb, ea * (gv[e] + a.dt_bias[h * kDim + 8 * hl + e])))
+                            : expf(gv[e]);
   }
   kq = row16_sum(kq);
-  const float bt = sigmoid_of(__bfloat162float(a.beta[n * a.Hv + h]));
+  const float braw = __bfloat162float(a.beta[n * a.Hv + h]);
+  const float bt = a.beta_logit ? sigmoid_of(braw) : braw;
   const __nv_bfloat16* vrow = a.v + (n * a.Hv + h) * kDim;
   __nv_bfloat16* orow = a.o + (n * a.Hv + h) * kDim;
   if constexpr (kStaged<StateT>) {
@@ -191,7 +196,8 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
                                  const kda_bf16* beta, const float* A_log, const float* dt_bias, void* state,
                                  int32_t state_dtype, const int32_t* state_indices,
                                  const int32_t* state_indices_host, int64_t num_slots, int64_t N, int64_t Hqk,
-                                 int64_t Hv, int64_t head_dim, float scale, float lower_bound, kda_bf16* o,
+                                 int64_t Hv, int64_t head_dim, float scale, float lower_bound,
+                                 int32_t use_gate_in_kernel, int32_t beta_is_logit, kda_bf16* o,
                                  struct CUstream_st* stream) {
   if (N < 1 || Hqk < 1 || Hv < 1) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: N, Hqk and Hv must be positive");
   if (Hv % Hqk != 0) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: Hv must be a multiple of Hqk");
@@ -199,10 +205,13 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
   const float s_def = 1.0f / std::sqrt((float)kda::kDim);
   if (!std::isnan(scale) && scale != s_def)
     return dfail(KDA_ERR_UNSUPPORTED, "decode: scale must be 1/sqrt(128) (NaN selects it)");
-  if (lower_bound != -5.0f) return dfail(KDA_ERR_UNSUPPORTED, "decode: lower_bound must be -5");
+  if ((use_gate_in_kernel != 0 && use_gate_in_kernel != 1) || (beta_is_logit != 0 && beta_is_logit != 1))
+    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: use_gate_in_kernel and beta_is_logit must be 0 or 1");
+  if (use_gate_in_kernel && lower_bound != -5.0f)
+    return dfail(KDA_ERR_UNSUPPORTED, "decode: lower_bound must be -5 with the gate computed in the kernel");
   if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32)
     return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_dtype must be KDA_STATE_BF16 or KDA_STATE_FP32");
-  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !state || !o)
+  if (!q || !k || !v || !g || !beta || !state || !o || (use_gate_in_kernel && (!A_log || !dt_bias)))
     return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: null tensor pointer");
   if ((state_indices == nullptr) != (state_indices_host == nullptr))
     return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_indices needs its host mirror (and the reverse)");
@@ -225,8 +234,9 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
   const Span out{o, 2 * (size_t)N * Hv * kda::kDim};
   const Span ins[] = {{q, 2 * (size_t)N * Hqk * kda::kDim}, {k, 2 * (size_t)N * Hqk * kda::kDim},
                       {v, 2 * (size_t)N * Hv * kda::kDim},  {g, 2 * (size_t)N * Hv * kda::kDim},
-                      {beta, 2 * (size_t)N * Hv},           {A_log, 4 * (size_t)Hv},
-                      {dt_bias, 4 * (size_t)Hv * kda::kDim}};
+                      {beta, 2 * (size_t)N * Hv},
+                      {A_log, use_gate_in_kernel ? 4 * (size_t)Hv : 0},
+                      {dt_bias, use_gate_in_kernel ? 4 * (size_t)Hv * kda::kDim : 0}};
   for (const Span& in : ins)
     if (overlap(in, st) || overlap(in, out)) return dfail(KDA_ERR_ALIASING, "decode: an input overlaps the state or o");
   if (overlap(st, out)) return dfail(KDA_ERR_ALIASING, "decode: o overlaps the state");
@@ -256,6 +266,8 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
   a.r = Hv / Hqk;
   a.scale = s_def;
   a.lb = lower_bound;
+  a.gate_in_kernel = use_gate_in_kernel;
+  a.beta_logit = beta_is_logit;
   const unsigned grid = (unsigned)(N * Hv);
   const size_t smem = state_dtype == KDA_STATE_BF16 ? esz * kda::kDim * kda::kDim : 0;
   if (state_dtype == KDA_STATE_BF16) {

@@ -129,10 +129,14 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
 
   const int ti = tid >> 4;
   const int c8 = (tid & 15) * 8;
-  const float ea = expf(P.A_log[h]);
+  // prefill gate modes: g already in log space (A_log and dt_bias unused), beta already sigmoided
+  const bool log_g = kPf && !pf.gate_in_kernel;
+  const bool beta_logit = !kPf || pf.beta_logit;
+  bool g_range_bad = false;
+  const float ea = log_g ? 0.f : expf(P.A_log[h]);
   float dtb[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) dtb[e] = P.dt_bias[h * kDim + c8 + e];
+  for (int e = 0; e < 8; ++e) dtb[e] = log_g ? 0.f : P.dt_bias[h * kDim + c8 + e];
 
   const int64_t nchunks = (si.len + kChunk - 1) / kChunk;
   const int ck_every = kCkTokens / kChunk;
@@ -177,7 +181,12 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         const float z = ea * (gv[e] + dtb[e]);
         qv[e] *= rq;
         kv[e] *= rk;
-        la[e] = valid ? log_decay_of(P.lb, z) : 0.f;
+        if (log_g) {
+          g_range_bad |= valid && !(gv[e] >= -5.f && gv[e] <= 0.f);
+          la[e] = valid ? gv[e] : 0.f;
+        } else {
+          la[e] = valid ? log_decay_of(P.lb, z) : 0.f;
+        }
       }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -187,7 +196,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         *reinterpret_cast<float4*>(sm.Pa + col) = make_float4(la[o], la[o + 1], la[o + 2], la[o + 3]);
         *reinterpret_cast<float4*>(sm.Vs + col) = make_float4(vv[o], vv[o + 1], vv[o + 2], vv[o + 3]);
       }
-      if (tid < kChunk) sm.bs[tid] = (tid < ntc) ? sigmoid_of(braw) : 0.f;
+      if (tid < kChunk) sm.bs[tid] = (tid < ntc) ? (beta_logit ? sigmoid_of(braw) : braw) : 0.f;
     }
     __syncthreads();
     if (tid < kDim) {
@@ -447,8 +456,9 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       }
     }
   } else if (tid == 0) {
-    atomicExch(P.status, 1);
+    atomicOr(P.status, 1);
   }
+  if (g_range_bad) atomicOr(P.status, 2);
   tc::fence_before();
   __syncthreads();
   if (warp == 0) {

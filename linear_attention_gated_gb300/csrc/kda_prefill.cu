@@ -5,7 +5,8 @@
 // the training forward kernel's prefill instantiation (kda_fwd.cu): the same
 // chunked arithmetic, without the backward's tapes and checkpoints, with the
 // initial state read from and the final state written back to the pool slot,
-// and optional BF16 state checkpoints.
+// optional BF16 state checkpoints, and the page's gate modes (g precomputed in
+// log space, beta already sigmoided).
 #include "../../include/kda.h"
 #include "kda_common.cuh"
 
@@ -38,7 +39,8 @@ extern "C" kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kd
                                   const kda_bf16* beta, const float* A_log, const float* dt_bias,
                                   const int64_t* cu_seqlens, const int64_t* cu_seqlens_host, int64_t num_seqs,
                                   int64_t B, int64_t T, int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
-                                  float lower_bound, void* state, int32_t state_dtype,
+                                  float lower_bound, int32_t use_gate_in_kernel, int32_t beta_is_logit,
+                                  void* state, int32_t state_dtype,
                                   const int32_t* state_indices, const int32_t* state_indices_host,
                                   int64_t num_slots, kda_bf16* o, kda_bf16* checkpoints,
                                   int64_t num_checkpoints, const int64_t* checkpoint_cu_starts,
@@ -52,10 +54,13 @@ extern "C" kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kd
   const float s_def = 1.0f / std::sqrt((float)kda::kDim);
   if (!std::isnan(scale) && scale != s_def)
     return pfail(KDA_ERR_UNSUPPORTED, "prefill: scale must be 1/sqrt(128) (NaN selects it)");
-  if (lower_bound != -5.0f) return pfail(KDA_ERR_UNSUPPORTED, "prefill: lower_bound must be -5");
+  if ((use_gate_in_kernel != 0 && use_gate_in_kernel != 1) || (beta_is_logit != 0 && beta_is_logit != 1))
+    return pfail(KDA_ERR_INVALID_ARGUMENT, "prefill: use_gate_in_kernel and beta_is_logit must be 0 or 1");
+  if (use_gate_in_kernel && lower_bound != -5.0f)
+    return pfail(KDA_ERR_UNSUPPORTED, "prefill: lower_bound must be -5 with the gate computed in the kernel");
   if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32)
     return pfail(KDA_ERR_INVALID_ARGUMENT, "prefill: state_dtype must be KDA_STATE_BF16 or KDA_STATE_FP32");
-  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !state || !o)
+  if (!q || !k || !v || !g || !beta || !state || !o || (use_gate_in_kernel && (!A_log || !dt_bias)))
     return pfail(KDA_ERR_INVALID_ARGUMENT, "prefill: null tensor pointer");
   if ((cu_seqlens == nullptr) != (cu_seqlens_host == nullptr))
     return pfail(KDA_ERR_INVALID_ARGUMENT, "prefill: cu_seqlens needs its host mirror (and the reverse)");
@@ -118,8 +123,10 @@ extern "C" kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kd
                        {device_status, device_status ? sizeof(int32_t) : 0}};
   const Span ins[] = {{q, 2 * (size_t)Ttot * Hqk * kda::kDim}, {k, 2 * (size_t)Ttot * Hqk * kda::kDim},
                       {v, 2 * (size_t)Ttot * Hv * kda::kDim},  {g, 2 * (size_t)Ttot * Hv * kda::kDim},
-                      {beta, 2 * (size_t)Ttot * Hv},           {A_log, 4 * (size_t)Hv},
-                      {dt_bias, 4 * (size_t)Hv * kda::kDim},    {cu_seqlens, cu_seqlens ? 8 * (size_t)(N + 1) : 0},
+                      {beta, 2 * (size_t)Ttot * Hv},
+                      {A_log, use_gate_in_kernel ? 4 * (size_t)Hv : 0},
+                      {dt_bias, use_gate_in_kernel ? 4 * (size_t)Hv * kda::kDim : 0},
+                      {cu_seqlens, cu_seqlens ? 8 * (size_t)(N + 1) : 0},
                       {state_indices, state_indices ? 4 * (size_t)N : 0},
                       {checkpoint_cu_starts, checkpoint_cu_starts ? 8 * (size_t)(N + 1) : 0}};
   for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
@@ -164,6 +171,8 @@ extern "C" kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kd
   pf.ck = reinterpret_cast<__nv_bfloat16*>(checkpoints);
   pf.ck_starts = checkpoint_cu_starts;
   pf.ck_every_chunks = checkpoints ? (int)(checkpoint_every_n_tokens / kda::kChunk) : 1;
+  pf.gate_in_kernel = use_gate_in_kernel;
+  pf.beta_logit = beta_is_logit;
   if ((e = kda::launch_prefill(P, fo, pf, N * Hv, stream)) != cudaSuccess)
     return pfail(KDA_ERR_CUDA, cudaGetErrorString(e));
   return KDA_OK;

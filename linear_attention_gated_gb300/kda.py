@@ -70,10 +70,11 @@ def load_library(path: str = LIB_PATH):
     lib.kda_last_error_message.restype = ctypes.c_char_p
     lib.kda_bwd_noalloc.argtypes = [P] * 8 + [P, P, I, I, I, I, I, I, F, F] + [P] * 10 + [P]
     lib.kda_bwd_noalloc.restype = ctypes.c_int
-    lib.kda_decode.argtypes = [P] * 8 + [ctypes.c_int32, P, P, I, I, I, I, I, F, F, P, P]
+    lib.kda_decode.argtypes = [P] * 8 + [ctypes.c_int32, P, P, I, I, I, I, I, F, F, ctypes.c_int32,
+                                         ctypes.c_int32, P, P]
     lib.kda_decode.restype = ctypes.c_int
-    lib.kda_prefill.argtypes = [P] * 7 + [P, P, I, I, I, I, I, I, F, F, P, ctypes.c_int32, P, P, I, P, P, I, P, P,
-                                          I, P, P]
+    lib.kda_prefill.argtypes = [P] * 7 + [P, P, I, I, I, I, I, I, F, F, ctypes.c_int32, ctypes.c_int32, P,
+                                          ctypes.c_int32, P, P, I, P, P, I, P, P, I, P, P]
     lib.kda_prefill.restype = ctypes.c_int
     lib.kda_selftest_device_timeout.argtypes = [P]
     lib.kda_selftest_device_timeout.restype = ctypes.c_int
@@ -283,15 +284,25 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_
     return tuple(out)
 
 
+def _want_gate_params(A_log, dt_bias, Hv, K, use_gate_in_kernel):
+    if use_gate_in_kernel or A_log is not None:
+        _want(A_log, "A_log", torch.float32, (Hv,))
+    if use_gate_in_kernel or dt_bias is not None:
+        _want(dt_bias, "dt_bias", torch.float32, (Hv, K))
+
+
 def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scale=None, lower_bound=-5.0,
-               out=None):
+               out=None, use_gate_in_kernel=False, beta_is_logit=False):
     """One decode step (T = 1): updates ``state`` in place and returns o.
 
-    q, k [N, 1, Hqk, 128] and v, g [N, 1, Hv, 128] BF16, beta [N, 1, Hv] BF16
-    logits, A_log [Hv] and dt_bias [Hv, 128] FP32; state [num_slots, Hv, 128,
-    128] BF16 or FP32 (value-first), read and written at slot state_indices[n]
-    (int32 [N], on the device; slot n when None). Argument marshalling only: the
-    step is one launch of the library's decode kernel."""
+    q, k [N, 1, Hqk, 128] and v, g [N, 1, Hv, 128] BF16, beta [N, 1, Hv] BF16,
+    A_log [Hv] and dt_bias [Hv, 128] FP32 (None allowed unless
+    use_gate_in_kernel); state [num_slots, Hv, 128, 128] BF16 or FP32
+    (value-first), read and written at slot state_indices[n] (int32 [N], on the
+    device; slot n when None). Gate modes and their defaults as on the
+    recurrent_kda page: g is the log decay unless ``use_gate_in_kernel``, beta
+    is already sigmoided unless ``beta_is_logit``. Argument marshalling only:
+    the step is one launch of the library's decode kernel."""
     lib = load_library()
     N, T, Hqk, K = q.shape
     Hv = v.shape[2]
@@ -300,7 +311,7 @@ def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scal
     _want(q, "q", torch.bfloat16); _want(k, "k", torch.bfloat16, q.shape)
     _want(v, "v", torch.bfloat16); _want(g, "g", torch.bfloat16, v.shape)
     _want(beta, "beta", torch.bfloat16, (N, 1, Hv))
-    _want(A_log, "A_log", torch.float32, (Hv,)); _want(dt_bias, "dt_bias", torch.float32, (Hv, K))
+    _want_gate_params(A_log, dt_bias, Hv, K, use_gate_in_kernel)
     if state.dtype == torch.bfloat16:
         sdt = 0
     elif state.dtype == torch.float32:
@@ -324,27 +335,31 @@ def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scal
                             _ptr(state), sdt, _ptr(idx_dev) if idx_dev is not None else None,
                             ctypes.c_void_p(idx_host.data_ptr()) if idx_host is not None else None,
                             state.shape[0], N, Hqk, Hv, K, float("nan") if scale is None else float(scale),
-                            float(lower_bound), _ptr(out), _stream_handle(dev))
+                            float(lower_bound), int(bool(use_gate_in_kernel)), int(bool(beta_is_logit)),
+                            _ptr(out), _stream_handle(dev))
     _check(rc)
     return out
 
 
 def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_indices=None, checkpoints=None,
                 checkpoint_cu_starts=None, checkpoint_every_n_tokens=0, scale=None, lower_bound=-5.0, out=None,
-                device_status=None):
+                device_status=None, use_gate_in_kernel=False, beta_is_logit=False):
     """Inference prefill from a state pool: returns o; the final state of every
     sequence is written back to its slot of ``state`` (BF16 or FP32, [num_slots,
     Hv, 128, 128]); optional BF16 ``checkpoints`` [C, Hv, 128, 128] every
     ``checkpoint_every_n_tokens`` tokens, counted by the int64 device tensor
-    ``checkpoint_cu_starts`` [N + 1]. Layouts as for kda_fwd. Argument
-    marshalling only: one launch of the library's forward kernel."""
+    ``checkpoint_cu_starts`` [N + 1]. Layouts as for kda_fwd. Gate modes as
+    for kda_decode; with the gate precomputed (use_gate_in_kernel False) every
+    g must lie in [-5, 0], else bit 1 of ``device_status`` (int32 device
+    tensor) is set. Argument marshalling only: one launch of the library's
+    forward kernel."""
     lib = load_library()
     B, T, Hqk, K = q.shape
     Hv = v.shape[2]
     _want(q, "q", torch.bfloat16); _want(k, "k", torch.bfloat16, q.shape)
     _want(v, "v", torch.bfloat16); _want(g, "g", torch.bfloat16, v.shape)
     _want(beta, "beta", torch.bfloat16, (B, T, Hv))
-    _want(A_log, "A_log", torch.float32, (Hv,)); _want(dt_bias, "dt_bias", torch.float32, (Hv, K))
+    _want_gate_params(A_log, dt_bias, Hv, K, use_gate_in_kernel)
     sdt = {torch.bfloat16: 0, torch.float32: 1}.get(state.dtype)
     if sdt is None:
         raise TypeError("state must be bfloat16 or float32")
@@ -367,7 +382,8 @@ def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_
     with torch.cuda.device(dev):
         rc = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
                              _ptr(cu_seqlens), host(cu_host), N, B, T, Hqk, Hv, K,
-                             float("nan") if scale is None else float(scale), float(lower_bound), _ptr(state), sdt,
+                             float("nan") if scale is None else float(scale), float(lower_bound),
+                             int(bool(use_gate_in_kernel)), int(bool(beta_is_logit)), _ptr(state), sdt,
                              _ptr(state_indices), host(idx_host), state.shape[0], _ptr(out), _ptr(checkpoints), n_ck,
                              _ptr(checkpoint_cu_starts), host(cks_host), int(checkpoint_every_n_tokens),
                              _ptr(device_status), _stream_handle(dev))

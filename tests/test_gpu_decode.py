@@ -18,6 +18,8 @@ from kda_test_utils import BF16_ATOL, BF16_REL_L2, BF16_RTOL, FP32_REL_L2, rel_l
 
 pytestmark = pytest.mark.gpu
 
+LOGITS = dict(use_gate_in_kernel=True, beta_is_logit=True)  # the training-style inputs of make_inputs
+
 
 @pytest.fixture(scope="module", autouse=True)
 def library():
@@ -50,7 +52,7 @@ def test_decode_step_matches_oracle(state_dtype):
     o_ref, s_ref = _oracle_forward(x, state.float())
     d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
     st = state.cuda()
-    o = kda.kda_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], st)
+    o = kda.kda_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], st, **LOGITS)
     torch.cuda.synchronize()
     _bf16_check("o", o.float().cpu().numpy(), o_ref)
     got = st.float().cpu().numpy()
@@ -72,7 +74,7 @@ def test_decode_steps_reproduce_forward():
     for t in range(T):
         tok = {k: d[k][:, t:t + 1].contiguous() for k in ("q", "k", "v", "g", "beta")}
         outs.append(kda.kda_decode(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"], d["A_log"],
-                                   d["dt_bias"], st))
+                                   d["dt_bias"], st, **LOGITS))
     torch.cuda.synchronize()
     _bf16_check("o", torch.cat(outs, dim=1).float().cpu().numpy(), o_ref)
     assert rel_l2(st.cpu().numpy(), s_ref) <= FP32_REL_L2
@@ -88,7 +90,7 @@ def test_decode_state_indices():
     d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
     p = pool.cuda()
     o = kda.kda_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], p,
-                       state_indices=slots.cuda())
+                       state_indices=slots.cuda(), **LOGITS)
     torch.cuda.synchronize()
     _bf16_check("o", o.float().cpu().numpy(), o_ref)
     got = p.cpu()
@@ -104,11 +106,41 @@ def test_decode_rejections():
     pool = torch.zeros((4, 1, 128, 128), device="cuda")
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], pool)
     with pytest.raises(kda.KdaError, match="share a state slot"):
-        kda.kda_decode(*args, state_indices=torch.tensor([1, 1], dtype=torch.int32, device="cuda"))
+        kda.kda_decode(*args, state_indices=torch.tensor([1, 1], dtype=torch.int32, device="cuda"), **LOGITS)
     with pytest.raises(kda.KdaError, match="out of range"):
-        kda.kda_decode(*args, state_indices=torch.tensor([0, 4], dtype=torch.int32, device="cuda"))
+        kda.kda_decode(*args, state_indices=torch.tensor([0, 4], dtype=torch.int32, device="cuda"), **LOGITS)
     small = torch.zeros((1, 1, 128, 128), device="cuda")
     with pytest.raises(kda.KdaError, match="slot per sequence"):
-        kda.kda_decode(*args[:7], small)
+        kda.kda_decode(*args[:7], small, **LOGITS)
     with pytest.raises(kda.KdaError, match="overlaps"):
-        kda.kda_decode(*args, out=d["v"])
+        kda.kda_decode(*args, out=d["v"], **LOGITS)
+    with pytest.raises(kda.KdaError, match="lower_bound"):
+        kda.kda_decode(*args, lower_bound=-3.0, **LOGITS)
+    with pytest.raises(TypeError, match="A_log"):
+        kda.kda_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, pool, **LOGITS)
+
+
+@pytest.mark.parametrize("use_gate_in_kernel,beta_is_logit", [(False, False), (False, True), (True, False)],
+                         ids=["log_g_sigmoided_beta", "log_g_beta_logit", "gate_in_kernel_sigmoided_beta"])
+def test_decode_gate_modes(use_gate_in_kernel, beta_is_logit):
+    """The recurrent_kda page's gate modes: g already the log decay (A_log and
+    dt_bias then not needed), beta already sigmoided."""
+    from linear_attention_gated_gb300 import kda
+    x = ki.make_inputs(4, 1, 2, 4, seed=36)
+    y = ki.precomputed_gate_inputs(x, seed=37)
+    if use_gate_in_kernel:
+        y["g"] = x["g"]
+    if beta_is_logit:
+        y["beta"] = x["beta"]
+    f = {k: v.double().numpy() for k, v in y.items() if isinstance(v, torch.Tensor)}
+    o_ref, s_ref = oracle.forward(f["q"], f["k"], f["v"], f["g"], f["beta"], f["A_log"], f["dt_bias"],
+                                  f["h0"], log_space_g=not use_gate_in_kernel,
+                                  presigmoid_beta=not beta_is_logit)
+    d = {k: v.cuda() for k, v in y.items() if isinstance(v, torch.Tensor)}
+    st = d["h0"].clone()
+    gate = (d["A_log"], d["dt_bias"]) if use_gate_in_kernel else (None, None)
+    o = kda.kda_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], *gate, st,
+                       use_gate_in_kernel=use_gate_in_kernel, beta_is_logit=beta_is_logit)
+    torch.cuda.synchronize()
+    _bf16_check("o", o.float().cpu().numpy(), o_ref)
+    assert rel_l2(st.cpu().numpy(), s_ref) <= FP32_REL_L2

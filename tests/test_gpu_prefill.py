@@ -20,6 +20,8 @@ from kda_test_utils import BF16_ATOL, BF16_REL_L2, BF16_RTOL, FP32_REL_L2, rel_l
 
 pytestmark = pytest.mark.gpu
 
+LOGITS = dict(use_gate_in_kernel=True, beta_is_logit=True)  # the training-style inputs of make_inputs
+
 
 @pytest.fixture(scope="module", autouse=True)
 def library():
@@ -38,11 +40,11 @@ def _bf16_check(name, x, ref):
     assert rel_l2(x, ref) <= BF16_REL_L2, (name, rel_l2(x, ref))
 
 
-def _oracle(x, h0, lengths):
+def _oracle(x, h0, lengths, **modes):
     f = {k: v.double().numpy() for k, v in x.items() if isinstance(v, torch.Tensor) and k != "cu_seqlens"}
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
     return oracle.forward(f["q"], f["k"], f["v"], f["g"], f["beta"], f["A_log"], f["dt_bias"],
-                          h0.double().numpy(), cu_seqlens=cu)
+                          h0.double().numpy(), cu_seqlens=cu, **modes)
 
 
 def _prefix_state(x, h0, lengths, n, upto):
@@ -64,7 +66,7 @@ def test_prefill_matches_oracle_and_training_forward():
     d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
     pool = d["h0"].clone()
     o = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], pool,
-                        cu_seqlens=d["cu_seqlens"])
+                        cu_seqlens=d["cu_seqlens"], **LOGITS)
     torch.cuda.synchronize()
     _bf16_check("o", o.float().cpu().numpy(), o_ref)
     assert rel_l2(pool.cpu().numpy(), s_ref) <= FP32_REL_L2
@@ -90,7 +92,7 @@ def test_prefill_bf16_pool_slots_and_checkpoints():
     ck = torch.full((int(starts[-1]), 2, 128, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     o = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], pool,
                         cu_seqlens=d["cu_seqlens"], state_indices=slots.cuda(), checkpoints=ck,
-                        checkpoint_cu_starts=starts.cuda(), checkpoint_every_n_tokens=every)
+                        checkpoint_cu_starts=starts.cuda(), checkpoint_every_n_tokens=every, **LOGITS)
     torch.cuda.synchronize()
     _bf16_check("o", o.float().cpu().numpy(), o_ref)
     got = pool.float().cpu()
@@ -113,11 +115,57 @@ def test_prefill_rejections():
     bad = torch.tensor([0, 1, 3], dtype=torch.int64, device="cuda")  # sequence 1 needs 1 row, not 2
     with pytest.raises(kda.KdaError, match="ceil"):
         kda.kda_prefill(*args, cu_seqlens=d["cu_seqlens"], checkpoints=ck, checkpoint_cu_starts=bad,
-                        checkpoint_every_n_tokens=32)
+                        checkpoint_every_n_tokens=32, **LOGITS)
     with pytest.raises(kda.KdaError, match="multiple of 16"):
         kda.kda_prefill(*args, cu_seqlens=d["cu_seqlens"], checkpoints=ck,
                         checkpoint_cu_starts=torch.tensor([0, 1, 2], dtype=torch.int64, device="cuda"),
-                        checkpoint_every_n_tokens=24)
+                        checkpoint_every_n_tokens=24, **LOGITS)
     with pytest.raises(kda.KdaError, match="share a state slot"):
         kda.kda_prefill(*args, cu_seqlens=d["cu_seqlens"],
-                        state_indices=torch.tensor([1, 1], dtype=torch.int32, device="cuda"))
+                        state_indices=torch.tensor([1, 1], dtype=torch.int32, device="cuda"), **LOGITS)
+
+
+@pytest.mark.parametrize("use_gate_in_kernel,beta_is_logit", [(False, False), (False, True), (True, False)],
+                         ids=["log_g_sigmoided_beta", "log_g_beta_logit", "gate_in_kernel_sigmoided_beta"])
+def test_prefill_gate_modes(use_gate_in_kernel, beta_is_logit):
+    """The recurrent_kda page's gate modes over packed sequences with ragged
+    tails: g already the log decay (in [-5, 0]; A_log and dt_bias not needed),
+    beta already sigmoided. The status word stays clear."""
+    from linear_attention_gated_gb300 import kda
+    lengths = [37, 16, 90]
+    x = ki.make_inputs(1, 0, 2, 4, seed=45, lengths=lengths)
+    y = ki.precomputed_gate_inputs(x, seed=46)
+    if use_gate_in_kernel:
+        y["g"] = x["g"]
+    if beta_is_logit:
+        y["beta"] = x["beta"]
+    o_ref, s_ref = _oracle(y, y["h0"], lengths, log_space_g=not use_gate_in_kernel,
+                           presigmoid_beta=not beta_is_logit)
+    d = {k: v.cuda() for k, v in y.items() if isinstance(v, torch.Tensor)}
+    pool = d["h0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gate = (d["A_log"], d["dt_bias"]) if use_gate_in_kernel else (None, None)
+    o = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], *gate, pool, cu_seqlens=d["cu_seqlens"],
+                        device_status=status, use_gate_in_kernel=use_gate_in_kernel,
+                        beta_is_logit=beta_is_logit)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _bf16_check("o", o.float().cpu().numpy(), o_ref)
+    assert rel_l2(pool.cpu().numpy(), s_ref) <= FP32_REL_L2
+
+
+def test_prefill_log_gate_out_of_range_sets_status():
+    """A log-space gate value above 0 (a decay above 1) is outside the range
+    the chunked evaluation accepts: bit 1 of the status word is set. The value
+    used (0.25) keeps every intermediate finite."""
+    from linear_attention_gated_gb300 import kda
+    lengths = [20]
+    x = ki.precomputed_gate_inputs(ki.make_inputs(1, 0, 1, 1, seed=47, lengths=lengths), seed=48)
+    x["g"][0, 7, 0, 3] = 0.25
+    d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    pool = d["h0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, pool, cu_seqlens=d["cu_seqlens"],
+                    device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
