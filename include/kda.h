@@ -181,6 +181,52 @@ kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16*
 /* State element types for kda_decode. */
 enum { KDA_STATE_BF16 = 0, KDA_STATE_FP32 = 1 };
 
+/* Device bytes of the arena kda_step_host needs for this problem: the device
+ * copies of its eleven inputs and ten outputs (each 256-byte aligned) followed
+ * by one context workspace (kda_ctx_workspace_bytes). Same shape arguments and
+ * errors as kda_ctx_workspace_bytes. */
+kda_status kda_step_arena_bytes(int64_t B, int64_t T, int64_t Hqk, int64_t Hv,
+                                const int64_t* cu_seqlens_host, int64_t num_seqs, size_t* bytes);
+
+/* One training step from and to host memory (flashinfer.kda_training forward
+ * and backward; gradient list of flashinfer.kda_backward.recurrent_kda_backward):
+ * enqueues on `stream` the host-to-device copies of q, k, v, g, beta, A_log,
+ * dt_bias, initial_state h0, cu_seqlens (packed layout only), d_o and d_hT
+ * into `arena`, then kda_fwd and kda_bwd on those copies, then the
+ * device-to-host copies of o, h_T and the eight gradients, and returns without
+ * waiting. Every tensor argument is a HOST pointer with the layout and dtype
+ * of kda_fwd / kda_bwd; cu_seqlens_host (NULL for the fixed layout) is read
+ * during the call. Host buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister): then the copies are asynchronous and run on the copy
+ * engines; pageable buffers work but their copies are staged by the host.
+ * The host buffers must stay valid and untouched until the stream reaches the
+ * end of the step. `arena`: caller-owned device memory of at least
+ * kda_step_arena_bytes(), 256-byte aligned, not used by anything else until
+ * the step completes. `ctx`: as for kda_fwd (NULL on the first call; reused
+ * afterwards with the same arena, shapes and stream; freed with
+ * kda_ctx_destroy). The kernels run on `stream`; the input copies on
+ * `h2d_stream` and the output copies on `d2h_stream` (each NULL for `stream`).
+ * The context orders them with three events of its own: the kernels wait for
+ * this step's input copies and for the previous step's output copies from
+ * the same arena, the input copies wait for the previous step's kernels on
+ * the same arena, the output copies wait for this step's kernels. A caller that
+ * alternates two arenas (two contexts) on shared copy and compute streams gets
+ * step i+1's inputs copied in while step i computes, and step i's outputs
+ * copied out while step i+1 computes. To wait for a step, synchronise
+ * `d2h_stream` (or the device).
+ * Errors: those of kda_fwd and kda_bwd; KDA_ERR_WORKSPACE_TOO_SMALL for a small
+ * arena; KDA_ERR_INVALID_ARGUMENT for a NULL pointer, a misaligned arena or a
+ * device pointer where a host buffer is expected. Nothing is allocated. */
+kda_status kda_step_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                         const kda_bf16* beta, const float* A_log, const float* dt_bias, const float* h0,
+                         const int64_t* cu_seqlens_host, int64_t num_seqs, int64_t B, int64_t T,
+                         int64_t Hqk, int64_t Hv, int64_t head_dim, float scale, float lower_bound,
+                         const kda_bf16* d_o, const float* d_hT, kda_bf16* o, float* h_T, kda_bf16* dq,
+                         kda_bf16* dk, kda_bf16* dv, kda_bf16* dg, kda_bf16* dbeta, float* dA_log,
+                         float* ddt_bias, float* dh0, void* arena, size_t arena_bytes, kda_ctx** ctx,
+                         struct CUstream_st* stream, struct CUstream_st* h2d_stream,
+                         struct CUstream_st* d2h_stream);
+
 /* Gate modes of kda_decode and kda_prefill (flashinfer.kda.recurrent_kda,
  * parameters g, beta, A_log, use_gate_in_kernel, lower_bound and
  * beta_is_logit):

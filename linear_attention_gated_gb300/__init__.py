@@ -2,12 +2,14 @@
 
 ``kda_fwd`` / ``kda_bwd`` (and the aliases ``recurrent_kda_training_forward`` /
 ``recurrent_kda_training_backward``), the inference ``kda_prefill`` and the
-single-token ``kda_decode`` call libkda.so; see include/kda.h.
+single-token ``kda_decode`` call libkda.so; ``HostStep`` runs whole training
+steps from and to host memory (``kda_step_host``); see include/kda.h.
 """
 
 from .kda import (  # noqa: F401
     EXPORTED,
     GRAD_NAMES,
+    HostStep,
     KdaContext,
     KdaError,
     kda_bwd,

@@ -185,7 +185,23 @@ struct kda_ctx {
   bool forward_done = false;
   kda::Problem prob{};
   std::vector<Range> inputs;  // borrowed forward inputs, for the backward's aliasing checks
+  cudaEvent_t step_ev[3] = {nullptr, nullptr, nullptr};  // kda_step_host stream ordering
+  ~kda_ctx() {
+    for (cudaEvent_t e : step_ev)
+      if (e) cudaEventDestroy(e);
+  }
 };
+
+cudaError_t kda::step_events(kda_ctx* c, cudaEvent_t ev[3]) {
+  for (int i = 0; i < 3; ++i) {
+    if (!c->step_ev[i]) {
+      const cudaError_t e = cudaEventCreateWithFlags(&c->step_ev[i], cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    ev[i] = c->step_ev[i];
+  }
+  return cudaSuccess;
+}
 
 extern "C" {
 

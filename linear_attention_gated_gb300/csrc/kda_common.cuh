@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+struct kda_ctx;  // the saved-forward context of the C ABI (kda_api.cu)
+
 namespace kda {
 
 constexpr int kDim = 128;      // K = V = 128 (flashinfer.kda_training, module description)
@@ -150,6 +152,11 @@ __device__ __forceinline__ float row16_sum(float x) {
 
 // Sets the message kda_last_error_message() returns on this thread (kda_api.cu).
 void set_last_error(const char* msg);
+
+// The three events kda_step_host orders its streams with, owned by the context
+// and created on first use (kda_api.cu): [0] inputs copied in, [1] forward and
+// backward done, [2] outputs copied out.
+cudaError_t step_events(::kda_ctx* c, cudaEvent_t ev[3]);
 
 // Launchers (defined in kda_fwd.cu / kda_bwd.cu).
 cudaError_t launch_forward(const Problem& P, const FwdOut& out, int64_t units, cudaStream_t s);

@@ -31,7 +31,7 @@ _STATUS = {
 EXPORTED = ("kda_ctx_workspace_bytes", "kda_fwd", "kda_bwd", "kda_ctx_status", "kda_ctx_destroy",
             "kda_status_string", "kda_last_error_message", "kda_chunk_tokens",
             "kda_checkpoint_tokens", "kda_bwd_noalloc", "kda_decode", "kda_prefill",
-            "kda_selftest_device_timeout")
+            "kda_selftest_device_timeout", "kda_step_arena_bytes", "kda_step_host")
 
 
 class KdaError(RuntimeError):
@@ -63,6 +63,10 @@ def load_library(path: str = LIB_PATH):
     lib.kda_ctx_status.argtypes = [P]
     lib.kda_ctx_status.restype = ctypes.c_int
     lib.kda_ctx_destroy.argtypes = [P]
+    lib.kda_step_arena_bytes.argtypes = [I, I, I, I, P, I, ctypes.POINTER(S)]
+    lib.kda_step_arena_bytes.restype = ctypes.c_int
+    lib.kda_step_host.argtypes = [P] * 8 + [P, I, I, I, I, I, I, F, F] + [P] * 12 + [P, S, ctypes.POINTER(P), P, P, P]
+    lib.kda_step_host.restype = ctypes.c_int
     lib.kda_ctx_destroy.restype = None
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
@@ -403,6 +407,96 @@ def selftest_device_timeout(device=None) -> int:
 
 
 recurrent_kda_training_forward = kda_fwd
+
+
+class HostStep:
+    """Training steps from and to host memory through kda_step_host: owns one
+    device arena (kda_step_arena_bytes) and the context created in it. Each call
+    enqueues the input copies on ``h2d_stream``, the forward and backward on
+    ``stream`` and the output copies on ``d2h_stream`` (each defaults to a new
+    stream of its own; pass the same streams to two HostStep objects and use
+    them in turn to overlap one step's copies with the other's kernels) and
+    returns; ``synchronize()`` waits for the output copies. Host tensors should
+    be pinned (``pin_memory()``)."""
+
+    IN_NAMES = ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state", "do", "dfinal_state")
+
+    def __init__(self, B, T, Hqk, Hv, cu_seqlens_cpu=None, device=None, stream=None, h2d_stream=None,
+                 d2h_stream=None):
+        lib = load_library()
+        self.dev = torch.device(device if device is not None else "cuda")
+        self.B, self.T, self.Hqk, self.Hv = B, T, Hqk, Hv
+        self.cu = None if cu_seqlens_cpu is None else cu_seqlens_cpu.to(torch.int64).contiguous()
+        self.N = B if self.cu is None else self.cu.numel() - 1
+        n = ctypes.c_size_t(0)
+        _check(lib.kda_step_arena_bytes(B, T, Hqk, Hv, _ptr(self.cu), self.N if self.cu is not None else 0,
+                                        ctypes.byref(n)))
+        self.arena = torch.empty(int(n.value), dtype=torch.uint8, device=self.dev)
+        self.stream = stream if stream is not None else torch.cuda.Stream(self.dev)
+        self.h2d_stream = h2d_stream if h2d_stream is not None else torch.cuda.Stream(self.dev)
+        self.d2h_stream = d2h_stream if d2h_stream is not None else torch.cuda.Stream(self.dev)
+        self.handle = ctypes.c_void_p(None)
+
+    def shapes(self):
+        B, T, Hqk, Hv, N, D = self.B, self.T, self.Hqk, self.Hv, self.N, DIM
+        bf, f32 = torch.bfloat16, torch.float32
+        ins = {"q": ((B, T, Hqk, D), bf), "k": ((B, T, Hqk, D), bf), "v": ((B, T, Hv, D), bf),
+               "g": ((B, T, Hv, D), bf), "beta": ((B, T, Hv), bf), "A_log": ((Hv,), f32),
+               "dt_bias": ((Hv, D), f32), "initial_state": ((N, Hv, D, D), f32), "do": ((B, T, Hv, D), bf),
+               "dfinal_state": ((N, Hv, D, D), f32)}
+        outs = (("o", (B, T, Hv, D), bf), ("final_state", (N, Hv, D, D), f32), ("dq", (B, T, Hqk, D), bf),
+                ("dk", (B, T, Hqk, D), bf), ("dv", (B, T, Hv, D), bf), ("dg", (B, T, Hv, D), bf),
+                ("dbeta", (B, T, Hv), bf), ("dA_log", (Hv,), f32), ("ddt_bias", (Hv, D), f32),
+                ("dinitial_state", (N, Hv, D, D), f32))
+        return ins, outs
+
+    def empty_outputs(self, pin_memory=True):
+        """Host output buffers in the order (o, final_state, dq, dk, dv, dg, dbeta,
+        dA_log, ddt_bias, dinitial_state)."""
+        _, outs = self.shapes()
+        return tuple(torch.empty(shp, dtype=dt, pin_memory=pin_memory) for _, shp, dt in outs)
+
+    def __call__(self, q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_state, out,
+                 scale=None, lower_bound=-5.0):
+        lib = load_library()
+        ins, outs = self.shapes()
+        args = dict(zip(self.IN_NAMES, (q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_state)))
+        for name, t in args.items():
+            _want(t, name, ins[name][1], ins[name][0])
+            if t.device.type != "cpu":
+                raise ValueError(f"{name} must be a host tensor")
+        if len(out) != len(outs):
+            raise ValueError("out must hold ten host tensors")
+        for t, (name, shp, dt) in zip(out, outs):
+            _want(t, name, dt, shp)
+            if t.device.type != "cpu":
+                raise ValueError(f"{name} must be a host tensor")
+        with torch.cuda.device(self.dev):
+            rc = lib.kda_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                                   _ptr(initial_state), _ptr(self.cu), self.N if self.cu is not None else 0,
+                                   self.B, self.T, self.Hqk, self.Hv, DIM,
+                                   float("nan") if scale is None else float(scale), float(lower_bound),
+                                   _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out], _ptr(self.arena),
+                                   self.arena.numel(), ctypes.byref(self.handle),
+                                   ctypes.c_void_p(self.stream.cuda_stream),
+                                   ctypes.c_void_p(self.h2d_stream.cuda_stream),
+                                   ctypes.c_void_p(self.d2h_stream.cuda_stream))
+        _check(rc)
+        return out
+
+    def synchronize(self):
+        self.d2h_stream.synchronize()
+
+    def status(self):
+        _check(load_library().kda_ctx_status(self.handle))
+
+    def __del__(self):
+        try:
+            if self.handle and self.handle.value:
+                load_library().kda_ctx_destroy(self.handle)
+                self.handle = ctypes.c_void_p(None)
+        except Exception:
+            pass
 
 
 def recurrent_kda_training_backward(context, do, dfinal_state, out=None):
