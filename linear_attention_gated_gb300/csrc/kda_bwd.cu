@@ -227,12 +227,13 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
             tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
-          // dO W^T: the A tile is read as 128 rows from dOU on; rows 0..15 are dO
-          // and the rest (other shared-memory tiles) only fill D lanes 16..127,
-          // which are never read
+          // dO W^T with M = 64: the A tile is read as 64 rows from dOU on, of which rows 0..15
+          // are dO and land in TMEM lanes 0..15 (M = 64 puts rows 16 w .. 16 w + 15 in lanes
+          // 32 w .. 32 w + 15); the other rows only fill lanes that are never read
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st)
-            tc::mma_ss(tbase + kColM1, tc::kdesc(dou, st, kDim), tc::kdesc(wt, st, kDim), i32, st > 0);
+            tc::mma_ss(tbase + kColM1, tc::kdesc(dou, st, kDim), tc::kdesc(wt, st, kDim), tc::idesc_tf32(64, 32),
+                       st > 0);
           tc::mma_commit(mb1);
         }
         if (!tc::mbar_wait(rdy2, mph)) break;

@@ -44,11 +44,11 @@ constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 256;  // two CTAs per SM share the 512 columns
 constexpr uint32_t kColS = 0;        // FP32 state S (lane = value row v, column = key k)
 constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns; the last 16 then also take + W^T B^T
-constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T : lanes 0..31, 16 columns (A and B)
+constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T (M = 64): A in lanes 0..15, B in lanes 32..47, 16 columns
 
 struct FwdSmem {
   // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128). As the A operand of the A/B
-  // product it is read as 128 rows: rows 32..127 fall on the tiles below and only fill TMEM
+  // product (M = 64) it is read as 64 rows: rows 32..63 fall on the tile below and only fill TMEM
   // lanes that are never read.
   unsigned char KQ[32 * kDim * 4];
   unsigned char KiT[kChunk * kDim * 4];    // k^ / gamma rows t, TF32 (K-major, K = 128)
@@ -267,7 +267,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
           tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, tc::kdesc(kq, st, kDim), tc::idesc_tf32(128, 32), st > 0);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ss(tbase + kColAB, tc::kdesc(kq, st, kDim), tc::kdesc(kit, st, kDim), tc::idesc_tf32(128, 16), st > 0);
+          tc::mma_ss(tbase + kColAB, tc::kdesc(kq, st, kDim), tc::kdesc(kit, st, kDim), tc::idesc_tf32(64, 16), st > 0);
         tc::mma_commit(mbar);
       }
       __syncwarp();
@@ -275,41 +275,43 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     ok = ok && tc::mbar_wait(mbar, parity);
     parity ^= 1;
     tc::fence_after();
-    if (warp == 0) {
-      // A (lanes 0..15, strictly lower) and B (lanes 16..31, lower) from tensor memory; for
-      // the backward the tape holds A row-major and B transposed (its columns are read there)
+    if (warp < 2) {
+      // A (D rows 0..15: warp 0's lanes 0..15, strictly lower) and B (D rows 16..31: warp 1's
+      // lanes 0..15, lower) from tensor memory (an M = 64 product places rows 16 w .. 16 w + 15
+      // in lanes 32 w .. 32 w + 15); for the backward the tape holds A row-major and B
+      // transposed (its columns are read there)
       float d16[16];
       tc::tmem_ld16(tl + kColAB, d16);
       float* tape = kPf ? nullptr : P.abtape + ((si.ch_base + c) * P.Hv + h) * 512;
       if (lane < kChunk) {
         const int i = lane;
+        if (warp == 0) {
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          d16[j] = j < i ? d16[j] : 0.f;
-          sm.AsT[j][i] = d16[j];
-        }
-        if constexpr (!kPf) {
+          for (int j = 0; j < kChunk; ++j) {
+            d16[j] = j < i ? d16[j] : 0.f;
+            sm.AsT[j][i] = d16[j];
+          }
+          if constexpr (!kPf) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<float4*>(tape + i * 16 + 4 * q4) =
-                make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
-        }
-      } else {
-        const int i = lane - kChunk;
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<float4*>(tape + i * 16 + 4 * q4) =
+                  make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
+          }
+        } else {
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          d16[j] = j <= i ? d16[j] : 0.f;
-          if constexpr (!kPf) tape[256 + j * 16 + i] = d16[j];
-        }
+          for (int j = 0; j < kChunk; ++j) {
+            d16[j] = j <= i ? d16[j] : 0.f;
+            if constexpr (!kPf) tape[256 + j * 16 + i] = d16[j];
+          }
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          *reinterpret_cast<float4*>(sm.Bt + tc::kmaj(i, 4 * q4, kChunk)) =
-              make_float4(tc::round_tf32(d16[4 * q4]), tc::round_tf32(d16[4 * q4 + 1]), tc::round_tf32(d16[4 * q4 + 2]),
-                          tc::round_tf32(d16[4 * q4 + 3]));
+          for (int q4 = 0; q4 < 4; ++q4) {
+            *reinterpret_cast<float4*>(sm.Bt + tc::kmaj(i, 4 * q4, kChunk)) =
+                make_float4(tc::round_tf32(d16[4 * q4]), tc::round_tf32(d16[4 * q4 + 1]), tc::round_tf32(d16[4 * q4 + 2]),
+                            tc::round_tf32(d16[4 * q4 + 3]));
+          }
         }
       }
     }
-    if (__syncthreads_or(!ok)) { aborted = true; break; }
     // ---- state checkpoint and decay S <- S0 diag(gamma_C) in tensor memory
     {
       const bool ck = !kPf && (c % ck_every) == 0;
@@ -347,6 +349,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         tc::tmem_st16(tl + kColS + col, x);
       }
     }
+    if (__syncthreads_or(!ok)) { aborted = true; break; }  // A and B in shared memory
     // ---- W by forward substitution: both warps of a state row solve for W; each then
     // writes the u tape of half of the tokens and one TF32 part of W (the output's B W term
     // is added by the tensor core with the state update)
