@@ -338,8 +338,9 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
             "config": {"workload": args.workload, "sequences": N, "tokens": Ttot, "Hqk": w.hqk, "Hv": w.hv,
                        "head_dim": DIM, "token_heads_per_gpu": token_heads, "io_dtype": "bf16",
-                       "state_dtype": "fp32", "l2": "inputs larger than L2 (each token tensor "
-                       f"{d['q'].numel() * 2 / 1e6:.0f} MB > 129 MB), no flush",
+                       "state_dtype": "fp32", "l2": f"a forward moves {ab['fwd'] / 1e6:.0f} MB and a backward "
+                       f"{ab['bwd'] / 1e6:.0f} MB, each > 129 MB of L2 (largest token tensor "
+                       f"{d['v'].numel() * 2 / 1e6:.0f} MB), no flush",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
             "e2e": e2e}
@@ -407,7 +408,7 @@ def bench_decode(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=12):
+def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=32):
     """Inputs in pinned host memory; each step goes through the C-ABI call
     kda_step_host, which copies that step's inputs in, runs the forward and the
     backward and copies o, the final state and every gradient out. Two arenas
