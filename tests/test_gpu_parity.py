@@ -59,6 +59,21 @@ def test_parity_small(name, cfg):
     _log(name, compare(gpu, ref))
 
 
+def test_extreme_gates_and_betas():
+    """Half of the key dimensions near the strongest decay the gate allows (g = 4: a in [-5, -4.9]
+    for every token, so one 16-token sub-chunk spans a factor of about e^-80, near the end of
+    FP32's normal range), the other half near none (g = -4: a in [-0.09, 0]), and beta logits of
+    -12 or +12: the chunked form's decay factors and their inverses reach their extremes and must
+    still match the oracle."""
+    x = ki.make_inputs(1, 0, 2, 2, seed=106, lengths=[70, 33])
+    dims = torch.arange(ki.DIM)
+    x["g"] = torch.where(dims % 2 == 0, 4.0, -4.0).expand_as(x["g"]).to(torch.bfloat16).contiguous()
+    tok = torch.arange(x["beta"].shape[1]).view(1, -1, 1)
+    x["beta"] = torch.where(tok % 3 == 0, -12.0, 12.0).expand_as(x["beta"]).to(torch.bfloat16).contiguous()
+    gpu, _ = run_gpu(x)
+    _log("extreme_gates_and_betas", compare(gpu, run_oracle(x)))
+
+
 # full-size workloads: sampled query/key heads (None = all)
 WORKLOADS = [
     ("fixed_b1_t64_h2", None),
