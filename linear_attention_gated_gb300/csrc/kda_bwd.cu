@@ -60,6 +60,8 @@ namespace {
 constexpr int kThreads = 256;             // compute threads
 constexpr int kBlock = kThreads + 32;      // plus the MMA-issuing warp
 constexpr int kTileF = kChunk * kLds;
+constexpr int kDopLd = kDim + 8;          // padded row (BF16 elements) of the staged dO tile: a token
+                                          // per lane then falls on different banks
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // G, FP32 accumulator (lanes v, columns k)
 constexpr uint32_t kColGT = 128;  // G^T, the same adjoint transposed (lanes k, columns v)
@@ -93,7 +95,7 @@ struct BwdSmem {
   __nv_bfloat16 Sq[kChunk * kDim];        // q, k, g, do of the sub-chunk (cp.async staging)
   __nv_bfloat16 Sk[kChunk * kDim];
   __nv_bfloat16 Sg[kChunk * kDim];
-  __nv_bfloat16 dOp[kChunk * kDim];
+  __nv_bfloat16 dOp[kChunk * kDopLd];
   float As[kChunk][kChunk];               // A and B^T of the sub-chunk, from the forward (cp.async
   float BsT[kChunk][kChunk];              // staging); As and BsT must stay contiguous
   float M1[kChunk][kChunk];               // dO W^T (W = diag(beta) U)
@@ -176,7 +178,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     const int ntc = rows_of(cc);
     const bool okr = srow < ntc;
     const int64_t t = si.t0 + cc * kChunk + srow;
-    tc::cp_async16(sm.dOp + srow * kDim + scol, okr ? a.d_o + (t * P.Hv + h) * kDim + scol : a.d_o, okr ? 16u : 0u);
+    tc::cp_async16(sm.dOp + srow * kDopLd + scol, okr ? a.d_o + (t * P.Hv + h) * kDim + scol : a.d_o, okr ? 16u : 0u);
     const float* us = okr ? P.utape + (t * P.Hv + h) * kDim + scol : P.utape;
     tc::cp_async16(sm.Up + srow * kLds + scol, us, okr ? 16u : 0u);
     tc::cp_async16(sm.Up + srow * kLds + scol + 4, okr ? us + 4 : us, okr ? 16u : 0u);
@@ -426,10 +428,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           const float w = bt * ua[e];
           whi[e] = tc::round_tf32(w);
           wlo[e] = tc::round_tf32(w - whi[e]);
-          dof[e] = __bfloat162float(sm.dOp[ot * kDim + k0 + e]);
-          *reinterpret_cast<float*>(sm.dOUv + tc::kmaj(k0 + e, ot, 32)) = dof[e];
-          *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, ot, 32)) = tc::round_tf32(s * qt[e]);
-          *reinterpret_cast<float*>(sm.QKT + tc::kmaj(k0 + e, 16 + ot, 32)) = tc::round_tf32(-kt[e]);
+          dof[e] = __bfloat162float(sm.dOp[ot * kDopLd + k0 + e]);
         }
         *reinterpret_cast<float4*>(sm.Ktp + ot * kLds + k0) = make_float4(kt[0], kt[1], kt[2], kt[3]);
         *reinterpret_cast<float4*>(sm.Qtp + ot * kLds + k0) = make_float4(qt[0], qt[1], qt[2], qt[3]);
@@ -439,6 +438,15 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         *reinterpret_cast<float4*>(sm.Wt[0] + tc::kmaj(ot, k0, kDim)) = make_float4(whi[0], whi[1], whi[2], whi[3]);
         *reinterpret_cast<float4*>(sm.Wt[1] + tc::kmaj(ot, k0, kDim)) = make_float4(wlo[0], wlo[1], wlo[2], wlo[3]);
         *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(ot, k0, kDim)) = make_float4(dof[0], dof[1], dof[2], dof[3]);
+      }
+      {  // dO as rows v (K = token) for dO^T B and the adjoint updates: value dim v, 8 tokens, so that
+         // each float4 store covers 4 tokens and a warp's stores cover whole 8 x 4 core matrices
+        const int v = tid & (kDim - 1), t0 = 8 * (tid >> 7);
+        float d8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d8[j] = __bfloat162float(sm.dOp[(t0 + j) * kDopLd + v]);
+        *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(v, t0, 32)) = make_float4(d8[0], d8[1], d8[2], d8[3]);
+        *reinterpret_cast<float4*>(sm.dOUv + tc::kmaj(v, t0 + 4, 32)) = make_float4(d8[4], d8[5], d8[6], d8[7]);
       }
       {  // scale B^T as rows t, K = j (B[j][t] is BsT[t][j]), split into TF32 hi + lo
         const int t = tid >> 4, j = tid & 15;
@@ -455,6 +463,20 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       // chain needs it), then S0^T dO^T, Gd^T W^T and dO W^T
       if (tid == 0) tc::mbar_arrive(rdy1);  // operands of the first MMA group are in place
       if (warp >= 4) {
+        {  // QKT, rows k: columns 0..15 scale q^g, 16..31 -k^g (the adjoint updates of the second group)
+          const int k = tid - 128;
+#pragma unroll
+          for (int t4 = 0; t4 < kChunk; t4 += 4) {
+            float qv[4], kv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              qv[j] = tc::round_tf32(s * sm.Qtp[(t4 + j) * kLds + k]);
+              kv[j] = tc::round_tf32(-sm.Ktp[(t4 + j) * kLds + k]);
+            }
+            *reinterpret_cast<float4*>(sm.QKT + tc::kmaj(k, t4, 32)) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+            *reinterpret_cast<float4*>(sm.QKT + tc::kmaj(k, 16 + t4, 32)) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+          }
+        }
         // dO W^T = dO (W_hi + W_lo)^T from tensor memory (dO is exact in TF32)
         ok = ok && tc::mbar_wait(mb1, ph);
         tc::fence_after();
@@ -674,19 +696,27 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         const float* da = cmb + 2 * kTileF;
         const bool valid = ti < nt;
         const int64_t t = tc0 + ti;
-        float dg8[8], dq8[8], dk8[8];
+        float dg8[8], dq8[8], dk8[8], da8[8];
         float pq = 0.f, pk = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int o = ti * kLds + c8 + 4 * hh;
+          const float4 x = *reinterpret_cast<const float4*>(da + o);
+          const float4 y = *reinterpret_cast<const float4*>(dQh + o);
+          const float4 z = *reinterpret_cast<const float4*>(dKh + o);
+          da8[4 * hh] = x.x; da8[4 * hh + 1] = x.y; da8[4 * hh + 2] = x.z; da8[4 * hh + 3] = x.w;
+          dq8[4 * hh] = y.x; dq8[4 * hh + 1] = y.y; dq8[4 * hh + 2] = y.z; dq8[4 * hh + 3] = y.w;
+          dk8[4 * hh] = z.x; dk8[4 * hh + 1] = z.y; dk8[4 * hh + 2] = z.z; dk8[4 * hh + 3] = z.w;
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           // sigmoid'(z) = sigmoid(z) sigmoid(-z) = e / (1 + e)^2 with e = exp(-|z|) (no cancellation)
           const float ex = __expf(-fabsf(zz[e]));
           const float den = __fdividef(1.0f, 1.0f + ex);
-          const float dz = valid ? da[ti * kLds + c8 + e] * P.lb * ex * den * den : 0.f;
+          const float dz = valid ? da8[e] * P.lb * ex * den * den : 0.f;
           dg8[e] = dz * ea;
           ddt_acc[e] += dg8[e];
           dA_acc += dz * zz[e];
-          dq8[e] = dQh[ti * kLds + c8 + e];
-          dk8[e] = dKh[ti * kLds + c8 + e];
           pq += qhat[e] * dq8[e];
           pk += khat[e] * dk8[e];
         }

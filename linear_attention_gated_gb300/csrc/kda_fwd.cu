@@ -230,9 +230,8 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         const float4 qh4 = *reinterpret_cast<const float4*>(sm.Pq + t * kLds + k0);
         const float4 kh4 = *reinterpret_cast<const float4*>(sm.Pk + t * kLds + k0);
         const float4 g4 = *reinterpret_cast<const float4*>(sm.Pa + t * kLds + k0);
-        const float4 c4 = *reinterpret_cast<const float4*>(sm.gC + k0);
         const float qa[4] = {qh4.x, qh4.y, qh4.z, qh4.w}, ka[4] = {kh4.x, kh4.y, kh4.z, kh4.w};
-        const float ga[4] = {g4.x, g4.y, g4.z, g4.w}, ca[4] = {c4.x, c4.y, c4.z, c4.w};
+        const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
         float kt[4], qt[4], ki[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -240,10 +239,6 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
           kt[e] = ka[e] * ga[e];
           qt[e] = qa[e] * ga[e];
           ki[e] = ka[e] * inv;
-          const float kb = ka[e] * (ca[e] * inv);
-          const float kb_hi = tc::round_tf32(kb);
-          *reinterpret_cast<float*>(sm.KbT[0] + tc::kmaj(k0 + e, t, kChunk)) = kb_hi;
-          *reinterpret_cast<float*>(sm.KbT[1] + tc::kmaj(k0 + e, t, kChunk)) = tc::round_tf32(kb - kb_hi);
         }
         *reinterpret_cast<float4*>(sm.KQ + tc::kmaj(t, k0, kDim)) =
             make_float4(tc::round_tf32(kt[0]), tc::round_tf32(kt[1]), tc::round_tf32(kt[2]), tc::round_tf32(kt[3]));
@@ -251,6 +246,24 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             make_float4(tc::round_tf32(qt[0]), tc::round_tf32(qt[1]), tc::round_tf32(qt[2]), tc::round_tf32(qt[3]));
         *reinterpret_cast<float4*>(sm.KiT + tc::kmaj(t, k0, kDim)) =
             make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
+      }
+    }
+    {  // (k^ gamma_C / gamma)^T as rows k (K = token) in TF32 hi + lo: key k, 8 tokens, so that each
+       // float4 store covers 4 tokens and a warp's stores cover whole 8 x 4 core matrices
+      const int k = tid & (kDim - 1), t0 = 8 * (tid >> 7);
+      const float gck = sm.gC[k];
+#pragma unroll
+      for (int t4 = 0; t4 < 8; t4 += 4) {
+        float hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int t = t0 + t4 + j;
+          const float kb = sm.Pk[t * kLds + k] * (gck * __fdividef(1.0f, sm.Pa[t * kLds + k]));
+          hi[j] = tc::round_tf32(kb);
+          lo[j] = tc::round_tf32(kb - hi[j]);
+        }
+        *reinterpret_cast<float4*>(sm.KbT[0] + tc::kmaj(k, t0 + t4, kChunk)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<float4*>(sm.KbT[1] + tc::kmaj(k, t0 + t4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
     tc::fence_async_smem();
