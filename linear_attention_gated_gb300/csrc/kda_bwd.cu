@@ -109,7 +109,7 @@ struct BwdSmem {
   float rho0[2][kDim];                    // halves of sum_v Gd * S0
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
   float dbp[4][kChunk];                   // per-warp partial dbeta
-  unsigned long long mbar[5];
+  unsigned long long mbar[6];
   uint32_t tmem_base;
 };
 
@@ -143,7 +143,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 5; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), 1);
+    for (int i = 0; i < 6; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), 1);
   }
   tc::fence_before();
   __syncthreads();
@@ -153,6 +153,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   const uint32_t mbD = tc::smem_u32(&sm.mbar[0]), mb1 = tc::smem_u32(&sm.mbar[1]);
   const uint32_t mb2 = tc::smem_u32(&sm.mbar[2]);
   const uint32_t rdy1 = tc::smem_u32(&sm.mbar[3]), rdy2 = tc::smem_u32(&sm.mbar[4]);  // compute -> MMA warp
+  const uint32_t mbS = tc::smem_u32(&sm.mbar[5]);  // a sub-chunk's checkpoint has landed in S0s
   uint32_t ph = 0;  // every barrier completes once per sub-chunk
   bool ok = true;
   bool aborted = false;
@@ -186,14 +187,13 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::cp_async16(&sm.As[0][0] + tid * 4, P.abtape + ((si.ch_base + cc) * P.Hv + h) * 512 + tid * 4, 16u);
     tc::cp_async_commit();
   };
-  auto prefetch_state = [&](int64_t cc) {
+  // The checkpoint (64 KiB, contiguous) is staged by the copy engine: four bulk copies issued by
+  // one thread, counted in transaction bytes on mbS.
+  auto stage_state = [&](int64_t cc) {
     const float* src = P.ckpt + ((si.ck_base + cc / ck_every) * P.Hv + h) * kDim * kDim;
+    tc::mbar_arrive_expect_tx(mbS, (uint32_t)(kDim * kDim * 4));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int f = tid + kThreads * i;
-      tc::cp_async16(sm.S0s + f * 16, src + f * 4, 16u);
-    }
-    tc::cp_async_commit();
+    for (int i = 0; i < 4; ++i) tc::bulk_g2s(tc::smem_u32(sm.S0s + i * 16384), src + i * 4096, 16384u, mbS);
   };
 
   if (warp == kThreads / 32) {
@@ -286,7 +286,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     }
     prefetch_qkg(nchunks - 1);
     prefetch_late(nchunks - 1);
-    prefetch_state(nchunks - 1);
+    if (tid == 0) stage_state(nchunks - 1);
+    int64_t staged = 1;  // checkpoint bulk copies issued; each completes one phase of mbS
 
     const int ti = tid >> 4;
     const int c8 = (tid & 15) * 8;
@@ -342,7 +343,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           }
         }
     };
-    tc::cp_async_wait<2>();  // q, k, g of the first sub-chunk (dO/u/A/B and the state may be in flight)
+    tc::cp_async_wait<1>();  // q, k, g of the first sub-chunk (dO/u/A/B may be in flight)
     csync();
     prologue(nchunks - 1);
     for (int64_t c = nchunks - 1; c >= 0; --c) {
@@ -365,8 +366,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         for (int i = 0; i < kChunk; ++i) sm.Pa[i * kLds + tid] = av[i];
         sm.gC[tid] = av[kChunk - 1];
       }
-      if (c > 0) tc::cp_async_wait<1>();  // dO, u, A/B and the state of this sub-chunk (the next q, k, g may be in flight)
+      if (c > 0) tc::cp_async_wait<1>();  // dO, u and A/B of this sub-chunk (the next q, k, g may be in flight)
       else tc::cp_async_wait_all();
+      ok = ok && tc::mbar_wait(mbS, ph);  // and its checkpoint
       csync();
       // ---- P2: decay of the adjoint, G <- G diag(gamma_C) (lanes v) and G^T <- diag(gamma_C) G^T
       // (lanes k), with sum_v Gd * S0 from the FP32 checkpoint, the low part of Gd^T for the
@@ -584,22 +586,17 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       csync();
       // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T
       if (tid == 0) tc::mbar_arrive(rdy2);  // operands of the second MMA group are in place
-      if (warp >= 4) {  // dV W^T in FP32
-        const int t2 = tid - 128;
-#pragma unroll
-        for (int rep = 0; rep < 2; ++rep) {
-          const int pidx = t2 + 128 * rep, i = pidx >> 4, j = pidx & 15;
-          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tid < kChunk) sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
+      {  // dV W^T in FP32, one entry (i, j) per thread
+        const int i = tid >> 4, j = tid & 15;
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-          for (int vv = 0; vv < kDim; vv += 4)
-            fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
-                 *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
-          const float acc = hsum4(a4);
-          sm.M2[i][j] = acc * sm.bs[j];
-          sm.M2T[j][i] = acc * sm.bs[j];
-        }
-      } else if (tid < kChunk) {
-        sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
+        for (int vv = 0; vv < kDim; vv += 4)
+          fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
+               *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
+        const float acc = hsum4(a4);
+        sm.M2[i][j] = acc * sm.bs[j];
+        sm.M2T[j][i] = acc * sm.bs[j];
       }
       ok = ok && tc::mbar_wait(mb1, ph);
       ok = ok && tc::mbar_wait(mb2, ph);
@@ -607,7 +604,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       if (csync_or(!ok)) { aborted = true; break; }
       if (c > 0) {  // dO, u, A/B and S0 of this sub-chunk are no longer read
         prefetch_late(c - 1);
-        prefetch_state(c - 1);
+        if (tid == 0) stage_state(c - 1);
+        ++staged;
       }
       // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows i0 .. i0 + 7 with
       // i0 = 8 hv a compile-time constant, so the triangular masks drop whole terms)
@@ -687,7 +685,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           tv[i * kLds + tid] = run;
         }
       }
-      if (c > 0) tc::cp_async_wait<2>();  // q, k, g of the next sub-chunk, for its prologue below
+      if (c > 0) tc::cp_async_wait<1>();  // q, k, g of the next sub-chunk, for its prologue below
       csync();
       // ---- P9: epilogue: gate / sigmoid / L2-norm backward and stores
       {
@@ -752,6 +750,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::fence_before();
     }
     tc::cp_async_wait_all();
+    // no bulk copy may still be landing when the block exits (normally every one has been waited for)
+    if (tid == 0) tc::mbar_wait(mbS, (uint32_t)((staged - 1) & 1));
     csync();
     if (!aborted) {
       // dinitial_state = G (from its transposed copy, for coalesced stores)

@@ -86,8 +86,21 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
   asm volatile("fence.mbarrier_init.release.cluster;");
 }
 
-// Bounded wait for the given phase parity (about two seconds of SM clock);
-// false if it gave up.
+// Arrive on an mbarrier and raise its expected transaction count by `bytes`:
+// the phase completes once the arrivals are in and that many bytes have landed.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+
+// Copy engine bulk copy, global -> shared, of `bytes` bytes (a multiple of 16;
+// both addresses 16-byte aligned); completion is counted on the mbarrier in
+// transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
 // Plain arrive (release at CTA scope) on an mbarrier.
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
