@@ -285,7 +285,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       }
       __syncwarp();
     }
-    ok = ok && tc::mbar_wait(mbar, parity);
+    if (ok) ok = tc::mbar_wait_warp(mbar, parity);
     parity ^= 1;
     tc::fence_after();
     if (warp < 2) {
@@ -440,7 +440,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     }
     // ---- meanwhile, the next sub-chunk's prologue (it touches no tensor-core operand)
     if (c + 1 < nchunks) prologue(c + 1);
-    ok = ok && tc::mbar_wait(mbar, parity);
+    if (ok) ok = tc::mbar_wait_warp(mbar, parity);
     parity ^= 1;
     tc::fence_after();
     {  // the output of this warp's half of the tokens: o = scale (S0 (q^ gamma)^T + W^T B^T)

@@ -123,6 +123,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long l
   }
 }
 
+// The same wait for a whole (converged) warp: lane 0 polls and the result is
+// shared, so the other 31 lanes put no traffic on the mbarrier while it spins.
+// Lane 0's acquire is passed on to the warp by the shuffle's warp barrier.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t mbar, uint32_t parity, long long limit = 1ll << 32) {
+  uint32_t ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(mbar, parity, limit) ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 // Make generic-proxy shared-memory writes visible to the tensor core.
