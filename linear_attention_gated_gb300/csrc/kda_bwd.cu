@@ -110,6 +110,7 @@ struct BwdSmem {
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
   float dbp[4][kChunk];                   // per-warp partial dbeta
   unsigned long long mbar[6];
+  const float* ck_next[2];                // checkpoint of sub-chunk c - 1, for the MMA warp (slot (c - 1) & 1)
   uint32_t tmem_base;
 };
 
@@ -260,6 +261,16 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
             tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
           tc::mma_commit(mb2);
         }
+        // once this group has completed, S0s is free: stage the next (earlier) sub-chunk's
+        // checkpoint, whose address the compute warps left in shared memory
+        if (c > 0) {
+          if (!tc::mbar_wait(mb2, mph)) break;
+          const float* src;
+          asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(src) : "r"(tc::smem_u32(&sm.ck_next[(c - 1) & 1])));
+          tc::mbar_arrive_expect_tx(mbS, (uint32_t)(kDim * kDim * 4));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tc::bulk_g2s(tc::smem_u32(sm.S0s + i * 16384), src + i * 4096, 16384u, mbS);
+        }
         mph ^= 1;
       }
     }
@@ -351,7 +362,12 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       const int nt = rows_of(c);
       csync();  // the prologue of this sub-chunk is in place
       // ---- P1: cumulative decay (one key column per thread); the next q, k, g are fetched meanwhile
-      if (c > 0) prefetch_qkg(c - 1);
+      if (c > 0) {
+        prefetch_qkg(c - 1);
+        // two slots: the MMA warp reads this one after the group-2 completion of sub-chunk c, and it
+        // is written again two sub-chunks later, after that warp has issued sub-chunk c - 1's work
+        if (tid == 0) sm.ck_next[(c - 1) & 1] = P.ckpt + ((si.ck_base + (c - 1) / ck_every) * P.Hv + h) * kDim * kDim;
+      }
       if (tid < kDim) {
         float av[kChunk];
 #pragma unroll
@@ -604,8 +620,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       if (csync_or(!ok)) { aborted = true; break; }
       if (c > 0) {  // dO, u, A/B and S0 of this sub-chunk are no longer read
         prefetch_late(c - 1);
-        if (tid == 0) stage_state(c - 1);
-        ++staged;
+        ++staged;  // the MMA warp stages the checkpoint of c - 1
       }
       // ---- P7: assemble d q^, d k^ and the gauge term (lane k, rows i0 .. i0 + 7 with
       // i0 = 8 hv a compile-time constant, so the triangular masks drop whole terms)
