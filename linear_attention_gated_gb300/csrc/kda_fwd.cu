@@ -19,9 +19,11 @@
 // Tensor cores (tcgen05.mma kind::tf32, FP32 accumulators in TMEM) compute the
 // two state-sized contractions S0 [k^ gamma; q^ gamma]^T (128x32, the state as
 // the tensor-memory A operand) and W^T (k^ gamma_C/gamma) (128x128, added into
-// the state); the 16x16 A and B run in FP32 on CUDA cores while the first
-// contraction is in flight, and the next sub-chunk's prologue while the second
-// one is. Token tiles are prefetched into registers one sub-chunk ahead.
+// the state, W^T written by the solving threads into tensor memory as its A
+// operand), as well as the 16x16 A and B (an M = 64 product next to the first
+// contraction) and the output's B W term (next to the second); the next
+// sub-chunk's prologue runs while the second group is in flight. Token tiles
+// are prefetched into registers one sub-chunk ahead.
 // Operands written to shared memory are rounded to TF32; the state read as the
 // A operand is truncated to TF32 by the tensor core (it only feeds the sub-chunk's
 // Y and O); the state update uses split TF32 (x = hi + lo, three products) so
@@ -45,6 +47,7 @@ constexpr uint32_t kTmemCols = 256;  // two CTAs per SM share the 512 columns
 constexpr uint32_t kColS = 0;        // FP32 state S (lane = value row v, column = key k)
 constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns; the last 16 then also take + W^T B^T
 constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T (M = 64): A in lanes 0..15, B in lanes 32..47, 16 columns
+constexpr uint32_t kColW = 176;      // W^T (lane = value row v, column = token): TF32 hi in 16 columns, lo in the next 16
 
 struct FwdSmem {
   // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128). As the A operand of the A/B
@@ -54,7 +57,6 @@ struct FwdSmem {
   unsigned char KiT[kChunk * kDim * 4];    // k^ / gamma rows t, TF32 (K-major, K = 128)
   unsigned char Bt[kChunk * kChunk * 4];   // B rows t, TF32 (K-major, K = 16): O += W^T B^T
   unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo (K = 16)
-  unsigned char Wa[2][kDim * kChunk * 4];  // W^T, rows v, TF32 hi / lo                     (K = 16)
   float Pq[kTileF];                        // q^
   float Pk[kTileF];                        // k^
   float Pa[kTileF];                        // log decay, then gamma
@@ -390,6 +392,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       // this warp's half of the tokens (compile-time): u tape and one TF32 part of W
       auto emit = [&](auto chc) {
         constexpr int c_h = decltype(chc)::value;
+        float xw[kChunk];
 #pragma unroll
         for (int tt = 0; tt < 8; ++tt) {
           const int t = 8 * c_h + tt;
@@ -403,8 +406,9 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             const float hi = tc::round_tf32(w[4 * t4 + e]);
             x[e] = c_h == 0 ? hi : tc::round_tf32(w[4 * t4 + e] - hi);
           }
-          *reinterpret_cast<float4*>(sm.Wa[c_h] + tc::kmaj(sv, 4 * t4, kChunk)) = make_float4(x[0], x[1], x[2], x[3]);
+          xw[4 * t4] = x[0]; xw[4 * t4 + 1] = x[1]; xw[4 * t4 + 2] = x[2]; xw[4 * t4 + 3] = x[3];
         }
+        tc::tmem_st16(tl + kColW + 16 * c_h, xw);  // the tensor-memory A operand of the update
       };
       if (ch == 0) emit(std::integral_constant<int, 0>{});
       else emit(std::integral_constant<int, 1>{});
@@ -418,21 +422,20 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
-        const uint32_t wa[2] = {tc::smem_u32(sm.Wa[0]), tc::smem_u32(sm.Wa[1])};
         const uint32_t kb[2] = {tc::smem_u32(sm.KbT[0]), tc::smem_u32(sm.KbT[1])};
         const uint32_t bt = tc::smem_u32(sm.Bt);
-        const int pa[3] = {0, 1, 0}, pb[3] = {0, 0, 1};
+        const int pa[3] = {0, 16, 0}, pb[3] = {0, 0, 1};
 #pragma unroll
         for (int p = 0; p < 3; ++p)
 #pragma unroll
           for (int st = 0; st < kChunk / 8; ++st)
-            tc::mma_ss(tbase + kColS, tc::kdesc(wa[pa[p]], st, kChunk), tc::kdesc(kb[pb[p]], st, kChunk),
+            tc::mma_ts(tbase + kColS, tbase + kColW + pa[p] + 8 * st, tc::kdesc(kb[pb[p]], st, kChunk),
                        tc::idesc_tf32(128, 128), 1);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
 #pragma unroll
           for (int st = 0; st < kChunk / 8; ++st)
-            tc::mma_ss(tbase + kColYO + 16, tc::kdesc(wa[p], st, kChunk), tc::kdesc(bt, st, kChunk),
+            tc::mma_ts(tbase + kColYO + 16, tbase + kColW + 16 * p + 8 * st, tc::kdesc(bt, st, kChunk),
                        tc::idesc_tf32(128, 16), 1);
         tc::mma_commit(mbar);
       }
