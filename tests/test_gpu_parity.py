@@ -74,6 +74,25 @@ def test_extreme_gates_and_betas():
     _log("extreme_gates_and_betas", compare(gpu, run_oracle(x)))
 
 
+def _random_case(seed):
+    """A seeded random small problem: layout, sequence count and lengths (ragged, 1..159 tokens),
+    query/key heads and GQA ratio."""
+    rng = np.random.default_rng(seed)
+    hqk = int(rng.integers(1, 4))
+    hv = hqk * int(rng.choice([1, 2, 4]))
+    if rng.random() < 0.5:
+        lengths = [int(t) for t in rng.integers(1, 160, int(rng.integers(1, 5)))]
+        return dict(B=1, T=0, hqk=hqk, hv=hv, seed=seed, lengths=lengths)
+    return dict(B=int(rng.integers(1, 4)), T=int(rng.integers(1, 120)), hqk=hqk, hv=hv, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(300, 316))
+def test_parity_random_shapes(seed):
+    x = ki.make_inputs(**_random_case(seed))
+    gpu, _ = run_gpu(x)
+    _log(f"random_{seed}", compare(gpu, run_oracle(x)))
+
+
 # full-size workloads: sampled query/key heads (None = all)
 WORKLOADS = [
     ("fixed_b1_t64_h2", None),
