@@ -41,8 +41,12 @@
 // Gd^T's truncated-away low part, so it is split TF32 on both sides. dO W^T
 // (dO exact in TF32, W split) also runs on the tensor core. The
 // forward's FP32 A and B of each sub-chunk are reused. The next sub-chunk's
-// token tiles, u, A/B and state checkpoint are prefetched with cp.async into
-// buffers freed earlier in the current sub-chunk. The 16x16 intra-chunk
+// token tiles, u and A/B are prefetched with cp.async into buffers freed
+// earlier in the current sub-chunk; its state checkpoint (64 KiB, contiguous)
+// arrives by four bulk copies that the MMA warp issues once the second group
+// has finished reading S0. Operand tiles whose K dimension is the token are
+// stored key-major (one float4 per 4 tokens of a row), so that a warp's
+// stores fill whole core matrices without bank conflicts. The 16x16 intra-chunk
 // products, the substitutions and the combination run in FP32 on CUDA cores:
 // the decay gradient is a difference of nearly equal terms and needs them at
 // full single precision. The gate, sigmoid and L2-norm backward are applied in
