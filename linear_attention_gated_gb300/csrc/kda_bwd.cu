@@ -764,7 +764,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           a.dbeta[(tc0 + tid) * P.Hv + h] = __float2bfloat16_rn(sm.dba[tid] * sm.bs[tid] * bn);
         }
       }
-      if (c > 0) prologue(c - 1);
+      prologue(c - 1);  // also after the last sub-chunk (harmless, unused): no branch between it and the epilogue
       ph ^= 1;
       tc::fence_before();
     }
