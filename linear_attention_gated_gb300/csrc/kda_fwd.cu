@@ -442,7 +442,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       __syncwarp();
     }
     // ---- meanwhile, the next sub-chunk's prologue (it touches no tensor-core operand)
-    if (c + 1 < nchunks) prologue(c + 1);
+    prologue(c + 1);  // also past the last sub-chunk (all rows invalid, unused): no branch before the output
     if (ok) ok = tc::mbar_wait_warp(mbar, parity);
     parity ^= 1;
     tc::fence_after();
