@@ -207,62 +207,66 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
     // so no compute warp is held by the tensor pipe's queue.
     if (tc::elect_one()) {
       uint32_t mph = 0;
+      // Base descriptors of the operand tiles; K-step st of a tile adds 16 * st (256 bytes) to the
+      // address field, and step st of the S0^T tile 256 * st. They are made opaque once per
+      // sub-chunk, so that ptxas forms each step's descriptor with one add next to its MMA
+      // instead of hoisting every (tile, step) descriptor out of the loop into registers.
+      const uint64_t kKi = tc::kdesc(tc::smem_u32(sm.Ki), 0, kDim), kS0 = tc::sdesc(tc::smem_u32(sm.S0s), 2048u, 128u);
+      const uint64_t kDou = tc::kdesc(tc::smem_u32(sm.dOU), 0, kDim), kDv = tc::kdesc(tc::smem_u32(sm.dOU) + 2 * 4096, 0, kDim);
+      const uint64_t kWt = tc::kdesc(tc::smem_u32(sm.Wt[0]), 0, kDim), kDouv = tc::kdesc(tc::smem_u32(sm.dOUv), 0, 32);
+      const uint64_t kBs0 = tc::kdesc(tc::smem_u32(sm.Bsc[0]), 0, kChunk), kBs1 = tc::kdesc(tc::smem_u32(sm.Bsc[1]), 0, kChunk);
+      const uint64_t kQkt = tc::kdesc(tc::smem_u32(sm.QKT), 0, 32), kDul = tc::kdesc(tc::smem_u32(sm.dUlo), 0, kChunk);
       for (int64_t c = nchunks - 1; c >= 0; --c) {
         if (!tc::mbar_wait(rdy1, mph)) break;
         tc::fence_after();
+        uint64_t dKi = kKi, dS0 = kS0, dDou = kDou, dDv = kDv, dWt = kWt, dDouv = kDouv, dBs0 = kBs0, dBs1 = kBs1,
+                 dQkt = kQkt, dDul = kDul;
+        asm volatile("" : "+l"(dKi), "+l"(dS0), "+l"(dDou), "+l"(dDv), "+l"(dWt));
+        asm volatile("" : "+l"(dDouv), "+l"(dBs0), "+l"(dBs1), "+l"(dQkt), "+l"(dDul));
         {
-          const uint32_t ki = tc::smem_u32(sm.Ki), s0 = tc::smem_u32(sm.S0s);
-          const uint32_t dou = tc::smem_u32(sm.dOU), wt = tc::smem_u32(sm.Wt[0]);
-          const uint32_t douv = tc::smem_u32(sm.dOUv);
-          const uint32_t bsc[2] = {tc::smem_u32(sm.Bsc[0]), tc::smem_u32(sm.Bsc[1])};
           const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st)
-            tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, tc::kdesc(ki, st, kDim), i16, st > 0);
+            tc::mma_ts(tbase + kColDW, tbase + kColG + 8 * st, dKi + 16u * st, i16, st > 0);
 #pragma unroll
-          for (int p = 0; p < 2; ++p)  // dO (rows v, exact in TF32) with scale B^T hi and lo
+          for (int st = 0; st < 2; ++st)  // dO (rows v, exact in TF32) with scale B^T hi and lo
+            tc::mma_ss(tbase + kColDW, dDouv + 16u * st, dBs0 + 16u * st, i16, 1);
 #pragma unroll
-            for (int st = 0; st < 2; ++st)
-              tc::mma_ss(tbase + kColDW, tc::kdesc(douv, st, 32), tc::kdesc(bsc[p], st, kChunk), i16, 1);
+          for (int st = 0; st < 2; ++st)
+            tc::mma_ss(tbase + kColDW, dDouv + 16u * st, dBs1 + 16u * st, i16, 1);
           tc::mma_commit(mbD);
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st) {
-            tc::mma_ss(tbase + kColQ, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
-                       st > 0);
-            tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, tc::kdesc(wt, st, kDim), i32, st > 0);
+            tc::mma_ss(tbase + kColQ, dS0 + 256u * st, dDou + 16u * st, i16, st > 0);
+            tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, dWt + 16u * st, i32, st > 0);
           }
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
-            tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, tc::kdesc(wt, st, kDim), i32, 1);
+            tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, dWt + 16u * st, i32, 1);
           // dO W^T with M = 64: the A tile is read as 64 rows from dOU on, of which rows 0..15
           // are dO and land in TMEM lanes 0..15 (M = 64 puts rows 16 w .. 16 w + 15 in lanes
           // 32 w .. 32 w + 15); the other rows only fill lanes that are never read
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st)
-            tc::mma_ss(tbase + kColM1, tc::kdesc(dou, st, kDim), tc::kdesc(wt, st, kDim), tc::idesc_tf32(64, 32),
-                       st > 0);
+            tc::mma_ss(tbase + kColM1, dDou + 16u * st, dWt + 16u * st, tc::idesc_tf32(64, 32), st > 0);
           tc::mma_commit(mb1);
         }
         if (!tc::mbar_wait(rdy2, mph)) break;
         tc::fence_after();
         {
-          const uint32_t dou = tc::smem_u32(sm.dOU) + 2 * 4096;  // rows 16..31 (dV)
-          const uint32_t qkt = tc::smem_u32(sm.QKT), douv = tc::smem_u32(sm.dOUv), dul = tc::smem_u32(sm.dUlo);
-          const uint32_t s0 = tc::smem_u32(sm.S0s);
           const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
 #pragma unroll
-          for (int st = 0; st < kDim / 8; ++st)
-            tc::mma_ss(tbase + kColR, tc::sdesc(s0 + (uint32_t)st * 4096u, 2048u, 128u), tc::kdesc(dou, st, kDim), i16,
-                       st > 0);
+          for (int st = 0; st < kDim / 8; ++st)  // S0^T dV^T (dV: rows 16..31 of dOU)
+            tc::mma_ss(tbase + kColR, dS0 + 256u * st, dDv + 16u * st, i16, st > 0);
 #pragma unroll
           for (int st = 0; st < 4; ++st) {
-            tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, st, 32), tc::kdesc(douv, st, 32), i128, 1);
-            tc::mma_ss(tbase + kColG, tc::kdesc(douv, st, 32), tc::kdesc(qkt, st, 32), i128, 1);
+            tc::mma_ss(tbase + kColGT, dQkt + 16u * st, dDouv + 16u * st, i128, 1);
+            tc::mma_ss(tbase + kColG, dDouv + 16u * st, dQkt + 16u * st, i128, 1);
           }
 #pragma unroll
           for (int st = 0; st < 2; ++st)  // -k^g (columns 16..31 of QKT) with the dV lo part, for G^T only:
             // G (lanes v) is only ever read truncated to TF32, as the A operand of Gd (k^/g)^T
-            tc::mma_ss(tbase + kColGT, tc::kdesc(qkt, 2 + st, 32), tc::kdesc(dul, st, kChunk), i128, 1);
+            tc::mma_ss(tbase + kColGT, dQkt + 16u * (2 + st), dDul + 16u * st, i128, 1);
           tc::mma_commit(mb2);
         }
         // once this group has completed, S0s is free: stage the next (earlier) sub-chunk's
