@@ -276,13 +276,14 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
-        const uint32_t kq = tc::smem_u32(sm.KQ), kit = tc::smem_u32(sm.KiT);
+        // K-step st of a tile adds 16 * st to its descriptor's address field
+        const uint64_t dkq = tc::kdesc(tc::smem_u32(sm.KQ), 0, kDim), dkit = tc::kdesc(tc::smem_u32(sm.KiT), 0, kDim);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, tc::kdesc(kq, st, kDim), tc::idesc_tf32(128, 32), st > 0);
+          tc::mma_ts(tbase + kColYO, tbase + kColS + 8 * st, dkq + 16u * st, tc::idesc_tf32(128, 32), st > 0);
 #pragma unroll
         for (int st = 0; st < kDim / 8; ++st)
-          tc::mma_ss(tbase + kColAB, tc::kdesc(kq, st, kDim), tc::kdesc(kit, st, kDim), tc::idesc_tf32(64, 16), st > 0);
+          tc::mma_ss(tbase + kColAB, dkq + 16u * st, dkit + 16u * st, tc::idesc_tf32(64, 16), st > 0);
         tc::mma_commit(mbar);
       }
       __syncwarp();
@@ -422,21 +423,23 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     if (warp == 0) {
       if (tc::elect_one()) {
         tc::fence_after();
-        const uint32_t kb[2] = {tc::smem_u32(sm.KbT[0]), tc::smem_u32(sm.KbT[1])};
-        const uint32_t bt = tc::smem_u32(sm.Bt);
-        const int pa[3] = {0, 16, 0}, pb[3] = {0, 0, 1};
+        // base descriptors made opaque here, so each K-step's descriptor is one add next to its MMA
+        // rather than a register held across the sub-chunk loop
+        uint64_t dkb0 = tc::kdesc(tc::smem_u32(sm.KbT[0]), 0, kChunk), dkb1 = tc::kdesc(tc::smem_u32(sm.KbT[1]), 0, kChunk);
+        uint64_t dbt = tc::kdesc(tc::smem_u32(sm.Bt), 0, kChunk);
+        asm volatile("" : "+l"(dkb0), "+l"(dkb1), "+l"(dbt));
+        const int pa[3] = {0, 16, 0};
+        const uint64_t pb[3] = {dkb0, dkb0, dkb1};
 #pragma unroll
         for (int p = 0; p < 3; ++p)
 #pragma unroll
           for (int st = 0; st < kChunk / 8; ++st)
-            tc::mma_ts(tbase + kColS, tbase + kColW + pa[p] + 8 * st, tc::kdesc(kb[pb[p]], st, kChunk),
-                       tc::idesc_tf32(128, 128), 1);
+            tc::mma_ts(tbase + kColS, tbase + kColW + pa[p] + 8 * st, pb[p] + 16u * st, tc::idesc_tf32(128, 128), 1);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
 #pragma unroll
           for (int st = 0; st < kChunk / 8; ++st)
-            tc::mma_ts(tbase + kColYO + 16, tbase + kColW + 16 * p + 8 * st, tc::kdesc(bt, st, kChunk),
-                       tc::idesc_tf32(128, 16), 1);
+            tc::mma_ts(tbase + kColYO + 16, tbase + kColW + 16 * p + 8 * st, dbt + 16u * st, tc::idesc_tf32(128, 16), 1);
         tc::mma_commit(mbar);
       }
       __syncwarp();
