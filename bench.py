@@ -237,10 +237,17 @@ def main():
     ap.add_argument("--decode", type=int, default=0, metavar="N",
                     help="instead of the training step, time decode steps (T = 1) of N sequences x 96 heads")
     ap.add_argument("--decode-state", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--prefill", action="store_true",
+                    help="instead of the training step, time inference prefill of the workload from a state pool")
+    ap.add_argument("--prefill-checkpoint", type=int, default=0, metavar="N",
+                    help="prefill: BF16 state checkpoints every N tokens (a multiple of 16; 0 = none)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.decode:
         bench_decode(args)
+        return
+    if args.prefill:
+        bench_prefill(args)
         return
 
     world, rank, local = dist_setup()
@@ -403,6 +410,82 @@ def bench_decode(args):
                        "l2": f"state pool {N * H * DIM * DIM * esz / 1e6:.0f} MB > 129 MB, no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "kda_decode_kernel",
+                         "peak_src": peaks["src"], "algorithmic_bytes_per_launch": bytes_step},
+            "gpu_launches": args.steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
+def bench_prefill(args):
+    """Inference prefill of the named workload from a state pool (slot n per
+    sequence, FP32 or BF16 per --decode-state, updated in place), optionally
+    with BF16 state checkpoints; prints one JSON line with HBM roofline."""
+    import itertools
+
+    import torch
+
+    import kda_inputs as ki
+    from linear_attention_gated_gb300 import build as cuda_build
+    from linear_attention_gated_gb300 import kda_prefill, load_library
+
+    cuda_build.build()
+    load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = ki.WORKLOADS[args.workload]
+    x = ki.workload_inputs(args.workload)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cu_cpu = x["cu_seqlens"]
+    B, T = x["q"].shape[:2]
+    N = cu_cpu.numel() - 1 if cu_cpu is not None else B
+    lens = (cu_cpu[1:] - cu_cpu[:-1]).tolist() if cu_cpu is not None else [T] * B
+    Ttot = sum(lens)
+    sdt = torch.bfloat16 if args.decode_state == "bf16" else torch.float32
+    state = d["h0"].to(sdt).contiguous()
+    ck = ck_starts = ck_cpu = None
+    n_ck = 0
+    if args.prefill_checkpoint:
+        per = [(L + args.prefill_checkpoint - 1) // args.prefill_checkpoint for L in lens]
+        ck_cpu = torch.tensor([0] + list(itertools.accumulate(per)), dtype=torch.int64)
+        n_ck = int(ck_cpu[-1])
+        ck = torch.empty((n_ck, w.hv, DIM, DIM), dtype=torch.bfloat16, device=dev)
+        ck_starts = ck_cpu.to(dev)
+    o = torch.empty_like(d["v"])
+    stream = torch.cuda.current_stream(dev)
+    def step():
+        kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"], state,
+                    cu_seqlens=d["cu_seqlens"], checkpoints=ck, checkpoint_cu_starts=ck_starts,
+                    checkpoint_every_n_tokens=args.prefill_checkpoint, out=o, use_gate_in_kernel=True,
+                    beta_is_logit=True, cu_seqlens_cpu=cu_cpu, checkpoint_cu_starts_cpu=ck_cpu)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    sec = t0.elapsed_time(t1) / 1e3 / args.steps
+    esz = 2 if sdt == torch.bfloat16 else 4
+    # q, k read per query/key head; v, g, beta read and o written per value head; every unit's state
+    # read and written once; each checkpoint written once
+    bytes_step = (Ttot * (512 * w.hqk + (256 * 3 + 2) * w.hv) + N * w.hv * 2 * esz * DIM * DIM
+                  + n_ck * w.hv * 2 * DIM * DIM)
+    peaks = read_peaks()
+    achieved = bytes_step / sec / 1e9
+    line = {"metric": "KDA prefill token·heads/s (1 GB300)", "value": Ttot * w.hv / sec, "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec,
+            "higher_is_better": True, "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": f"prefill_{args.workload}", "sequences": N, "tokens": Ttot, "Hqk": w.hqk,
+                       "Hv": w.hv, "head_dim": DIM, "state_dtype": args.decode_state,
+                       "checkpoint_every_n_tokens": args.prefill_checkpoint,
+                       "l2": f"a prefill moves {bytes_step / 1e6:.0f} MB > 129 MB of L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "kda_fwd_kernel (prefill)",
                          "peak_src": peaks["src"], "algorithmic_bytes_per_launch": bytes_step},
             "gpu_launches": args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)

@@ -347,7 +347,8 @@ def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scal
 
 def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_indices=None, checkpoints=None,
                 checkpoint_cu_starts=None, checkpoint_every_n_tokens=0, scale=None, lower_bound=-5.0, out=None,
-                device_status=None, use_gate_in_kernel=False, beta_is_logit=False):
+                device_status=None, use_gate_in_kernel=False, beta_is_logit=False, *, cu_seqlens_cpu=None,
+                state_indices_cpu=None, checkpoint_cu_starts_cpu=None):
     """Inference prefill from a state pool: returns o; the final state of every
     sequence is written back to its slot of ``state`` (BF16 or FP32, [num_slots,
     Hv, 128, 128]); optional BF16 ``checkpoints`` [C, Hv, 128, 128] every
@@ -356,7 +357,9 @@ def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_
     for kda_decode; with the gate precomputed (use_gate_in_kernel False) every
     g must lie in [-5, 0], else bit 1 of ``device_status`` (int32 device
     tensor) is set. Argument marshalling only: one launch of the library's
-    forward kernel."""
+    forward kernel. The ``*_cpu`` keywords pass trusted CPU mirrors of the
+    device index tensors; without them the mirrors are copied from the device
+    (a synchronising copy)."""
     lib = load_library()
     B, T, Hqk, K = q.shape
     Hv = v.shape[2]
@@ -372,10 +375,20 @@ def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_
     if out is None:
         out = torch.empty_like(v)
     _want(out, "out", torch.bfloat16, v.shape)
-    cu_host = cu_seqlens.cpu() if cu_seqlens is not None else None
+    def mirror(t, given, name):
+        if t is None:
+            if given is not None:
+                raise ValueError(f"{name}_cpu given without {name}")
+            return None
+        if given is None:
+            return t.cpu()
+        if given.device.type != "cpu" or given.shape != t.shape or given.dtype != t.dtype:
+            raise ValueError(f"{name}_cpu must be a CPU tensor of the shape and dtype of {name}")
+        return given
+    cu_host = mirror(cu_seqlens, cu_seqlens_cpu, "cu_seqlens")
     N = (cu_host.numel() - 1) if cu_host is not None else B
-    idx_host = state_indices.cpu() if state_indices is not None else None
-    cks_host = checkpoint_cu_starts.cpu() if checkpoint_cu_starts is not None else None
+    idx_host = mirror(state_indices, state_indices_cpu, "state_indices")
+    cks_host = mirror(checkpoint_cu_starts, checkpoint_cu_starts_cpu, "checkpoint_cu_starts")
     n_ck = 0
     if checkpoints is not None:
         _want(checkpoints, "checkpoints", torch.bfloat16)
