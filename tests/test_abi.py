@@ -74,6 +74,9 @@ def test_workspace_bytes_grows_with_problem(lib):
 
 @pytest.mark.parametrize("args,status", [
     ((0, 64, 2, 2, None), 1),           # B = 0
+    ((1, 0, 2, 2, None), 1),            # T = 0 (no tokens)
+    ((1, 64, 2, 2, [0]), 1),            # packed with no sequences
+    ((1, 64, 0, 2, None), 1),           # no query/key heads
     ((1, 64, 3, 4, None), 1),           # Hv not a multiple of Hqk
     ((2, 64, 2, 2, [0, 32, 64]), 1),    # packed with B != 1
     ((1, 64, 2, 2, [0, 32, 32, 64]), 1),  # empty sequence

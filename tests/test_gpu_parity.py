@@ -74,6 +74,16 @@ def test_extreme_gates_and_betas():
     _log("extreme_gates_and_betas", compare(gpu, run_oracle(x)))
 
 
+def test_long_sequence():
+    """One 32763-token sequence and a 21-token one, GQA 1:2: 2048 sub-chunks of FP32 state and
+    adjoint accumulation in one unit. The decay gradient's per-sub-chunk anchor, the parameter
+    gradients summed over the whole sequence and the initial-state gradient carried back through
+    it must still meet the bars."""
+    x = ki.make_inputs(1, 0, 1, 2, seed=107, lengths=[32763, 21])
+    gpu, _ = run_gpu(x)
+    _log("long_sequence", compare(gpu, run_oracle(x)))
+
+
 def _random_case(seed):
     """A seeded random small problem: layout, sequence count and lengths (ragged, 1..159 tokens),
     query/key heads and GQA ratio."""
