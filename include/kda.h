@@ -127,7 +127,9 @@ kda_status kda_bwd(kda_ctx* ctx, const kda_bf16* d_o, const float* d_hT, kda_bf1
 
 /* Synchronises the context's stream and reports the first device-side error
  * (KDA_ERR_DEVICE_TIMEOUT if a bounded wait gave up, KDA_ERR_CUDA on a CUDA
- * error), else KDA_OK. */
+ * error), else KDA_OK. The timeout word lives in the workspace and is cleared
+ * only when a context is created: once set, it stays set for this context and
+ * the outputs of every call made with it since are not to be trusted. */
 kda_status kda_ctx_status(kda_ctx* ctx);
 
 /* Frees the host-side context. The workspace stays owned by the caller. Safe on NULL. */
