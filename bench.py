@@ -491,13 +491,16 @@ def bench_prefill(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=32):
+def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=64):
     """Inputs in pinned host memory; each step goes through the C-ABI call
     kda_step_host, which copies that step's inputs in, runs the forward and the
     backward and copies o, the final state and every gradient out. Two arenas
     take the steps in turn on shared copy-in, compute and copy-out streams, so
     step i+1's inputs and step i-1's outputs travel while step i computes; the
-    timed region covers every step's copies and kernels."""
+    timed region covers every step's copies and kernels, including the pipeline's
+    fill (the first copy-in and the first kernels, before any copy-out) and its
+    drain, about 10 ms in all on the packed 8 x 1024-token, 96-head workload, i.e.
+    0.15 ms of each of the 64 steps."""
     import torch
     from linear_attention_gated_gb300 import HostStep
     names_in = ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "h0", "do", "dfinal_state"]
@@ -532,7 +535,8 @@ def measure_e2e(x, d, dev, stream, kda_fwd, kda_bwd, token_heads, world, steps=3
         r.status()
     return {"value": job_value(token_heads, world, el / steps), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "api": "kda_step_host",
-            "overlap": "two arenas taken in turn; copy-in, compute and copy-out streams"}
+            "overlap": "two arenas taken in turn; copy-in, compute and copy-out streams; "
+                       "the pipeline's fill and drain inside the timed region"}
 
 
 if __name__ == "__main__":
