@@ -191,7 +191,7 @@ def cpu_baseline(x, w, target_s=12.0):
         dt, cores = oracle_sample_run(x, list(range(nh)), r)
     th = nh * token_heads_per_qk
     return {"value": th / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{WORKLOAD}: query/key heads 0..{nh - 1} of {w.hqk} (all sequences), "
+            "sample": f"{w.name}: query/key heads 0..{nh - 1} of {w.hqk} (all sequences), "
                       f"{th} token·heads, FP64 forward + backward, {dt:.1f} s"}
 
 
@@ -199,11 +199,11 @@ def run_reference(args, world, rank):
     import kda_inputs as ki
     if rank != 0:
         return
-    w = ki.WORKLOADS[WORKLOAD]
-    x = ki.workload_inputs(WORKLOAD)
+    w = ki.WORKLOADS[args.workload]
+    x = ki.workload_inputs(args.workload)
     r = w.hv // w.hqk
-    heads = list(range(2))
-    th = len(heads) * x["q"].shape[1] * r
+    heads = list(range(min(2, w.hqk)))
+    th = len(heads) * x["q"].shape[0] * x["q"].shape[1] * r
     for _ in range(args.warmup):
         oracle_sample_run(x, heads, r)
     times = []
@@ -213,12 +213,12 @@ def run_reference(args, world, rank):
         times.append(dt)
     total = sum(times)
     value = th * args.steps / total
-    sample = (f"{WORKLOAD}: query/key heads {heads} of {w.hqk} (all sequences) per step, "
+    sample = (f"{w.name}: query/key heads {heads} of {w.hqk} (all sequences) per step, "
               f"{th} token·heads, FP64 forward + backward")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "data": "synthetic", "config": {"workload": w.name, "sample": sample},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -268,9 +268,10 @@ def main():
     w = ki.WORKLOADS[args.workload]
     x = ki.workload_inputs(args.workload)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
-    cu_cpu = x["cu_seqlens"]
-    N = cu_cpu.numel() - 1
-    Ttot = int(cu_cpu[-1])
+    cu_cpu = x["cu_seqlens"]  # None for the fixed [B, T] layout
+    B, T = x["q"].shape[:2]
+    N = cu_cpu.numel() - 1 if cu_cpu is not None else B
+    Ttot = B * T
     units = N * w.hv
     token_heads = Ttot * w.hv
     stream = torch.cuda.current_stream(dev)
