@@ -68,14 +68,14 @@ def kernel_source_sha(name):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
-    """DRAM bytes per launch from a committed ncu summary, or None if absent or
-    taken on a different version of the kernel's source."""
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, or None if absent, taken
+    on a different version of the kernel's source, or scaled to another workload."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path)).get(kernel)
-    if not d or d.get("source_sha") != kernel_source_sha(d.get("source", "")):
+    if not d or d.get("source_sha") != kernel_source_sha(d.get("source", "")) or d.get("workload") != workload:
         return None
     return d.get("bytes_per_launch")
 
@@ -330,7 +330,7 @@ def main():
     dom_bytes = ab["bwd"] if dom == "kda_bwd_kernel" else ab["fwd"]
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, args.workload),
                 "kernel": dom, "peak_src": peaks["src"],
                 "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
                 "step_frac": (ab["fwd"] + ab["bwd"]) / (elapsed / args.steps) / 1e9 / peaks["hbm_gbs"],
