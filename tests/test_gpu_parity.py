@@ -168,6 +168,31 @@ def test_context_reuse_matches_fresh_context():
         assert torch.equal(reused[name], fresh[name]), name
 
 
+def test_two_contexts_on_two_streams_at_once():
+    """Two problems enqueued on two streams before either is waited for (their kernels may
+    share the GPU) give bit for bit what each gives alone: a context shares no device state
+    with another."""
+    from linear_attention_gated_gb300 import kda_bwd, kda_fwd
+    xs = [to_device(ki.make_inputs(1, 0, 2, 4, seed=16, lengths=[300, 47, 129])),
+          to_device(ki.make_inputs(3, 200, 1, 2, seed=17))]
+    alone = [run_gpu(ki.make_inputs(1, 0, 2, 4, seed=16, lengths=[300, 47, 129]))[0],
+             run_gpu(ki.make_inputs(3, 200, 1, 2, seed=17))[0]]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    results = []
+    for x, s in zip(xs, streams):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            o, hT, ctx = kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["A_log"], x["dt_bias"], x["h0"],
+                                 cu_seqlens=x.get("cu_seqlens"), cu_seqlens_cpu=x.get("cu_seqlens_cpu"))
+            grads = kda_bwd(ctx, x["do"], x["dfinal_state"])
+        results.append((o, hT) + tuple(grads))
+    torch.cuda.synchronize()
+    for want, got in zip(alone, results):
+        for name, t in zip(["o", "final_state", "dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias",
+                            "dinitial_state"], got):
+            assert torch.equal(t.cpu(), want[name]), name
+
+
 def test_every_output_element_written():
     """Outputs pre-filled with NaN come back finite (no unwritten region)."""
     from linear_attention_gated_gb300 import kda_bwd, kda_fwd
