@@ -98,6 +98,10 @@ kda_status kda_ctx_workspace_bytes(int64_t B, int64_t T, int64_t Hqk, int64_t Hv
  *   requires identical shapes, device, stream and workspace, and overwrites its
  *   saved checkpoints. The inputs are borrowed by the context: they must stay
  *   allocated and unmodified until kda_bwd has been enqueued.
+ * CUDA graphs: creating a context copies the launch plan from host memory, so
+ *   create it outside any capture; a call that reuses it (and kda_bwd) only
+ *   launches kernels on `stream` and may be captured into a CUDA graph. A replay
+ *   reads whatever the captured input buffers hold at that time.
  */
 kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
                    const kda_bf16* beta, const float* A_log, const float* dt_bias,
