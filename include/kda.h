@@ -264,7 +264,13 @@ kda_status kda_step_host(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v
  *                   KDA_STATE_FP32 per state_dtype; read and written in place
  *   state_indices   device int32 [N] and its trusted host mirror
  *                   state_indices_host (both NULL, or both set); every index in
- *                   [0, num_slots) and no slot used twice
+ *                   [0, num_slots) and no slot used twice. The call checks the
+ *                   mirror; the kernel reads the device copy and checks its
+ *                   range again: a device index outside [0, num_slots) (one
+ *                   that no longer matches the mirror, as in a replayed CUDA
+ *                   graph whose indices were rewritten) leaves the pool alone
+ *                   and sets that sequence's o to NaN. Distinct slots on the
+ *                   device stay the caller's duty there.
  *   o               BF16 [N, 1, Hv, 128], overwritten
  * Hv must be a multiple of Hqk (value head h reads query/key head h / (Hv/Hqk));
  * head_dim 128; scale NaN or 1/sqrt(128); lower_bound -5. Device pointers are
@@ -301,7 +307,10 @@ kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, c
  *   state            [num_slots, Hv, 128, 128] value-first, state_dtype
  *                    KDA_STATE_BF16 or KDA_STATE_FP32, read and written in place
  *   state_indices    device int32 [N] and its host mirror (both NULL, or both
- *                    set); in range, no slot used twice
+ *                    set); in range, no slot used twice. The kernel checks the
+ *                    range of the device copy again: an index outside
+ *                    [0, num_slots) sets bit 2 (value 4) of device_status and
+ *                    leaves that sequence's slot alone (its o unspecified).
  *   o                BF16 [B, T, Hv, 128]
  *   checkpoints      optional BF16 [num_checkpoints, Hv, 128, 128] value-first:
  *                    for each sequence, rows checkpoint_cu_starts[n] + j hold
@@ -313,7 +322,7 @@ kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, c
  *                    with checkpoints NULL).
  *   device_status    optional device int32: bit 0 (value 1) is set if a
  *                    bounded device wait gave up (then o and the pool are
- *                    incomplete), bit 1 (value 2) as said above; bits are only
+ *                    incomplete), bits 1 and 2 (values 2, 4) as said above; bits are only
  *                    ever set, never cleared. NULL uses a word inside the library.
  * Units run in index order. Validation errors return before any launch;
  * otherwise the work is enqueued on `stream`. Nothing is allocated. */

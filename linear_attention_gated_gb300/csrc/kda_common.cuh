@@ -59,6 +59,7 @@ struct PrefillArgs {
   const int64_t* cu;           // device cu_seqlens [N + 1], or null for B sequences of T tokens
   int64_t T;                   // tokens per sequence in the fixed layout
   const int32_t* slots;        // pool slot per sequence, or null (slot n)
+  int64_t num_slots;           // slots in the pool
   void* pool;                  // [num_slots, Hv, 128, 128] value-first, BF16 or FP32, in place
   int pool_bf16;               // 1: BF16 pool, 0: FP32 pool
   __nv_bfloat16* ck;           // [C, Hv, 128, 128] BF16 value-first, or null

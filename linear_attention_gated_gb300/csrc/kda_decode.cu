@@ -43,6 +43,7 @@ struct DecodeArgs {
   const float* dt_bias;       // [Hv, 128]
   void* state;                // [num_slots, Hv, 128, 128], BF16 or FP32
   const int32_t* idx;         // [N] slot per sequence, or null (slot n)
+  int64_t num_slots;          // slots in the pool
   __nv_bfloat16* o;           // [N, Hv, 128]
   int64_t Hqk, Hv, r;
   float scale, lb;
@@ -96,6 +97,17 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks<StateT>) kda_decode
   const int64_t n = unit / a.Hv, h = unit % a.Hv, qh = h / a.r;
   const int64_t slot = a.idx ? a.idx[n] : n;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (slot < 0 || slot >= a.num_slots) {
+    // a device index outside the pool (it no longer matches the host mirror the call was checked
+    // against, e.g. in a replayed graph): the state is not touched and this row of o reads NaN
+    if (tid < kDim / 8) {
+      float nan8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) nan8[e] = __int_as_float(0x7fc00000);
+      store_bf16x8(a.o + (n * a.Hv + h) * kDim + 8 * tid, nan8);
+    }
+    return;
+  }
   const int hl = lane & 15, half = lane >> 4;  // keys 8 hl .. 8 hl + 7 of row 2 warp + half (+16 per pass)
   StateT* S = reinterpret_cast<StateT*>(a.state) + ((slot * a.Hv + h) * kDim) * kDim;
   extern __shared__ __align__(16) unsigned char st_smem[];
@@ -260,6 +272,7 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
   a.dt_bias = dt_bias;
   a.state = state;
   a.idx = state_indices;
+  a.num_slots = num_slots;
   a.o = reinterpret_cast<__nv_bfloat16*>(o);
   a.Hqk = Hqk;
   a.Hv = Hv;

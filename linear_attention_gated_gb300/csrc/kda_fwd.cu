@@ -91,6 +91,14 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     si = P.seq[n];
   }
   const int64_t slot = kPf ? (pf.slots ? pf.slots[n] : n) : 0;
+  if constexpr (kPf) {
+    if (slot < 0 || slot >= pf.num_slots) {
+      // a device index outside the pool (it no longer matches the host mirror the call was
+      // checked against, e.g. in a replayed graph): flagged, and the pool is not touched
+      if (threadIdx.x == 0) atomicOr(P.status, 4);
+      return;
+    }
+  }
 
   const int sv = 32 * (warp & 3) + lane;  // state row (TMEM lane) of this thread
   const int ch = warp >> 2;               // column half [64 ch, 64 ch + 64)

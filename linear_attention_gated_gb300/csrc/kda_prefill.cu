@@ -166,6 +166,7 @@ extern "C" kda_status kda_prefill(const kda_bf16* q, const kda_bf16* k, const kd
   pf.cu = cu_seqlens;
   pf.T = T;
   pf.slots = state_indices;
+  pf.num_slots = num_slots;
   pf.pool = state;
   pf.pool_bf16 = state_dtype == KDA_STATE_BF16 ? 1 : 0;
   pf.ck = reinterpret_cast<__nv_bfloat16*>(checkpoints);

@@ -296,17 +296,20 @@ def _want_gate_params(A_log, dt_bias, Hv, K, use_gate_in_kernel):
 
 
 def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scale=None, lower_bound=-5.0,
-               out=None, use_gate_in_kernel=False, beta_is_logit=False):
+               out=None, use_gate_in_kernel=False, beta_is_logit=False, *, state_indices_cpu=None):
     """One decode step (T = 1): updates ``state`` in place and returns o.
 
     q, k [N, 1, Hqk, 128] and v, g [N, 1, Hv, 128] BF16, beta [N, 1, Hv] BF16,
     A_log [Hv] and dt_bias [Hv, 128] FP32 (None allowed unless
     use_gate_in_kernel); state [num_slots, Hv, 128, 128] BF16 or FP32
     (value-first), read and written at slot state_indices[n] (int32 [N], on the
-    device; slot n when None). Gate modes and their defaults as on the
-    recurrent_kda page: g is the log decay unless ``use_gate_in_kernel``, beta
-    is already sigmoided unless ``beta_is_logit``. Argument marshalling only:
-    the step is one launch of the library's decode kernel."""
+    device; slot n when None). ``state_indices_cpu``, a trusted CPU copy of
+    state_indices, is what the library validates; without it the indices are
+    copied to the host, which waits for the device. Gate modes and their
+    defaults as on the recurrent_kda page: g is the log decay unless
+    ``use_gate_in_kernel``, beta is already sigmoided unless ``beta_is_logit``.
+    Argument marshalling only: the step is one launch of the library's decode
+    kernel."""
     lib = load_library()
     N, T, Hqk, K = q.shape
     Hv = v.shape[2]
@@ -332,7 +335,15 @@ def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scal
         if state_indices.dtype != torch.int32 or state_indices.shape != (N,):
             raise ValueError("state_indices must be int32 [N]")
         idx_dev = state_indices.contiguous()
-        idx_host = idx_dev.cpu()
+        if state_indices_cpu is None:
+            idx_host = idx_dev.cpu()
+        else:
+            if (state_indices_cpu.dtype != torch.int32 or state_indices_cpu.shape != (N,)
+                    or state_indices_cpu.device.type != "cpu"):
+                raise ValueError("state_indices_cpu must be a CPU int32 [N] tensor")
+            idx_host = state_indices_cpu.contiguous()
+    elif state_indices_cpu is not None:
+        raise ValueError("state_indices_cpu given without state_indices")
     dev = q.device
     with torch.cuda.device(dev):
         rc = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),

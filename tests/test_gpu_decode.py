@@ -144,3 +144,44 @@ def test_decode_gate_modes(use_gate_in_kernel, beta_is_logit):
     torch.cuda.synchronize()
     _bf16_check("o", o.float().cpu().numpy(), o_ref)
     assert rel_l2(st.cpu().numpy(), s_ref) <= FP32_REL_L2
+
+
+def test_decode_graph_replay_with_rewritten_indices():
+    """A decode step with device slot indices, captured into a CUDA graph (the host mirror is
+    checked once, when the call is captured): a replay reads the device indices as they are
+    then. Rewritten to other distinct slots, it updates those slots exactly as an eager call
+    does; an index rewritten outside the pool leaves the pool alone and gives NaN for that
+    sequence, while the others are unaffected."""
+    from linear_attention_gated_gb300 import kda
+    x = ki.make_inputs(3, 1, 2, 2, seed=36)
+    pool0 = (0.05 * torch.randn((6, 2, 128, 128), generator=torch.Generator().manual_seed(37))).cuda()
+    d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    toks = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"])
+    idx_cpu = torch.tensor([0, 1, 2], dtype=torch.int32)
+    idx = idx_cpu.cuda()
+    pool = pool0.clone()
+    out = torch.empty_like(d["v"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        kda.kda_decode(*toks, pool, state_indices=idx, state_indices_cpu=idx_cpu, out=out, **LOGITS)
+
+    new = torch.tensor([4, 2, 5], dtype=torch.int32)
+    pool.copy_(pool0)
+    idx.copy_(new.cuda())
+    graph.replay()
+    ref_pool = pool0.clone()
+    ref_o = kda.kda_decode(*toks, ref_pool, state_indices=new.cuda(), state_indices_cpu=new, **LOGITS)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_o) and torch.equal(pool, ref_pool)
+
+    pool.copy_(pool0)
+    idx.copy_(torch.tensor([4, 6, 5], dtype=torch.int32).cuda())  # 6 is outside the 6-slot pool
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.isnan(out[1].float()).all()
+    assert torch.equal(out[0], ref_o[0]) and torch.equal(out[2], ref_o[2])
+    want = pool0.clone()
+    want[4], want[5] = ref_pool[4], ref_pool[5]
+    assert torch.equal(pool, want)

@@ -169,3 +169,31 @@ def test_prefill_log_gate_out_of_range_sets_status():
                     device_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 2
+
+
+def test_prefill_device_index_outside_pool_sets_status():
+    """The kernel checks the device slot indices again (they are what a replayed CUDA graph
+    reads): an index outside the pool, behind a host mirror that was in range, sets bit 2 of the
+    status word and leaves the pool alone; the other sequence is computed as usual."""
+    from linear_attention_gated_gb300 import kda
+    lengths = [40, 23]
+    x = ki.make_inputs(1, 0, 1, 2, seed=49, lengths=lengths)
+    d = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    pool0 = (0.05 * torch.randn((3, 2, 128, 128), generator=torch.Generator().manual_seed(50))).cuda()
+    cu_cpu = x["cu_seqlens"].clone()
+    mirror = torch.tensor([2, 0], dtype=torch.int32)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["A_log"], d["dt_bias"])
+    ref_pool = pool0.clone()
+    ref_o = kda.kda_prefill(*args, ref_pool, cu_seqlens=d["cu_seqlens"], cu_seqlens_cpu=cu_cpu,
+                            state_indices=mirror.cuda(), state_indices_cpu=mirror, **LOGITS)
+    pool = pool0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = kda.kda_prefill(*args, pool, cu_seqlens=d["cu_seqlens"], cu_seqlens_cpu=cu_cpu,
+                        state_indices=torch.tensor([2, 3], dtype=torch.int32, device="cuda"),
+                        state_indices_cpu=mirror, device_status=status, **LOGITS)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 4
+    assert torch.equal(o[:, :lengths[0]], ref_o[:, :lengths[0]])
+    want = pool0.clone()
+    want[2] = ref_pool[2]
+    assert torch.equal(pool, want)
