@@ -84,6 +84,20 @@ def test_long_sequence():
     _log("long_sequence", compare(gpu, run_oracle(x)))
 
 
+def test_zero_and_scaled_rows():
+    """Padding-like tokens with all-zero q or k (the norm's eps takes over: q^ = 0 and the norm
+    backward scales by 1/sqrt(1e-6) = 1000), a query row scaled by 1000 (normalised away) and value
+    rows scaled by 50 (outputs and state grow in proportion) still match the oracle."""
+    x = ki.make_inputs(1, 0, 2, 4, seed=108, lengths=[50, 29])
+    x["q"][0, 5:9] = 0
+    x["k"][0, 12:14] = 0
+    x["k"][0, 60] = 0
+    x["q"][0, 20] = (x["q"][0, 20].float() * 1000).to(torch.bfloat16)
+    x["v"][0, 30:40] = (x["v"][0, 30:40].float() * 50).to(torch.bfloat16)
+    gpu, _ = run_gpu(x)
+    _log("zero_and_scaled_rows", compare(gpu, run_oracle(x)))
+
+
 def _random_case(seed):
     """A seeded random small problem: layout, sequence count and lengths (ragged, 1..159 tokens),
     query/key heads and GQA ratio."""
