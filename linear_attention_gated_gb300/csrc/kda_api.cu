@@ -13,6 +13,7 @@
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
+#include "kda_host.h"
 #include "tc.cuh"
 
 using kda::SeqInfo;
@@ -77,6 +78,8 @@ kda_status make_shape(int64_t B, int64_t T, int64_t Hqk, int64_t Hv, const int64
     return fail(KDA_ERR_INVALID_ARGUMENT, "Hv must be a positive multiple of Hqk (Hqk=%lld Hv=%lld)",
                 (long long)Hqk, (long long)Hv);
   if (Hv / Hqk > 1024) return fail(KDA_ERR_UNSUPPORTED, "Hv / Hqk above 1024 is not supported");
+  if (const char* why = kda::size_limit_violation(B, T, Hv, cu_host ? num_seqs : 0))
+    return fail(KDA_ERR_UNSUPPORTED, "problem too large: %s", why);
   s.B = B; s.T = T; s.Hqk = Hqk; s.Hv = Hv;
   if (cu_host == nullptr) {
     s.packed = false;
@@ -244,12 +247,14 @@ int32_t kda_checkpoint_tokens(void) { return kda::kCkTokens; }
 
 kda_status kda_ctx_workspace_bytes(int64_t B, int64_t T, int64_t Hqk, int64_t Hv,
                                    const int64_t* cu_seqlens_host, int64_t num_seqs, size_t* bytes) {
-  if (!bytes) return fail(KDA_ERR_INVALID_ARGUMENT, "bytes is NULL");
-  Shape s;
-  kda_status st = make_shape(B, T, Hqk, Hv, cu_seqlens_host, num_seqs, &s);
-  if (st != KDA_OK) return st;
-  *bytes = make_layout(s).total;
-  return KDA_OK;
+  return kda::guarded([&]() -> kda_status {
+    if (!bytes) return fail(KDA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    Shape s;
+    kda_status st = make_shape(B, T, Hqk, Hv, cu_seqlens_host, num_seqs, &s);
+    if (st != KDA_OK) return st;
+    *bytes = make_layout(s).total;
+    return KDA_OK;
+  });
 }
 
 kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
@@ -258,172 +263,176 @@ kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, cons
                    int64_t B, int64_t T, int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
                    float lower_bound, kda_bf16* o, float* h_T, void* ctx_workspace, size_t ctx_bytes,
                    kda_ctx** ctx, struct CUstream_st* stream_) {
-  g_last_error.clear();
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (!ctx) return fail(KDA_ERR_INVALID_ARGUMENT, "ctx is NULL");
-  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !h0 || !o || !h_T || !ctx_workspace)
-    return fail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
-  if ((cu_seqlens_dev == nullptr) != (cu_seqlens_host == nullptr))
-    return fail(KDA_ERR_INVALID_ARGUMENT, "packed input needs both cu_seqlens and its host mirror");
-  if (head_dim != kda::kDim)
-    return fail(KDA_ERR_UNSUPPORTED, "head dimension must be 128 (got %lld)", (long long)head_dim);
-  const float s_req = (float)(1.0 / std::sqrt(128.0));
-  if (std::isnan(scale)) scale = s_req;
-  if (std::fabs(scale - s_req) > 1e-6f * s_req)
-    return fail(KDA_ERR_UNSUPPORTED, "scale must be 1/sqrt(128) (got %g)", (double)scale);
-  if (lower_bound != -5.0f)
-    return fail(KDA_ERR_UNSUPPORTED, "lower_bound must be -5 (got %g)", (double)lower_bound);
-  Shape s;
-  kda_status st = make_shape(B, T, Hqk, Hv, cu_seqlens_host, num_seqs, &s);
-  if (st != KDA_OK) return st;
-  const Layout L = make_layout(s);
-  if (ctx_bytes < L.total)
-    return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "context workspace needs %zu bytes, got %zu", L.total, ctx_bytes);
-  if (((uintptr_t)ctx_workspace % kAlign) != 0)
-    return fail(KDA_ERR_INVALID_ARGUMENT, "context workspace must be 256-byte aligned");
-  const void* vec_ptrs[] = {q, k, v, g, o, h_T, h0};
-  for (const void* p : vec_ptrs)
-    if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARGUMENT, "token and state tensors must be 16-byte aligned");
-  const size_t tok_qk = sizeof(kda_bf16) * (size_t)s.Ttot * Hqk * kda::kDim;
-  const size_t tok_v = sizeof(kda_bf16) * (size_t)s.Ttot * Hv * kda::kDim;
-  const size_t state = sizeof(float) * (size_t)s.N * Hv * kda::kDim * kda::kDim;
-  std::vector<Range> inputs = {
-      {q, tok_qk, "q"}, {k, tok_qk, "k"}, {v, tok_v, "v"}, {g, tok_v, "g"},
-      {beta, sizeof(kda_bf16) * (size_t)s.Ttot * Hv, "beta"}, {A_log, sizeof(float) * (size_t)Hv, "A_log"},
-      {dt_bias, sizeof(float) * (size_t)Hv * kda::kDim, "dt_bias"}, {h0, state, "initial_state"},
-      {cu_seqlens_dev, cu_seqlens_dev ? sizeof(int64_t) * (size_t)(s.N + 1) : 0, "cu_seqlens"}};
-  std::vector<Range> outputs = {{o, tok_v, "o"}, {h_T, state, "final_state"},
-                                {ctx_workspace, ctx_bytes, "context workspace"}};
-  if ((st = check_aliasing(inputs, outputs)) != KDA_OK) return st;
-  int dev = -1;
-  if ((st = check_device(&dev)) != KDA_OK) return st;
+  return kda::guarded([&]() -> kda_status {
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!ctx) return fail(KDA_ERR_INVALID_ARGUMENT, "ctx is NULL");
+    if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !h0 || !o || !h_T || !ctx_workspace)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
+    if ((cu_seqlens_dev == nullptr) != (cu_seqlens_host == nullptr))
+      return fail(KDA_ERR_INVALID_ARGUMENT, "packed input needs both cu_seqlens and its host mirror");
+    if (head_dim != kda::kDim)
+      return fail(KDA_ERR_UNSUPPORTED, "head dimension must be 128 (got %lld)", (long long)head_dim);
+    const float s_req = (float)(1.0 / std::sqrt(128.0));
+    if (std::isnan(scale)) scale = s_req;
+    if (std::fabs(scale - s_req) > 1e-6f * s_req)
+      return fail(KDA_ERR_UNSUPPORTED, "scale must be 1/sqrt(128) (got %g)", (double)scale);
+    if (lower_bound != -5.0f)
+      return fail(KDA_ERR_UNSUPPORTED, "lower_bound must be -5 (got %g)", (double)lower_bound);
+    Shape s;
+    kda_status st = make_shape(B, T, Hqk, Hv, cu_seqlens_host, num_seqs, &s);
+    if (st != KDA_OK) return st;
+    const Layout L = make_layout(s);
+    if (ctx_bytes < L.total)
+      return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "context workspace needs %zu bytes, got %zu", L.total, ctx_bytes);
+    if (((uintptr_t)ctx_workspace % kAlign) != 0)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "context workspace must be 256-byte aligned");
+    const void* vec_ptrs[] = {q, k, v, g, o, h_T, h0};
+    for (const void* p : vec_ptrs)
+      if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARGUMENT, "token and state tensors must be 16-byte aligned");
+    const size_t tok_qk = sizeof(kda_bf16) * (size_t)s.Ttot * Hqk * kda::kDim;
+    const size_t tok_v = sizeof(kda_bf16) * (size_t)s.Ttot * Hv * kda::kDim;
+    const size_t state = sizeof(float) * (size_t)s.N * Hv * kda::kDim * kda::kDim;
+    std::vector<Range> inputs = {
+        {q, tok_qk, "q"}, {k, tok_qk, "k"}, {v, tok_v, "v"}, {g, tok_v, "g"},
+        {beta, sizeof(kda_bf16) * (size_t)s.Ttot * Hv, "beta"}, {A_log, sizeof(float) * (size_t)Hv, "A_log"},
+        {dt_bias, sizeof(float) * (size_t)Hv * kda::kDim, "dt_bias"}, {h0, state, "initial_state"},
+        {cu_seqlens_dev, cu_seqlens_dev ? sizeof(int64_t) * (size_t)(s.N + 1) : 0, "cu_seqlens"}};
+    std::vector<Range> outputs = {{o, tok_v, "o"}, {h_T, state, "final_state"},
+                                  {ctx_workspace, ctx_bytes, "context workspace"}};
+    if ((st = check_aliasing(inputs, outputs)) != KDA_OK) return st;
+    int dev = -1;
+    if ((st = check_device(&dev)) != KDA_OK) return st;
 
-  kda_ctx* c = *ctx;
-  bool fresh = false;
-  if (c == nullptr) {
-    c = new (std::nothrow) kda_ctx();
-    if (!c) return fail(KDA_ERR_INVALID_ARGUMENT, "out of host memory");
-    fresh = true;
-    c->shape = s;
-    c->layout = L;
-    c->device = dev;
-    c->stream = stream;
-    c->ws = static_cast<char*>(ctx_workspace);
-    c->ws_bytes = ctx_bytes;
-    // longest sequence first; ties by (sequence, head)
-    c->order.resize(s.units);
-    for (int64_t u = 0; u < s.units; ++u) c->order[u] = (int32_t)u;
-    std::stable_sort(c->order.begin(), c->order.end(), [&](int32_t a, int32_t b) {
-      const int64_t la = s.cu[a / Hv + 1] - s.cu[a / Hv], lb = s.cu[b / Hv + 1] - s.cu[b / Hv];
-      return la > lb;
-    });
-    c->seq.resize(s.N);
-    int64_t ck = 0, chn = 0;
-    for (int64_t i = 0; i < s.N; ++i) {
-      c->seq[i].t0 = s.cu[i];
-      c->seq[i].len = s.cu[i + 1] - s.cu[i];
-      c->seq[i].ck_base = ck;
-      c->seq[i].ch_base = chn;
-      ck += (c->seq[i].len + kda::kCkTokens - 1) / kda::kCkTokens;
-      chn += (c->seq[i].len + kda::kChunk - 1) / kda::kChunk;
+    kda_ctx* c = *ctx;
+    bool fresh = false;
+    if (c == nullptr) {
+      c = new (std::nothrow) kda_ctx();
+      if (!c) return fail(KDA_ERR_INVALID_ARGUMENT, "out of host memory");
+      fresh = true;
+      c->shape = s;
+      c->layout = L;
+      c->device = dev;
+      c->stream = stream;
+      c->ws = static_cast<char*>(ctx_workspace);
+      c->ws_bytes = ctx_bytes;
+      // longest sequence first; ties by (sequence, head)
+      c->order.resize(s.units);
+      for (int64_t u = 0; u < s.units; ++u) c->order[u] = (int32_t)u;
+      std::stable_sort(c->order.begin(), c->order.end(), [&](int32_t a, int32_t b) {
+        const int64_t la = s.cu[a / Hv + 1] - s.cu[a / Hv], lb = s.cu[b / Hv + 1] - s.cu[b / Hv];
+        return la > lb;
+      });
+      c->seq.resize(s.N);
+      int64_t ck = 0, chn = 0;
+      for (int64_t i = 0; i < s.N; ++i) {
+        c->seq[i].t0 = s.cu[i];
+        c->seq[i].len = s.cu[i + 1] - s.cu[i];
+        c->seq[i].ck_base = ck;
+        c->seq[i].ch_base = chn;
+        ck += (c->seq[i].len + kda::kCkTokens - 1) / kda::kCkTokens;
+        chn += (c->seq[i].len + kda::kChunk - 1) / kda::kChunk;
+      }
+    } else {
+      if (!(c->shape == s)) return fail(KDA_ERR_CONTEXT, "context was created for a different shape");
+      if (c->device != dev) return fail(KDA_ERR_CONTEXT, "context belongs to device %d", c->device);
+      if (c->stream != stream) return fail(KDA_ERR_CONTEXT, "context must be reused on the stream that created it");
+      if (c->ws != ctx_workspace || c->ws_bytes != ctx_bytes)
+        return fail(KDA_ERR_CONTEXT, "context must be reused with the workspace it was created with");
     }
-  } else {
-    if (!(c->shape == s)) return fail(KDA_ERR_CONTEXT, "context was created for a different shape");
-    if (c->device != dev) return fail(KDA_ERR_CONTEXT, "context belongs to device %d", c->device);
-    if (c->stream != stream) return fail(KDA_ERR_CONTEXT, "context must be reused on the stream that created it");
-    if (c->ws != ctx_workspace || c->ws_bytes != ctx_bytes)
-      return fail(KDA_ERR_CONTEXT, "context must be reused with the workspace it was created with");
-  }
-  cudaError_t e;
-  if (fresh) {
-    if ((e = cudaMemcpyAsync(c->ws + L.order, c->order.data(), sizeof(int32_t) * s.units,
-                             cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(c->ws + L.seq, c->seq.data(), sizeof(SeqInfo) * s.N,
-                             cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(c->ws + L.status, 0, 16, stream)) != cudaSuccess) {
-      delete c;
-      return cuda_fail(e, "plan upload");
+    cudaError_t e;
+    if (fresh) {
+      if ((e = cudaMemcpyAsync(c->ws + L.order, c->order.data(), sizeof(int32_t) * s.units,
+                               cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+          (e = cudaMemcpyAsync(c->ws + L.seq, c->seq.data(), sizeof(SeqInfo) * s.N,
+                               cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+          (e = cudaMemsetAsync(c->ws + L.status, 0, 16, stream)) != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "plan upload");
+      }
     }
-  }
-  kda::Problem& P = c->prob;
-  P.q = reinterpret_cast<const __nv_bfloat16*>(q);
-  P.k = reinterpret_cast<const __nv_bfloat16*>(k);
-  P.v = reinterpret_cast<const __nv_bfloat16*>(v);
-  P.g = reinterpret_cast<const __nv_bfloat16*>(g);
-  P.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
-  P.A_log = A_log;
-  P.dt_bias = dt_bias;
-  P.h0 = h0;
-  P.order = reinterpret_cast<const int32_t*>(c->ws + L.order);
-  P.seq = reinterpret_cast<const SeqInfo*>(c->ws + L.seq);
-  P.ckpt = reinterpret_cast<float*>(c->ws + L.ckpt);
-  P.status = reinterpret_cast<int32_t*>(c->ws + L.status);
-  P.utape = reinterpret_cast<float*>(c->ws + L.utape);
-  P.abtape = reinterpret_cast<float*>(c->ws + L.abtape);
-  P.N = s.N;
-  P.Hqk = Hqk;
-  P.Hv = Hv;
-  P.r = (int32_t)(Hv / Hqk);
-  P.scale = scale;
-  P.lb = lower_bound;
-  kda::FwdOut out{reinterpret_cast<__nv_bfloat16*>(o), h_T};
-  c->forward_done = false;
-  if ((e = kda::launch_forward(P, out, s.units, stream)) != cudaSuccess) {
-    if (fresh) delete c;
-    return cuda_fail(e, "forward launch");
-  }
-  c->inputs = inputs;
-  c->forward_done = true;
-  *ctx = c;
-  return KDA_OK;
+    kda::Problem& P = c->prob;
+    P.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    P.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    P.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    P.g = reinterpret_cast<const __nv_bfloat16*>(g);
+    P.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    P.A_log = A_log;
+    P.dt_bias = dt_bias;
+    P.h0 = h0;
+    P.order = reinterpret_cast<const int32_t*>(c->ws + L.order);
+    P.seq = reinterpret_cast<const SeqInfo*>(c->ws + L.seq);
+    P.ckpt = reinterpret_cast<float*>(c->ws + L.ckpt);
+    P.status = reinterpret_cast<int32_t*>(c->ws + L.status);
+    P.utape = reinterpret_cast<float*>(c->ws + L.utape);
+    P.abtape = reinterpret_cast<float*>(c->ws + L.abtape);
+    P.N = s.N;
+    P.Hqk = Hqk;
+    P.Hv = Hv;
+    P.r = (int32_t)(Hv / Hqk);
+    P.scale = scale;
+    P.lb = lower_bound;
+    kda::FwdOut out{reinterpret_cast<__nv_bfloat16*>(o), h_T};
+    c->forward_done = false;
+    if ((e = kda::launch_forward(P, out, s.units, stream)) != cudaSuccess) {
+      if (fresh) delete c;
+      return cuda_fail(e, "forward launch");
+    }
+    c->inputs = inputs;
+    c->forward_done = true;
+    *ctx = c;
+    return KDA_OK;
+  });
 }
 
 kda_status kda_bwd(kda_ctx* c, const kda_bf16* d_o, const float* d_hT, kda_bf16* dq, kda_bf16* dk,
                    kda_bf16* dv, kda_bf16* dg, kda_bf16* dbeta, float* dA_log, float* ddt_bias,
                    float* dh0, struct CUstream_st* stream_) {
-  g_last_error.clear();
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (!c) return fail(KDA_ERR_INVALID_ARGUMENT, "ctx is NULL");
-  if (!c->forward_done) return fail(KDA_ERR_CONTEXT, "context holds no completed forward");
-  if (!d_o || !d_hT || !dq || !dk || !dv || !dg || !dbeta || !dA_log || !ddt_bias || !dh0)
-    return fail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
-  if (stream != c->stream) return fail(KDA_ERR_CONTEXT, "backward must run on the context's stream");
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device)
-    return fail(KDA_ERR_CONTEXT, "backward must run on the context's device (%d)", c->device);
-  const void* vec_ptrs[] = {d_o, d_hT, dq, dk, dv, dg, dh0};
-  for (const void* p : vec_ptrs)
-    if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARGUMENT, "token and state tensors must be 16-byte aligned");
-  const Shape& s = c->shape;
-  const size_t tok_qk = sizeof(kda_bf16) * (size_t)s.Ttot * s.Hqk * kda::kDim;
-  const size_t tok_v = sizeof(kda_bf16) * (size_t)s.Ttot * s.Hv * kda::kDim;
-  const size_t state = sizeof(float) * (size_t)s.N * s.Hv * kda::kDim * kda::kDim;
-  std::vector<Range> inputs = c->inputs;
-  inputs.push_back({d_o, tok_v, "do"});
-  inputs.push_back({d_hT, state, "dfinal_state"});
-  inputs.push_back({c->ws, c->ws_bytes, "context workspace"});
-  std::vector<Range> outputs = {
-      {dq, tok_qk, "dq"}, {dk, tok_qk, "dk"}, {dv, tok_v, "dv"}, {dg, tok_v, "dg"},
-      {dbeta, sizeof(kda_bf16) * (size_t)s.Ttot * s.Hv, "dbeta"},
-      {dA_log, sizeof(float) * (size_t)s.Hv, "dA_log"},
-      {ddt_bias, sizeof(float) * (size_t)s.Hv * kda::kDim, "ddt_bias"},
-      {dh0, state, "dinitial_state"}};
-  kda_status st = check_aliasing(inputs, outputs);
-  if (st != KDA_OK) return st;
-  kda::BwdArgs a;
-  a.d_o = reinterpret_cast<const __nv_bfloat16*>(d_o);
-  a.d_hT = d_hT;
-  a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
-  a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
-  a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
-  a.dg = reinterpret_cast<__nv_bfloat16*>(dg);
-  a.dbeta = reinterpret_cast<__nv_bfloat16*>(dbeta);
-  a.dh0 = dh0;
-  a.dqk_part = reinterpret_cast<float*>(c->ws + c->layout.dqk);
-  a.par_part = reinterpret_cast<float*>(c->ws + c->layout.par);
-  cudaError_t e = kda::launch_backward(c->prob, a, s.units, s.Ttot, dA_log, ddt_bias, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-  return KDA_OK;
+  return kda::guarded([&]() -> kda_status {
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!c) return fail(KDA_ERR_INVALID_ARGUMENT, "ctx is NULL");
+    if (!c->forward_done) return fail(KDA_ERR_CONTEXT, "context holds no completed forward");
+    if (!d_o || !d_hT || !dq || !dk || !dv || !dg || !dbeta || !dA_log || !ddt_bias || !dh0)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
+    if (stream != c->stream) return fail(KDA_ERR_CONTEXT, "backward must run on the context's stream");
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device)
+      return fail(KDA_ERR_CONTEXT, "backward must run on the context's device (%d)", c->device);
+    const void* vec_ptrs[] = {d_o, d_hT, dq, dk, dv, dg, dh0};
+    for (const void* p : vec_ptrs)
+      if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARGUMENT, "token and state tensors must be 16-byte aligned");
+    const Shape& s = c->shape;
+    const size_t tok_qk = sizeof(kda_bf16) * (size_t)s.Ttot * s.Hqk * kda::kDim;
+    const size_t tok_v = sizeof(kda_bf16) * (size_t)s.Ttot * s.Hv * kda::kDim;
+    const size_t state = sizeof(float) * (size_t)s.N * s.Hv * kda::kDim * kda::kDim;
+    std::vector<Range> inputs = c->inputs;
+    inputs.push_back({d_o, tok_v, "do"});
+    inputs.push_back({d_hT, state, "dfinal_state"});
+    inputs.push_back({c->ws, c->ws_bytes, "context workspace"});
+    std::vector<Range> outputs = {
+        {dq, tok_qk, "dq"}, {dk, tok_qk, "dk"}, {dv, tok_v, "dv"}, {dg, tok_v, "dg"},
+        {dbeta, sizeof(kda_bf16) * (size_t)s.Ttot * s.Hv, "dbeta"},
+        {dA_log, sizeof(float) * (size_t)s.Hv, "dA_log"},
+        {ddt_bias, sizeof(float) * (size_t)s.Hv * kda::kDim, "ddt_bias"},
+        {dh0, state, "dinitial_state"}};
+    kda_status st = check_aliasing(inputs, outputs);
+    if (st != KDA_OK) return st;
+    kda::BwdArgs a;
+    a.d_o = reinterpret_cast<const __nv_bfloat16*>(d_o);
+    a.d_hT = d_hT;
+    a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
+    a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
+    a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+    a.dg = reinterpret_cast<__nv_bfloat16*>(dg);
+    a.dbeta = reinterpret_cast<__nv_bfloat16*>(dbeta);
+    a.dh0 = dh0;
+    a.dqk_part = reinterpret_cast<float*>(c->ws + c->layout.dqk);
+    a.par_part = reinterpret_cast<float*>(c->ws + c->layout.par);
+    cudaError_t e = kda::launch_backward(c->prob, a, s.units, s.Ttot, dA_log, ddt_bias, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return KDA_OK;
+  });
 }
 
 kda_status kda_ctx_status(kda_ctx* c) {

@@ -21,6 +21,7 @@
 // straight back.
 #include "../../include/kda.h"
 #include "kda_common.cuh"
+#include "kda_host.h"
 #include "tc.cuh"
 
 #include <cmath>
@@ -211,87 +212,92 @@ extern "C" kda_status kda_decode(const kda_bf16* q, const kda_bf16* k, const kda
                                  int64_t Hv, int64_t head_dim, float scale, float lower_bound,
                                  int32_t use_gate_in_kernel, int32_t beta_is_logit, kda_bf16* o,
                                  struct CUstream_st* stream) {
-  if (N < 1 || Hqk < 1 || Hv < 1) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: N, Hqk and Hv must be positive");
-  if (Hv % Hqk != 0) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: Hv must be a multiple of Hqk");
-  if (head_dim != kda::kDim) return dfail(KDA_ERR_UNSUPPORTED, "decode: head_dim must be 128");
-  const float s_def = 1.0f / std::sqrt((float)kda::kDim);
-  if (!std::isnan(scale) && scale != s_def)
-    return dfail(KDA_ERR_UNSUPPORTED, "decode: scale must be 1/sqrt(128) (NaN selects it)");
-  if ((use_gate_in_kernel != 0 && use_gate_in_kernel != 1) || (beta_is_logit != 0 && beta_is_logit != 1))
-    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: use_gate_in_kernel and beta_is_logit must be 0 or 1");
-  if (use_gate_in_kernel && lower_bound != -5.0f)
-    return dfail(KDA_ERR_UNSUPPORTED, "decode: lower_bound must be -5 with the gate computed in the kernel");
-  if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32)
-    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_dtype must be KDA_STATE_BF16 or KDA_STATE_FP32");
-  if (!q || !k || !v || !g || !beta || !state || !o || (use_gate_in_kernel && (!A_log || !dt_bias)))
-    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: null tensor pointer");
-  if ((state_indices == nullptr) != (state_indices_host == nullptr))
-    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_indices needs its host mirror (and the reverse)");
-  if (state_indices_host) {
-    std::unordered_set<int32_t> seen;
-    for (int64_t i = 0; i < N; ++i) {
-      const int32_t s = state_indices_host[i];
-      if (s < 0 || s >= num_slots) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state index out of range");
-      if (!seen.insert(s).second)
-        return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: two sequences share a state slot");
+  return kda::guarded([&]() -> kda_status {
+    if (N < 1 || Hqk < 1 || Hv < 1) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: N, Hqk and Hv must be positive");
+    if (Hv % Hqk != 0) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: Hv must be a multiple of Hqk");
+    if (kda::size_limit_violation(N, 1, Hv, 0) || N > INT32_MAX / Hv)
+      return dfail(KDA_ERR_UNSUPPORTED, "decode: too many (sequence, head) units");
+    if (num_slots > (int64_t(1) << 31)) return dfail(KDA_ERR_UNSUPPORTED, "decode: more than 2^31 pool slots");
+    if (head_dim != kda::kDim) return dfail(KDA_ERR_UNSUPPORTED, "decode: head_dim must be 128");
+    const float s_def = 1.0f / std::sqrt((float)kda::kDim);
+    if (!std::isnan(scale) && scale != s_def)
+      return dfail(KDA_ERR_UNSUPPORTED, "decode: scale must be 1/sqrt(128) (NaN selects it)");
+    if ((use_gate_in_kernel != 0 && use_gate_in_kernel != 1) || (beta_is_logit != 0 && beta_is_logit != 1))
+      return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: use_gate_in_kernel and beta_is_logit must be 0 or 1");
+    if (use_gate_in_kernel && lower_bound != -5.0f)
+      return dfail(KDA_ERR_UNSUPPORTED, "decode: lower_bound must be -5 with the gate computed in the kernel");
+    if (state_dtype != KDA_STATE_BF16 && state_dtype != KDA_STATE_FP32)
+      return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_dtype must be KDA_STATE_BF16 or KDA_STATE_FP32");
+    if (!q || !k || !v || !g || !beta || !state || !o || (use_gate_in_kernel && (!A_log || !dt_bias)))
+      return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: null tensor pointer");
+    if ((state_indices == nullptr) != (state_indices_host == nullptr))
+      return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state_indices needs its host mirror (and the reverse)");
+    if (state_indices_host) {
+      std::unordered_set<int32_t> seen;
+      for (int64_t i = 0; i < N; ++i) {
+        const int32_t s = state_indices_host[i];
+        if (s < 0 || s >= num_slots) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: state index out of range");
+        if (!seen.insert(s).second)
+          return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: two sequences share a state slot");
+      }
+    } else if (num_slots < N) {
+      return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: without state_indices the pool needs a slot per sequence");
     }
-  } else if (num_slots < N) {
-    return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: without state_indices the pool needs a slot per sequence");
-  }
-  const void* ptrs[] = {q, k, v, g, state, o};
-  for (const void* p : ptrs)
-    if ((uintptr_t)p & 15u) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: token and state tensors must be 16-byte aligned");
-  const size_t esz = state_dtype == KDA_STATE_BF16 ? 2 : 4;
-  const Span st{state, esz * (size_t)num_slots * Hv * kda::kDim * kda::kDim};
-  const Span out{o, 2 * (size_t)N * Hv * kda::kDim};
-  const Span ins[] = {{q, 2 * (size_t)N * Hqk * kda::kDim}, {k, 2 * (size_t)N * Hqk * kda::kDim},
-                      {v, 2 * (size_t)N * Hv * kda::kDim},  {g, 2 * (size_t)N * Hv * kda::kDim},
-                      {beta, 2 * (size_t)N * Hv},
-                      {A_log, use_gate_in_kernel ? 4 * (size_t)Hv : 0},
-                      {dt_bias, use_gate_in_kernel ? 4 * (size_t)Hv * kda::kDim : 0}};
-  for (const Span& in : ins)
-    if (overlap(in, st) || overlap(in, out)) return dfail(KDA_ERR_ALIASING, "decode: an input overlaps the state or o");
-  if (overlap(st, out)) return dfail(KDA_ERR_ALIASING, "decode: o overlaps the state");
-  if (state_indices && overlap(Span{state_indices, 4 * (size_t)N}, st))
-    return dfail(KDA_ERR_ALIASING, "decode: state_indices overlaps the state");
+    const void* ptrs[] = {q, k, v, g, state, o};
+    for (const void* p : ptrs)
+      if ((uintptr_t)p & 15u) return dfail(KDA_ERR_INVALID_ARGUMENT, "decode: token and state tensors must be 16-byte aligned");
+    const size_t esz = state_dtype == KDA_STATE_BF16 ? 2 : 4;
+    const Span st{state, esz * (size_t)num_slots * Hv * kda::kDim * kda::kDim};
+    const Span out{o, 2 * (size_t)N * Hv * kda::kDim};
+    const Span ins[] = {{q, 2 * (size_t)N * Hqk * kda::kDim}, {k, 2 * (size_t)N * Hqk * kda::kDim},
+                        {v, 2 * (size_t)N * Hv * kda::kDim},  {g, 2 * (size_t)N * Hv * kda::kDim},
+                        {beta, 2 * (size_t)N * Hv},
+                        {A_log, use_gate_in_kernel ? 4 * (size_t)Hv : 0},
+                        {dt_bias, use_gate_in_kernel ? 4 * (size_t)Hv * kda::kDim : 0}};
+    for (const Span& in : ins)
+      if (overlap(in, st) || overlap(in, out)) return dfail(KDA_ERR_ALIASING, "decode: an input overlaps the state or o");
+    if (overlap(st, out)) return dfail(KDA_ERR_ALIASING, "decode: o overlaps the state");
+    if (state_indices && overlap(Span{state_indices, 4 * (size_t)N}, st))
+      return dfail(KDA_ERR_ALIASING, "decode: state_indices overlaps the state");
 
-  int dev = -1, major = 0, minor = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
-  if (major != 10 || minor != 3) return dfail(KDA_ERR_UNSUPPORTED, "decode: kernels are built for sm_103a");
+    int dev = -1, major = 0, minor = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
+    if (major != 10 || minor != 3) return dfail(KDA_ERR_UNSUPPORTED, "decode: kernels are built for sm_103a");
 
-  kda::DecodeArgs a{};
-  a.q = reinterpret_cast<const __nv_bfloat16*>(q);
-  a.k = reinterpret_cast<const __nv_bfloat16*>(k);
-  a.v = reinterpret_cast<const __nv_bfloat16*>(v);
-  a.g = reinterpret_cast<const __nv_bfloat16*>(g);
-  a.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
-  a.A_log = A_log;
-  a.dt_bias = dt_bias;
-  a.state = state;
-  a.idx = state_indices;
-  a.num_slots = num_slots;
-  a.o = reinterpret_cast<__nv_bfloat16*>(o);
-  a.Hqk = Hqk;
-  a.Hv = Hv;
-  a.r = Hv / Hqk;
-  a.scale = s_def;
-  a.lb = lower_bound;
-  a.gate_in_kernel = use_gate_in_kernel;
-  a.beta_logit = beta_is_logit;
-  const unsigned grid = (unsigned)(N * Hv);
-  const size_t smem = state_dtype == KDA_STATE_BF16 ? esz * kda::kDim * kda::kDim : 0;
-  if (state_dtype == KDA_STATE_BF16) {
-    e = cudaFuncSetAttribute(kda::kda_decode_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) kda::kda_decode_kernel<__nv_bfloat16><<<grid, kda::kDecThreads, smem, stream>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(kda::kda_decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) kda::kda_decode_kernel<float><<<grid, kda::kDecThreads, smem, stream>>>(a);
-  }
-  if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
-  return KDA_OK;
+    kda::DecodeArgs a{};
+    a.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    a.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    a.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    a.g = reinterpret_cast<const __nv_bfloat16*>(g);
+    a.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    a.A_log = A_log;
+    a.dt_bias = dt_bias;
+    a.state = state;
+    a.idx = state_indices;
+    a.num_slots = num_slots;
+    a.o = reinterpret_cast<__nv_bfloat16*>(o);
+    a.Hqk = Hqk;
+    a.Hv = Hv;
+    a.r = Hv / Hqk;
+    a.scale = s_def;
+    a.lb = lower_bound;
+    a.gate_in_kernel = use_gate_in_kernel;
+    a.beta_logit = beta_is_logit;
+    const unsigned grid = (unsigned)(N * Hv);
+    const size_t smem = state_dtype == KDA_STATE_BF16 ? esz * kda::kDim * kda::kDim : 0;
+    if (state_dtype == KDA_STATE_BF16) {
+      e = cudaFuncSetAttribute(kda::kda_decode_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) kda::kda_decode_kernel<__nv_bfloat16><<<grid, kda::kDecThreads, smem, stream>>>(a);
+    } else {
+      e = cudaFuncSetAttribute(kda::kda_decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) kda::kda_decode_kernel<float><<<grid, kda::kDecThreads, smem, stream>>>(a);
+    }
+    if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return dfail(KDA_ERR_CUDA, cudaGetErrorString(e));
+    return KDA_OK;
+  });
 }

@@ -23,6 +23,7 @@
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
+#include "kda_host.h"
 
 namespace {
 
@@ -109,138 +110,142 @@ extern "C" kda_status kda_bwd_noalloc(
     int64_t head_dim, float scale, float lower_bound, const kda_bf16* d_o, const float* d_hT,
     kda_bf16* dq, kda_bf16* dk, kda_bf16* dv, kda_bf16* dg, kda_bf16* dbeta, float* dA_log,
     float* ddt_bias, float* dh0, struct CUstream_st* stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  kda::set_last_error("");
-  if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !h0 || !d_o || !d_hT || !dq || !dk || !dv ||
-      !dg || !dbeta || !dA_log || !ddt_bias || !dh0)
-    return nfail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
-  if ((cu_seqlens_dev == nullptr) != (cu_seqlens_host == nullptr))
-    return nfail(KDA_ERR_INVALID_ARGUMENT, "packed input needs both cu_seqlens and its host mirror");
-  if (head_dim != kda::kDim) return nfail(KDA_ERR_UNSUPPORTED, "head dimension must be 128");
-  const float s_req = (float)(1.0 / std::sqrt(128.0));
-  if (std::isnan(scale)) scale = s_req;
-  if (std::fabs(scale - s_req) > 1e-6f * s_req) return nfail(KDA_ERR_UNSUPPORTED, "scale must be 1/sqrt(128)");
-  if (lower_bound != -5.0f) return nfail(KDA_ERR_UNSUPPORTED, "lower_bound must be -5");
-  if (B < 1 || T < 1 || Hqk < 1 || Hv < 1 || Hv % Hqk != 0)
-    return nfail(KDA_ERR_INVALID_ARGUMENT, "need B, T >= 1 and Hv a positive multiple of Hqk");
-  int64_t N = B;
-  int64_t n_ck = 0, n_ch = 0;
-  if (cu_seqlens_host) {
-    if (B != 1 || num_seqs < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "packed input needs B == 1, num_seqs >= 1");
-    N = num_seqs;
-    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != T)
-      return nfail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must run from 0 to T");
-    for (int64_t i = 0; i < N; ++i) {
-      const int64_t len = cu_seqlens_host[i + 1] - cu_seqlens_host[i];
-      if (len < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "sequence %lld is empty", (long long)i);
-      n_ck += (len + kda::kCkTokens - 1) / kda::kCkTokens;
-      n_ch += (len + kda::kChunk - 1) / kda::kChunk;
+  return kda::guarded([&]() -> kda_status {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    kda::set_last_error("");
+    if (!q || !k || !v || !g || !beta || !A_log || !dt_bias || !h0 || !d_o || !d_hT || !dq || !dk || !dv ||
+        !dg || !dbeta || !dA_log || !ddt_bias || !dh0)
+      return nfail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
+    if ((cu_seqlens_dev == nullptr) != (cu_seqlens_host == nullptr))
+      return nfail(KDA_ERR_INVALID_ARGUMENT, "packed input needs both cu_seqlens and its host mirror");
+    if (head_dim != kda::kDim) return nfail(KDA_ERR_UNSUPPORTED, "head dimension must be 128");
+    const float s_req = (float)(1.0 / std::sqrt(128.0));
+    if (std::isnan(scale)) scale = s_req;
+    if (std::fabs(scale - s_req) > 1e-6f * s_req) return nfail(KDA_ERR_UNSUPPORTED, "scale must be 1/sqrt(128)");
+    if (lower_bound != -5.0f) return nfail(KDA_ERR_UNSUPPORTED, "lower_bound must be -5");
+    if (B < 1 || T < 1 || Hqk < 1 || Hv < 1 || Hv % Hqk != 0)
+      return nfail(KDA_ERR_INVALID_ARGUMENT, "need B, T >= 1 and Hv a positive multiple of Hqk");
+    if (const char* why = kda::size_limit_violation(B, T, Hv, cu_seqlens_host ? num_seqs : 0))
+      return nfail(KDA_ERR_UNSUPPORTED, "problem too large: %s", why);
+    int64_t N = B;
+    int64_t n_ck = 0, n_ch = 0;
+    if (cu_seqlens_host) {
+      if (B != 1 || num_seqs < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "packed input needs B == 1, num_seqs >= 1");
+      N = num_seqs;
+      if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != T)
+        return nfail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must run from 0 to T");
+      for (int64_t i = 0; i < N; ++i) {
+        const int64_t len = cu_seqlens_host[i + 1] - cu_seqlens_host[i];
+        if (len < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "sequence %lld is empty", (long long)i);
+        n_ck += (len + kda::kCkTokens - 1) / kda::kCkTokens;
+        n_ch += (len + kda::kChunk - 1) / kda::kChunk;
+      }
+    } else {
+      n_ck = B * ((T + kda::kCkTokens - 1) / kda::kCkTokens);
+      n_ch = B * ((T + kda::kChunk - 1) / kda::kChunk);
     }
-  } else {
-    n_ck = B * ((T + kda::kCkTokens - 1) / kda::kCkTokens);
-    n_ch = B * ((T + kda::kChunk - 1) / kda::kChunk);
-  }
-  const void* vec_ptrs[] = {q, k, v, g, h0, d_o, d_hT, dq, dk, dv, dg, dh0};
-  for (const void* p : vec_ptrs)
-    if ((uintptr_t)p & 15u) return nfail(KDA_ERR_INVALID_ARGUMENT, "token and state tensors must be 16-byte aligned");
+    const void* vec_ptrs[] = {q, k, v, g, h0, d_o, d_hT, dq, dk, dv, dg, dh0};
+    for (const void* p : vec_ptrs)
+      if ((uintptr_t)p & 15u) return nfail(KDA_ERR_INVALID_ARGUMENT, "token and state tensors must be 16-byte aligned");
 
-  const int64_t Ttot = B * T, units = N * Hv, r = Hv / Hqk;
-  const size_t D = kda::kDim;
-  // scratch layout
-  size_t off = 0;
-  const size_t o_order = off; off = up(off + sizeof(int32_t) * units);
-  const size_t o_seq = off;   off = up(off + sizeof(kda::SeqInfo) * N);
-  const size_t o_cu = off;    off = up(off + sizeof(int64_t) * (N + 1));
-  const size_t o_ck = off;    off = up(off + sizeof(float) * (size_t)n_ck * Hv * D * D);
-  const size_t o_ut = off;    off = up(off + sizeof(float) * (size_t)Ttot * Hv * D);
-  const size_t o_ab = off;    off = up(off + sizeof(float) * (size_t)n_ch * Hv * 2 * kda::kChunk * kda::kChunk);
-  const size_t o_dqk = off;   if (r > 1) off = up(off + sizeof(float) * (size_t)Ttot * Hv * 2 * D);
-  const size_t o_par = off;   off = up(off + sizeof(float) * (size_t)units * kda::kParStride);
-  const size_t o_o = off;     off = up(off + sizeof(kda_bf16) * (size_t)Ttot * Hv * D);
-  const size_t o_hT = off;    off = up(off + sizeof(float) * (size_t)N * Hv * D * D);
-  const size_t o_status = off; off = up(off + 16);
-  if (off > kNoAllocScratchBytes)
-    return nfail(KDA_ERR_WORKSPACE_TOO_SMALL,
-                 "problem needs %zu bytes of scratch; kda_bwd_noalloc has %zu (use kda_fwd + kda_bwd)",
-                 off, kNoAllocScratchBytes);
+    const int64_t Ttot = B * T, units = N * Hv, r = Hv / Hqk;
+    const size_t D = kda::kDim;
+    // scratch layout
+    size_t off = 0;
+    const size_t o_order = off; off = up(off + sizeof(int32_t) * units);
+    const size_t o_seq = off;   off = up(off + sizeof(kda::SeqInfo) * N);
+    const size_t o_cu = off;    off = up(off + sizeof(int64_t) * (N + 1));
+    const size_t o_ck = off;    off = up(off + sizeof(float) * (size_t)n_ck * Hv * D * D);
+    const size_t o_ut = off;    off = up(off + sizeof(float) * (size_t)Ttot * Hv * D);
+    const size_t o_ab = off;    off = up(off + sizeof(float) * (size_t)n_ch * Hv * 2 * kda::kChunk * kda::kChunk);
+    const size_t o_dqk = off;   if (r > 1) off = up(off + sizeof(float) * (size_t)Ttot * Hv * 2 * D);
+    const size_t o_par = off;   off = up(off + sizeof(float) * (size_t)units * kda::kParStride);
+    const size_t o_o = off;     off = up(off + sizeof(kda_bf16) * (size_t)Ttot * Hv * D);
+    const size_t o_hT = off;    off = up(off + sizeof(float) * (size_t)N * Hv * D * D);
+    const size_t o_status = off; off = up(off + 16);
+    if (off > kNoAllocScratchBytes)
+      return nfail(KDA_ERR_WORKSPACE_TOO_SMALL,
+                   "problem needs %zu bytes of scratch; kda_bwd_noalloc has %zu (use kda_fwd + kda_bwd)",
+                   off, kNoAllocScratchBytes);
 
-  const size_t tok_qk = sizeof(kda_bf16) * (size_t)Ttot * Hqk * D, tok_v = sizeof(kda_bf16) * (size_t)Ttot * Hv * D;
-  const size_t state = sizeof(float) * (size_t)N * Hv * D * D;
-  const Range ins[] = {{q, tok_qk, "q"}, {k, tok_qk, "k"}, {v, tok_v, "v"}, {g, tok_v, "g"},
-                       {beta, sizeof(kda_bf16) * (size_t)Ttot * Hv, "beta"}, {A_log, sizeof(float) * Hv, "A_log"},
-                       {dt_bias, sizeof(float) * Hv * D, "dt_bias"}, {h0, state, "initial_state"},
-                       {cu_seqlens_dev, cu_seqlens_dev ? sizeof(int64_t) * (N + 1) : 0, "cu_seqlens"},
-                       {d_o, tok_v, "do"}, {d_hT, state, "dfinal_state"}};
-  const Range outs[] = {{dq, tok_qk, "dq"}, {dk, tok_qk, "dk"}, {dv, tok_v, "dv"}, {dg, tok_v, "dg"},
-                        {dbeta, sizeof(kda_bf16) * (size_t)Ttot * Hv, "dbeta"}, {dA_log, sizeof(float) * Hv, "dA_log"},
-                        {ddt_bias, sizeof(float) * Hv * D, "ddt_bias"}, {dh0, state, "dinitial_state"}};
-  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
-    for (const Range& in : ins)
-      if (overlap(outs[i], in)) return nfail(KDA_ERR_ALIASING, "output %s overlaps %s", outs[i].name, in.name);
-    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
-      if (overlap(outs[i], outs[j])) return nfail(KDA_ERR_ALIASING, "output %s overlaps %s", outs[i].name, outs[j].name);
-  }
+    const size_t tok_qk = sizeof(kda_bf16) * (size_t)Ttot * Hqk * D, tok_v = sizeof(kda_bf16) * (size_t)Ttot * Hv * D;
+    const size_t state = sizeof(float) * (size_t)N * Hv * D * D;
+    const Range ins[] = {{q, tok_qk, "q"}, {k, tok_qk, "k"}, {v, tok_v, "v"}, {g, tok_v, "g"},
+                         {beta, sizeof(kda_bf16) * (size_t)Ttot * Hv, "beta"}, {A_log, sizeof(float) * Hv, "A_log"},
+                         {dt_bias, sizeof(float) * Hv * D, "dt_bias"}, {h0, state, "initial_state"},
+                         {cu_seqlens_dev, cu_seqlens_dev ? sizeof(int64_t) * (N + 1) : 0, "cu_seqlens"},
+                         {d_o, tok_v, "do"}, {d_hT, state, "dfinal_state"}};
+    const Range outs[] = {{dq, tok_qk, "dq"}, {dk, tok_qk, "dk"}, {dv, tok_v, "dv"}, {dg, tok_v, "dg"},
+                          {dbeta, sizeof(kda_bf16) * (size_t)Ttot * Hv, "dbeta"}, {dA_log, sizeof(float) * Hv, "dA_log"},
+                          {ddt_bias, sizeof(float) * Hv * D, "ddt_bias"}, {dh0, state, "dinitial_state"}};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+      for (const Range& in : ins)
+        if (overlap(outs[i], in)) return nfail(KDA_ERR_ALIASING, "output %s overlaps %s", outs[i].name, in.name);
+      for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+        if (overlap(outs[i], outs[j])) return nfail(KDA_ERR_ALIASING, "output %s overlaps %s", outs[i].name, outs[j].name);
+    }
 
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  int major = 0, minor = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return nfail(KDA_ERR_UNSUPPORTED, "kernels are built for sm_103a");
-  void* base = nullptr;
-  kda_status st = scratch_for_device(dev, &base);
-  if (st != KDA_OK) return st;
-  char* sc = static_cast<char*>(base);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return nfail(KDA_ERR_UNSUPPORTED, "kernels are built for sm_103a");
+    void* base = nullptr;
+    kda_status st = scratch_for_device(dev, &base);
+    if (st != KDA_OK) return st;
+    char* sc = static_cast<char*>(base);
 
-  int64_t* cu = reinterpret_cast<int64_t*>(sc + o_cu);
-  const int64_t* cu_src = cu_seqlens_dev;
-  if (!cu_seqlens_dev) {
-    kda_noalloc_fixed_cu_kernel<<<(unsigned)((B + 1 + 255) / 256), 256, 0, stream>>>(cu, B, T);
-    cu_src = cu;
-  }
-  kda_noalloc_plan_kernel<<<(unsigned)((units + 255) / 256), 256, 0, stream>>>(
-      cu_src, N, Hv, kda::kCkTokens, reinterpret_cast<int32_t*>(sc + o_order),
-      reinterpret_cast<kda::SeqInfo*>(sc + o_seq));
-  if ((e = cudaGetLastError()) != cudaSuccess) return nfail(KDA_ERR_CUDA, "plan launch: %s", cudaGetErrorString(e));
+    int64_t* cu = reinterpret_cast<int64_t*>(sc + o_cu);
+    const int64_t* cu_src = cu_seqlens_dev;
+    if (!cu_seqlens_dev) {
+      kda_noalloc_fixed_cu_kernel<<<(unsigned)((B + 1 + 255) / 256), 256, 0, stream>>>(cu, B, T);
+      cu_src = cu;
+    }
+    kda_noalloc_plan_kernel<<<(unsigned)((units + 255) / 256), 256, 0, stream>>>(
+        cu_src, N, Hv, kda::kCkTokens, reinterpret_cast<int32_t*>(sc + o_order),
+        reinterpret_cast<kda::SeqInfo*>(sc + o_seq));
+    if ((e = cudaGetLastError()) != cudaSuccess) return nfail(KDA_ERR_CUDA, "plan launch: %s", cudaGetErrorString(e));
 
-  kda::Problem P{};
-  P.q = reinterpret_cast<const __nv_bfloat16*>(q);
-  P.k = reinterpret_cast<const __nv_bfloat16*>(k);
-  P.v = reinterpret_cast<const __nv_bfloat16*>(v);
-  P.g = reinterpret_cast<const __nv_bfloat16*>(g);
-  P.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
-  P.A_log = A_log;
-  P.dt_bias = dt_bias;
-  P.h0 = h0;
-  P.order = reinterpret_cast<const int32_t*>(sc + o_order);
-  P.seq = reinterpret_cast<const kda::SeqInfo*>(sc + o_seq);
-  P.ckpt = reinterpret_cast<float*>(sc + o_ck);
-  P.status = reinterpret_cast<int32_t*>(sc + o_status);
-  P.utape = reinterpret_cast<float*>(sc + o_ut);
-  P.abtape = reinterpret_cast<float*>(sc + o_ab);
-  P.N = N;
-  P.Hqk = Hqk;
-  P.Hv = Hv;
-  P.r = (int32_t)r;
-  P.scale = scale;
-  P.lb = lower_bound;
-  kda::FwdOut fo{reinterpret_cast<__nv_bfloat16*>(sc + o_o), reinterpret_cast<float*>(sc + o_hT)};
-  if ((e = kda::launch_forward(P, fo, units, stream)) != cudaSuccess)
-    return nfail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
-  kda::BwdArgs a{};
-  a.d_o = reinterpret_cast<const __nv_bfloat16*>(d_o);
-  a.d_hT = d_hT;
-  a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
-  a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
-  a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
-  a.dg = reinterpret_cast<__nv_bfloat16*>(dg);
-  a.dbeta = reinterpret_cast<__nv_bfloat16*>(dbeta);
-  a.dh0 = dh0;
-  a.dqk_part = reinterpret_cast<float*>(sc + o_dqk);
-  a.par_part = reinterpret_cast<float*>(sc + o_par);
-  if ((e = kda::launch_backward(P, a, units, Ttot, dA_log, ddt_bias, stream)) != cudaSuccess)
-    return nfail(KDA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
-  return KDA_OK;
+    kda::Problem P{};
+    P.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    P.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    P.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    P.g = reinterpret_cast<const __nv_bfloat16*>(g);
+    P.beta = reinterpret_cast<const __nv_bfloat16*>(beta);
+    P.A_log = A_log;
+    P.dt_bias = dt_bias;
+    P.h0 = h0;
+    P.order = reinterpret_cast<const int32_t*>(sc + o_order);
+    P.seq = reinterpret_cast<const kda::SeqInfo*>(sc + o_seq);
+    P.ckpt = reinterpret_cast<float*>(sc + o_ck);
+    P.status = reinterpret_cast<int32_t*>(sc + o_status);
+    P.utape = reinterpret_cast<float*>(sc + o_ut);
+    P.abtape = reinterpret_cast<float*>(sc + o_ab);
+    P.N = N;
+    P.Hqk = Hqk;
+    P.Hv = Hv;
+    P.r = (int32_t)r;
+    P.scale = scale;
+    P.lb = lower_bound;
+    kda::FwdOut fo{reinterpret_cast<__nv_bfloat16*>(sc + o_o), reinterpret_cast<float*>(sc + o_hT)};
+    if ((e = kda::launch_forward(P, fo, units, stream)) != cudaSuccess)
+      return nfail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+    kda::BwdArgs a{};
+    a.d_o = reinterpret_cast<const __nv_bfloat16*>(d_o);
+    a.d_hT = d_hT;
+    a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
+    a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
+    a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+    a.dg = reinterpret_cast<__nv_bfloat16*>(dg);
+    a.dbeta = reinterpret_cast<__nv_bfloat16*>(dbeta);
+    a.dh0 = dh0;
+    a.dqk_part = reinterpret_cast<float*>(sc + o_dqk);
+    a.par_part = reinterpret_cast<float*>(sc + o_par);
+    if ((e = kda::launch_backward(P, a, units, Ttot, dA_log, ddt_bias, stream)) != cudaSuccess)
+      return nfail(KDA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+    return KDA_OK;
+  });
 }
 

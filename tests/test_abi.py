@@ -180,3 +180,17 @@ def test_bwd_rejects_null_context(lib):
 
 def test_ctx_destroy_accepts_null(lib):
     lib.kda_ctx_destroy(None)
+
+
+@pytest.mark.parametrize("args", [
+    (1 << 41, 64, 2, 2, None),          # more than 2^40 tokens
+    (1, 1 << 36, 2, 1 << 8, None),      # more than 2^40 token-heads
+    (1, 64, 1 << 12, 1 << 21, None),    # more than 2^20 value heads
+    ((1 << 62), (1 << 62), 2, 2, None),  # B * T would overflow 64 bits
+])
+def test_workspace_bytes_rejects_absurd_sizes(lib, args):
+    """Sizes that would overflow byte counts or build huge host tables are refused up front
+    (no exception crosses the C ABI, no crash)."""
+    rc, _ = ws_bytes(lib, *args)
+    assert rc == 2
+    assert "too large" in lib.kda_last_error_message().decode()
