@@ -486,7 +486,10 @@ def bench_prefill(args):
                        "checkpoint_every_n_tokens": args.prefill_checkpoint,
                        "l2": f"a prefill moves {bytes_step / 1e6:.0f} MB > 129 MB of L2, no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "kda_fwd_kernel (prefill)",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": ncu_traffic("kda_fwd_kernel_prefill", f"prefill_{args.workload}_"
+                                                f"{args.decode_state}_ck{args.prefill_checkpoint}"),
+                         "kernel": "kda_fwd_kernel (prefill)",
                          "peak_src": peaks["src"], "algorithmic_bytes_per_launch": bytes_step},
             "gpu_launches": args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
