@@ -148,7 +148,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 6; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), 1);
+    for (int i = 0; i < 6; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), i == 3 || i == 4 ? kThreads : 1);
   }
   tc::fence_before();
   __syncthreads();
@@ -484,11 +484,12 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::tmem_wait_st();
       tc::fence_async_smem();
       tc::fence_before();
-      csync();
       // ---- MMA group 1 (issued by the MMA warp): dW = Gd (k^/g)^T + scale dO^T B first (the dV
-      // chain needs it), then S0^T dO^T, Gd^T W^T and dO W^T
-      if (tid == 0) tc::mbar_arrive(rdy1);  // operands of the first MMA group are in place
+      // chain needs it), then S0^T dO^T, Gd^T W^T and dO W^T; every compute thread arrives once its
+      // own operand tiles are written (no CTA barrier)
+      tc::mbar_arrive(rdy1);
       if (warp >= 4) {
+        ok = ok && tc::mbar_wait(rdy1, ph);  // QKT below reads every thread's q^g and k^g rows
         {  // QKT, rows k: columns 0..15 scale q^g, 16..31 -k^g (the adjoint updates of the second group)
           const int k = tid - 128;
 #pragma unroll
@@ -607,9 +608,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
       tc::fence_async_smem();
       tc::fence_before();
-      csync();
-      // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T
-      if (tid == 0) tc::mbar_arrive(rdy2);  // operands of the second MMA group are in place
+      // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T;
+      // every compute thread arrives once its own operand tiles are written (no CTA barrier)
+      tc::mbar_arrive(rdy2);
       if (tid < kChunk) sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
       {  // dV W^T in FP32, one entry (i, j) per thread
         const int i = tid >> 4, j = tid & 15;
