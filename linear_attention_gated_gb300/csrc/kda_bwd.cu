@@ -157,7 +157,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   const uint32_t tl = tbase + lane_off;
   const uint32_t mbD = tc::smem_u32(&sm.mbar[0]), mb1 = tc::smem_u32(&sm.mbar[1]);
   const uint32_t mb2 = tc::smem_u32(&sm.mbar[2]);
-  const uint32_t rdy1 = tc::smem_u32(&sm.mbar[3]), rdy2 = tc::smem_u32(&sm.mbar[4]);  // compute -> MMA warp
+  // compute -> MMA warp: each of the 256 compute threads arrives once its operand tiles are stored
+  const uint32_t rdy1 = tc::smem_u32(&sm.mbar[3]), rdy2 = tc::smem_u32(&sm.mbar[4]);
   const uint32_t mbS = tc::smem_u32(&sm.mbar[5]);  // a sub-chunk's checkpoint has landed in S0s
   uint32_t ph = 0;  // every barrier completes once per sub-chunk
   bool ok = true;
