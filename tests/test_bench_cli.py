@@ -57,3 +57,16 @@ def test_reference_arm_under_two_ranks_prints_once():
     assert len(lines) == 1
     _check_reference_line(lines[0], "fixed_b1_t64_h2")
     assert lines[0]["n_gpus"] == 2
+
+
+def test_algorithmic_bytes():
+    """The roofline's compulsory bytes: per token 512 Hqk + 770 Hv forward (q, k, v, g, beta read,
+    o written) and 1024 Hqk + 1284 Hv backward (the same reads plus do, the five token gradients
+    written), 1536 Hqk + 2054 Hv together; per unit two 64 KiB states each way."""
+    sys.path.insert(0, ROOT)
+    import bench
+    ab = bench.algorithmic_bytes(8192, 96, 96, 768)
+    assert ab["fwd"] == 8192 * (512 * 96 + 770 * 96) + 768 * 2 * 65536 == 1_108_869_120
+    assert ab["bwd"] == 8192 * (1024 * 96 + 1284 * 96) + 768 * 2 * 65536 == 1_915_748_352
+    ab = bench.algorithmic_bytes(55_196, 8, 64, 1536)
+    assert ab["fwd"] + ab["bwd"] == 55_196 * (1536 * 8 + 2054 * 64) + 1536 * 262_144
