@@ -194,3 +194,22 @@ def test_workspace_bytes_rejects_absurd_sizes(lib, args):
     rc, _ = ws_bytes(lib, *args)
     assert rc == 2
     assert "too large" in lib.kda_last_error_message().decode()
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_is_plain_c_and_cxx(tmp_path, lang, std):
+    """include/kda.h compiles on its own as strict C99 and as C++11 (no torch or CUDA headers
+    needed by a caller), with every warning an error."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / "use_kda.c"
+    src.write_text('#include "kda.h"\n'
+                   "int main(void) { size_t b = 0; kda_status s = kda_ctx_workspace_bytes(1, 64, 2, 2, 0, 0, &b);\n"
+                   "  return (int)s + (int)(kda_status_string(s) == 0); }\n")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror"] + (["-pedantic"] if lang == "c" else [])
+                       + ["-I", inc, "-fsyntax-only", "-x", lang, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
