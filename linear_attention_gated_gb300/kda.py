@@ -168,7 +168,10 @@ class KdaContext:
 def kda_fwd(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens=None, scale=None,
             lower_bound=-5.0, out=None, final_state_out=None, context_out=None, *,
             cu_seqlens_cpu=None):
-    """Training forward. Returns (o BF16 [B,T,Hv,128], final_state FP32 [N,Hv,128,128], ctx)."""
+    """Training forward (flashinfer.kda_training.recurrent_kda_training_forward, parameters; the
+    recurrence of flashinfer.kda_backward.recurrent_kda_backward, description). Returns
+    (o BF16 [B,T,Hv,128], final_state FP32 [N,Hv,128,128], ctx); ctx holds the state checkpoints
+    and tapes the backward consumes (flashinfer.kda_training, module description)."""
     lib = load_library()
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v, g must be [B, T, H, 128]")
@@ -228,7 +231,11 @@ GRAD_NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dA_log", "ddt_bias", "dinitial_s
 
 
 def kda_bwd(ctx: KdaContext, do, dfinal_state, out=None):
-    """Training backward. Returns (dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dinitial_state)."""
+    """Training backward from a saved context, without rerunning the forward
+    (flashinfer.kda_training.recurrent_kda_training_backward; gradient list and order of
+    flashinfer.kda_backward.recurrent_kda_backward, description). Returns
+    (dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dinitial_state); dg and dbeta are with respect to
+    the raw gate and the raw beta logits."""
     lib = load_library()
     if not isinstance(ctx, KdaContext) or not ctx.handle.value:
         raise KdaError(4, "not a forward context")
@@ -260,7 +267,9 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_
                     cu_seqlens=None, scale=None, lower_bound=-5.0, out=None, *, cu_seqlens_cpu=None):
     """Standalone backward that allocates no device memory in the library (for
     callers that cannot call cudaMalloc; scratch is a fixed array compiled into
-    libkda.so). Returns the eight gradients of kda_bwd. ``out`` (eight tensors in
+    libkda.so). The pages have no counterpart for this entry point; it computes
+    what recurrent_kda_training_forward followed by _backward computes
+    (flashinfer.kda_training). Returns the eight gradients of kda_bwd. ``out`` (eight tensors in
     return order) lets the caller own every output buffer as well."""
     lib = load_library()
     B, T, Hqk, D = q.shape
@@ -297,7 +306,8 @@ def _want_gate_params(A_log, dt_bias, Hv, K, use_gate_in_kernel):
 
 def kda_decode(q, k, v, g, beta, A_log, dt_bias, state, state_indices=None, scale=None, lower_bound=-5.0,
                out=None, use_gate_in_kernel=False, beta_is_logit=False, *, state_indices_cpu=None):
-    """One decode step (T = 1): updates ``state`` in place and returns o.
+    """One decode step (T = 1; flashinfer.kda.recurrent_kda, description and parameters q,
+    initial_state, ssm_state_indices): updates ``state`` in place and returns o.
 
     q, k [N, 1, Hqk, 128] and v, g [N, 1, Hv, 128] BF16, beta [N, 1, Hv] BF16,
     A_log [Hv] and dt_bias [Hv, 128] FP32 (None allowed unless
@@ -360,7 +370,9 @@ def kda_prefill(q, k, v, g, beta, A_log, dt_bias, state, cu_seqlens=None, state_
                 checkpoint_cu_starts=None, checkpoint_every_n_tokens=0, scale=None, lower_bound=-5.0, out=None,
                 device_status=None, use_gate_in_kernel=False, beta_is_logit=False, *, cu_seqlens_cpu=None,
                 state_indices_cpu=None, checkpoint_cu_starts_cpu=None):
-    """Inference prefill from a state pool: returns o; the final state of every
+    """Inference prefill from a state pool (flashinfer.kda.recurrent_kda, parameters
+    initial_state, ssm_state_indices, state_checkpoints, checkpoint_cu_starts and
+    checkpoint_every_n_tokens): returns o; the final state of every
     sequence is written back to its slot of ``state`` (BF16 or FP32, [num_slots,
     Hv, 128, 128]); optional BF16 ``checkpoints`` [C, Hv, 128, 128] every
     ``checkpoint_every_n_tokens`` tokens, counted by the int64 device tensor
@@ -434,7 +446,8 @@ recurrent_kda_training_forward = kda_fwd
 
 
 class HostStep:
-    """Training steps from and to host memory through kda_step_host: owns one
+    """Training steps (flashinfer.kda_training forward and backward) from and to
+    host memory through kda_step_host: owns one
     device arena (kda_step_arena_bytes) and the context created in it. Each call
     enqueues the input copies on ``h2d_stream``, the forward and backward on
     ``stream`` and the output copies on ``d2h_stream`` (each defaults to a new
