@@ -41,6 +41,8 @@ WORKLOAD = "packed_8x1024_h96"
 METRIC = "KDA fwd+bwd token·heads/s (1 GB300) and fraction of roofline"
 UNIT = "token·heads/s"
 DIM = 128
+# operand type of the tensor-core products (FP32 accumulation; the state and its adjoint are FP32)
+MMA_KIND = "tf32"
 
 
 def algorithmic_bytes(total_tokens, hqk, hv, units):
@@ -346,7 +348,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
             "config": {"workload": args.workload, "sequences": N, "tokens": Ttot, "Hqk": w.hqk, "Hv": w.hv,
                        "head_dim": DIM, "token_heads_per_gpu": token_heads, "io_dtype": "bf16",
-                       "state_dtype": "fp32", "l2": f"a forward moves {ab['fwd'] / 1e6:.0f} MB and a backward "
+                       "state_dtype": "fp32", "mma": MMA_KIND, "l2": f"a forward moves {ab['fwd'] / 1e6:.0f} MB and a backward "
                        f"{ab['bwd'] / 1e6:.0f} MB, each > 129 MB of L2 (largest token tensor "
                        f"{d['v'].numel() * 2 / 1e6:.0f} MB), no flush",
                        "parallelism": f"replicas x{world}"},

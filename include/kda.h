@@ -146,6 +146,45 @@ const char* kda_status_string(kda_status status);
 const char* kda_last_error_message(void);
 
 /*
+ * Standalone backward with a caller-owned workspace
+ * (flashinfer.kda_backward.recurrent_kda_backward: signature, description and
+ * the parameters workspace and out). From the forward's inputs, the initial
+ * state and the two adjoints it returns the eight gradients of kda_bwd, in the
+ * same order, into caller-owned buffers: it runs the training forward into the
+ * workspace (the checkpoints, and the output and final state, which it does
+ * not return) and then the backward.
+ * Bytes: kda_bwd_standalone_workspace_bytes() (same shape arguments and errors
+ * as kda_ctx_workspace_bytes): a context workspace followed by room for o and
+ * the final state.
+ * Inputs: those of kda_fwd (same layouts, rules and head mapping) and of
+ *   kda_bwd (d_o BF16 [B, T, Hv, 128], d_hT FP32 [N, Hv, 128, 128]).
+ * Outputs: dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0 as for kda_bwd.
+ * workspace / workspace_bytes: device memory, 256-byte aligned, owned by the
+ *   caller; no input or output may overlap it.
+ * ws_ctx: a host handle bound to the workspace, like kda_fwd's ctx. Pass a
+ *   pointer to NULL on the first call (it uploads the launch plan, built from
+ *   cu_seqlens_host, into the workspace: the "eager warm-up" of the page);
+ *   later calls with the same handle, shapes, workspace, device and stream only
+ *   launch kernels and may be captured into a CUDA graph (a replay reads the
+ *   buffers the captured pointers name). Free it with kda_ctx_destroy.
+ * Errors: those of kda_fwd and kda_bwd; KDA_ERR_WORKSPACE_TOO_SMALL;
+ *   KDA_ERR_ALIASING when an adjoint or gradient overlaps the workspace.
+ *   Device-side timeouts are reported by kda_ctx_status(*ws_ctx).
+ * Nothing is allocated on the device.
+ */
+kda_status kda_bwd_standalone_workspace_bytes(int64_t B, int64_t T, int64_t Hqk, int64_t Hv,
+                                              const int64_t* cu_seqlens_host, int64_t num_seqs,
+                                              size_t* bytes);
+kda_status kda_bwd_standalone(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                              const kda_bf16* beta, const float* A_log, const float* dt_bias, const float* h0,
+                              const int64_t* cu_seqlens_dev, const int64_t* cu_seqlens_host, int64_t num_seqs,
+                              int64_t B, int64_t T, int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
+                              float lower_bound, const kda_bf16* d_o, const float* d_hT, kda_bf16* dq,
+                              kda_bf16* dk, kda_bf16* dv, kda_bf16* dg, kda_bf16* dbeta, float* dA_log,
+                              float* ddt_bias, float* dh0, void* workspace, size_t workspace_bytes,
+                              kda_ctx** ws_ctx, struct CUstream_st* stream);
+
+/*
  * Standalone backward that allocates nothing. The documentation pages have no
  * counterpart for this entry point; it exists for callers that cannot call
  * cudaMalloc: code running while another component owns all device memory
@@ -168,10 +207,15 @@ const char* kda_last_error_message(void);
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture. Every call shares the one array and leaves its contents
- * behind; nothing in it needs to start at zero. Calls whose work overlaps on the
- * GPU (different streams, or several host threads) race on the array: serialise
- * them. Units run in index order. Nothing is allocated: no cudaMalloc, cudaFree
- * or allocating library routine is called.
+ * behind; the only part that must start at zero, a status word at the start of
+ * the array, is cleared by each call before its first launch. Calls whose work
+ * overlaps on the GPU (different streams, or several host threads) race on the
+ * array: serialise them. Units run in index order; the per-sequence plan is
+ * built on the device from cu_seqlens_dev and checked against what the host
+ * mirror implies (start 0, end T, non-empty sequences, the same checkpoint
+ * totals), so a device copy that disagrees never sends a kernel outside its
+ * buffers: it is reported by kda_noalloc_status instead. Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine is called.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
@@ -183,6 +227,14 @@ kda_status kda_bwd_noalloc(const kda_bf16* q, const kda_bf16* k, const kda_bf16*
                            kda_bf16* dq, kda_bf16* dk, kda_bf16* dv, kda_bf16* dg,
                            kda_bf16* dbeta, float* dA_log, float* ddt_bias, float* dh0,
                            struct CUstream_st* stream);
+
+/* Reads back the status word of the last kda_bwd_noalloc call on the current
+ * device, after synchronising `stream` (the stream that call used). Returns
+ * KDA_OK; KDA_ERR_INVALID_ARGUMENT when the device cu_seqlens disagreed with
+ * its host mirror (the gradients are then not meaningful); KDA_ERR_DEVICE_TIMEOUT
+ * when a bounded device wait gave up (some gradients were not written);
+ * KDA_ERR_CUDA on a CUDA error. Allocates nothing. */
+kda_status kda_noalloc_status(struct CUstream_st* stream);
 
 /* State element types for kda_decode. */
 enum { KDA_STATE_BF16 = 0, KDA_STATE_FP32 = 1 };

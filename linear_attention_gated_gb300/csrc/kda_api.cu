@@ -14,6 +14,7 @@
 #include "../../include/kda.h"
 #include "kda_common.cuh"
 #include "kda_host.h"
+#include "kda_layout.h"
 #include "tc.cuh"
 
 using kda::SeqInfo;
@@ -36,8 +37,7 @@ kda_status cuda_fail(cudaError_t e, const char* where) {
   return fail(KDA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
-constexpr size_t kAlign = 256;
-size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+constexpr size_t kAlign = kda::kCtxAlign;
 
 struct Shape {
   int64_t B = 0, T = 0, Hqk = 0, Hv = 0, N = 0, Ttot = 0, units = 0, n_ck = 0, n_ch = 0;
@@ -48,24 +48,12 @@ struct Shape {
   }
 };
 
-struct Layout {
-  size_t order = 0, seq = 0, ckpt = 0, utape = 0, abtape = 0, dqk = 0, par = 0, status = 0, total = 0;
-};
+using Layout = kda::CtxLayout;
 
 Layout make_layout(const Shape& s) {
-  Layout L;
-  size_t off = 0;
-  L.order = off; off = align_up(off + sizeof(int32_t) * s.units);
-  L.seq = off;   off = align_up(off + sizeof(SeqInfo) * s.N);
-  L.ckpt = off;  off = align_up(off + sizeof(float) * (size_t)s.n_ck * s.Hv * kda::kDim * kda::kDim);
-  L.utape = off; off = align_up(off + sizeof(float) * (size_t)s.Ttot * s.Hv * kda::kDim);
-  L.abtape = off; off = align_up(off + sizeof(float) * (size_t)s.n_ch * s.Hv * 2 * kda::kChunk * kda::kChunk);
-  L.dqk = off;
-  if (s.Hv != s.Hqk) off = align_up(off + sizeof(float) * (size_t)s.Ttot * s.Hv * 2 * kda::kDim);
-  L.par = off;   off = align_up(off + sizeof(float) * (size_t)s.units * kda::kParStride);
-  L.status = off; off = align_up(off + 16);
-  L.total = off;
-  return L;
+  kda::CtxCounts c;
+  c.N = s.N; c.Ttot = s.Ttot; c.Hqk = s.Hqk; c.Hv = s.Hv; c.n_ck = s.n_ck; c.n_ch = s.n_ch;
+  return kda::context_layout(c);
 }
 
 // Validates sizes and the host cu_seqlens mirror; fills the Shape.
@@ -106,8 +94,8 @@ kda_status make_shape(int64_t B, int64_t T, int64_t Hqk, int64_t Hv, const int64
   s.n_ck = 0;
   s.n_ch = 0;
   for (int64_t i = 0; i < s.N; ++i) {
-    s.n_ck += (s.cu[i + 1] - s.cu[i] + kda::kCkTokens - 1) / kda::kCkTokens;
-    s.n_ch += (s.cu[i + 1] - s.cu[i] + kda::kChunk - 1) / kda::kChunk;
+    s.n_ck += kda::checkpoints_of(s.cu[i + 1] - s.cu[i]);
+    s.n_ch += kda::subchunks_of(s.cu[i + 1] - s.cu[i]);
   }
   *out = std::move(s);
   return KDA_OK;
@@ -330,8 +318,8 @@ kda_status kda_fwd(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, cons
         c->seq[i].len = s.cu[i + 1] - s.cu[i];
         c->seq[i].ck_base = ck;
         c->seq[i].ch_base = chn;
-        ck += (c->seq[i].len + kda::kCkTokens - 1) / kda::kCkTokens;
-        chn += (c->seq[i].len + kda::kChunk - 1) / kda::kChunk;
+        ck += kda::checkpoints_of(c->seq[i].len);
+        chn += kda::subchunks_of(c->seq[i].len);
       }
     } else {
       if (!(c->shape == s)) return fail(KDA_ERR_CONTEXT, "context was created for a different shape");
@@ -447,5 +435,86 @@ kda_status kda_ctx_status(kda_ctx* c) {
 }
 
 void kda_ctx_destroy(kda_ctx* c) { delete c; }
+
+namespace {
+
+// kda_bwd_standalone's workspace: the context workspace of kda_fwd, then the
+// forward's output o and final state, which the backward does not return.
+struct StandaloneLayout {
+  size_t ctx_bytes = 0, o = 0, h_T = 0, total = 0;
+};
+
+kda_status standalone_layout(int64_t B, int64_t T, int64_t Hqk, int64_t Hv, const int64_t* cu_host,
+                             int64_t num_seqs, StandaloneLayout* L) {
+  Shape s;
+  kda_status st = make_shape(B, T, Hqk, Hv, cu_host, num_seqs, &s);
+  if (st != KDA_OK) return st;
+  L->ctx_bytes = make_layout(s).total;
+  L->o = L->ctx_bytes;
+  L->h_T = kda::ctx_align_up(L->o + sizeof(kda_bf16) * (size_t)s.Ttot * Hv * kda::kDim);
+  L->total = kda::ctx_align_up(L->h_T + sizeof(float) * (size_t)s.N * Hv * kda::kDim * kda::kDim);
+  return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_bwd_standalone_workspace_bytes(int64_t B, int64_t T, int64_t Hqk, int64_t Hv,
+                                              const int64_t* cu_seqlens_host, int64_t num_seqs,
+                                              size_t* bytes) {
+  return kda::guarded([&]() -> kda_status {
+    g_last_error.clear();
+    if (!bytes) return fail(KDA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    StandaloneLayout L;
+    kda_status st = standalone_layout(B, T, Hqk, Hv, cu_seqlens_host, num_seqs, &L);
+    if (st != KDA_OK) return st;
+    *bytes = L.total;
+    return KDA_OK;
+  });
+}
+
+kda_status kda_bwd_standalone(const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g,
+                              const kda_bf16* beta, const float* A_log, const float* dt_bias, const float* h0,
+                              const int64_t* cu_seqlens_dev, const int64_t* cu_seqlens_host, int64_t num_seqs,
+                              int64_t B, int64_t T, int64_t Hqk, int64_t Hv, int64_t head_dim, float scale,
+                              float lower_bound, const kda_bf16* d_o, const float* d_hT, kda_bf16* dq,
+                              kda_bf16* dk, kda_bf16* dv, kda_bf16* dg, kda_bf16* dbeta, float* dA_log,
+                              float* ddt_bias, float* dh0, void* workspace, size_t workspace_bytes,
+                              kda_ctx** ws_ctx, struct CUstream_st* stream) {
+  return kda::guarded([&]() -> kda_status {
+    g_last_error.clear();
+    if (!ws_ctx) return fail(KDA_ERR_INVALID_ARGUMENT, "ws_ctx is NULL");
+    if (!workspace) return fail(KDA_ERR_INVALID_ARGUMENT, "workspace is NULL");
+    if (!d_o || !d_hT || !dq || !dk || !dv || !dg || !dbeta || !dA_log || !ddt_bias || !dh0)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "a required tensor pointer is NULL");
+    if (head_dim != kda::kDim)
+      return fail(KDA_ERR_UNSUPPORTED, "head dimension must be 128 (got %lld)", (long long)head_dim);
+    StandaloneLayout L;
+    kda_status st = standalone_layout(B, T, Hqk, Hv, cu_seqlens_host, num_seqs, &L);
+    if (st != KDA_OK) return st;
+    if (workspace_bytes < L.total)
+      return fail(KDA_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", L.total, workspace_bytes);
+    if (((uintptr_t)workspace % kAlign) != 0)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+    // The forward writes the workspace before the backward reads the adjoints, and the
+    // backward writes the gradients while it reads the workspace: none may overlap it.
+    const int64_t N = cu_seqlens_host ? num_seqs : B;
+    const size_t Ttot = (size_t)B * T;
+    const size_t tok_qk = sizeof(kda_bf16) * Ttot * Hqk * kda::kDim, tok_v = sizeof(kda_bf16) * Ttot * Hv * kda::kDim;
+    const size_t state = sizeof(float) * (size_t)N * Hv * kda::kDim * kda::kDim;
+    const Range ws{workspace, workspace_bytes, "workspace"};
+    const Range others[] = {{d_o, tok_v, "do"}, {d_hT, state, "dfinal_state"}, {dq, tok_qk, "dq"},
+                            {dk, tok_qk, "dk"}, {dv, tok_v, "dv"}, {dg, tok_v, "dg"},
+                            {dbeta, sizeof(kda_bf16) * Ttot * Hv, "dbeta"}, {dA_log, sizeof(float) * Hv, "dA_log"},
+                            {ddt_bias, sizeof(float) * Hv * kda::kDim, "ddt_bias"}, {dh0, state, "dinitial_state"}};
+    for (const Range& r : others)
+      if (overlaps(ws, r)) return fail(KDA_ERR_ALIASING, "%s overlaps the workspace", r.name);
+    char* base = static_cast<char*>(workspace);
+    st = kda_fwd(q, k, v, g, beta, A_log, dt_bias, h0, cu_seqlens_dev, cu_seqlens_host, num_seqs, B, T, Hqk, Hv,
+                 head_dim, scale, lower_bound, reinterpret_cast<kda_bf16*>(base + L.o),
+                 reinterpret_cast<float*>(base + L.h_T), base, L.ctx_bytes, ws_ctx, stream);
+    if (st != KDA_OK) return st;
+    return kda_bwd(*ws_ctx, d_o, d_hT, dq, dk, dv, dg, dbeta, dA_log, ddt_bias, dh0, stream);
+  });
+}
 
 }  // extern "C"

@@ -808,7 +808,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         pp[kDim] = acc;
       }
     } else if (tid == 0) {
-      atomicExch(P.status, 1);
+      atomicOr(P.status, 1);
     }
   }
   tc::fence_before();

@@ -14,8 +14,10 @@
 // It runs the same forward kernel (to rebuild the state checkpoints; its output
 // and final state land in the scratch and are discarded) and the same backward
 // and reduction kernels as kda_fwd + kda_bwd, with every intermediate buffer
-// carved out of the scratch array. Units run in index order (no host-side plan
-// upload: a one-thread kernel writes the plan into the scratch).
+// carved out of the scratch array in the context layout kda_fwd uses. Units run
+// in index order (no host-side plan upload: a one-thread kernel writes the plan
+// into the scratch). The first 256 bytes of the array hold the status word that
+// kda_noalloc_status reads; each call clears it before its first launch.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -24,11 +26,12 @@
 #include "../../include/kda.h"
 #include "kda_common.cuh"
 #include "kda_host.h"
+#include "kda_layout.h"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = KDA_NOALLOC_SCRATCH_BYTES;  // 64 MiB
-constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = kda::kCtxAlign;                     // status word, then the context
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -43,7 +46,7 @@ kda_status nfail(kda_status st, const char* fmt, ...) {
   return st;
 }
 
-size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+size_t up(size_t x) { return kda::ctx_align_up(x); }
 
 // Device address of the scratch array on the current device, looked up once
 // per device (the host-side symbol is only a stand-in for it).
@@ -64,29 +67,61 @@ kda_status scratch_for_device(int dev, void** out) {
   return KDA_OK;
 }
 
-// Plan written on the device: identity unit order and per-sequence offsets.
-__global__ void kda_noalloc_plan_kernel(const int64_t* cu, int64_t N, int64_t Hv, int64_t ck_tokens,
-                                        int32_t* order, kda::SeqInfo* seq) {
+kda_status current_sm103(int* dev_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  int major = 0, minor = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+    return nfail(KDA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  if (major != 10 || minor != 3)
+    return nfail(KDA_ERR_UNSUPPORTED, "kernels are built for sm_103a; device %d is compute capability %d.%d", dev,
+                 major, minor);
+  *dev_out = dev;
+  return KDA_OK;
+}
+
+// Plan written on the device: identity unit order and per-sequence offsets, from
+// the device cu_seqlens (null: B sequences of T tokens). The scratch was sized
+// from the host mirror, so the device copy is checked against what that sizing
+// relied on: it starts at 0, every sequence is non-empty, it ends at B * T and
+// it gives the same checkpoint and sub-chunk totals. Then every token, checkpoint
+// and sub-chunk index the kernels form stays inside its buffer. A copy that
+// fails the check sets bit 2 (value 4) of the status word, and every sequence
+// becomes the first token with base 0, which keeps all accesses in bounds (the
+// gradients are then meaningless; kda_noalloc_status reports the error).
+__global__ void kda_noalloc_plan_kernel(const int64_t* cu, int64_t B, int64_t T, int64_t N, int64_t Hv,
+                                        int64_t n_ck, int64_t n_ch, int32_t* order, kda::SeqInfo* seq,
+                                        int32_t* status) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
+    bool ok = cu == nullptr || cu[0] == 0;
     int64_t ck = 0, chn = 0;
-    for (int64_t n = 0; n < N; ++n) {
-      const int64_t len = cu[n + 1] - cu[n];
-      seq[n].t0 = cu[n];
+    for (int64_t n = 0; n < N && ok; ++n) {
+      const int64_t t0 = cu ? cu[n] : n * T;
+      const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - t0;
+      ok = len >= 1 && len <= B * T;
+      seq[n].t0 = t0;
       seq[n].len = len;
       seq[n].ck_base = ck;
       seq[n].ch_base = chn;
-      ck += (len + ck_tokens - 1) / ck_tokens;
-      chn += (len + kda::kChunk - 1) / kda::kChunk;
+      ck += kda::checkpoints_of(len);
+      chn += kda::subchunks_of(len);
+    }
+    ok = ok && (cu == nullptr || cu[N] == B * T) && ck == n_ck && chn == n_ch;
+    if (!ok) {
+      for (int64_t n = 0; n < N; ++n) {
+        seq[n].t0 = 0;
+        seq[n].len = 1;
+        seq[n].ck_base = 0;
+        seq[n].ch_base = 0;
+      }
+      atomicOr(status, 4);
     }
   }
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < N * Hv;
        u += (int64_t)gridDim.x * blockDim.x)
     order[u] = (int32_t)u;
-}
-
-__global__ void kda_noalloc_fixed_cu_kernel(int64_t* cu, int64_t B, int64_t T) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i <= B) cu[i] = i * T;
 }
 
 struct Range {
@@ -137,12 +172,12 @@ extern "C" kda_status kda_bwd_noalloc(
       for (int64_t i = 0; i < N; ++i) {
         const int64_t len = cu_seqlens_host[i + 1] - cu_seqlens_host[i];
         if (len < 1) return nfail(KDA_ERR_INVALID_ARGUMENT, "sequence %lld is empty", (long long)i);
-        n_ck += (len + kda::kCkTokens - 1) / kda::kCkTokens;
-        n_ch += (len + kda::kChunk - 1) / kda::kChunk;
+        n_ck += kda::checkpoints_of(len);
+        n_ch += kda::subchunks_of(len);
       }
     } else {
-      n_ck = B * ((T + kda::kCkTokens - 1) / kda::kCkTokens);
-      n_ch = B * ((T + kda::kChunk - 1) / kda::kChunk);
+      n_ck = B * kda::checkpoints_of(T);
+      n_ch = B * kda::subchunks_of(T);
     }
     const void* vec_ptrs[] = {q, k, v, g, h0, d_o, d_hT, dq, dk, dv, dg, dh0};
     for (const void* p : vec_ptrs)
@@ -150,19 +185,14 @@ extern "C" kda_status kda_bwd_noalloc(
 
     const int64_t Ttot = B * T, units = N * Hv, r = Hv / Hqk;
     const size_t D = kda::kDim;
-    // scratch layout
-    size_t off = 0;
-    const size_t o_order = off; off = up(off + sizeof(int32_t) * units);
-    const size_t o_seq = off;   off = up(off + sizeof(kda::SeqInfo) * N);
-    const size_t o_cu = off;    off = up(off + sizeof(int64_t) * (N + 1));
-    const size_t o_ck = off;    off = up(off + sizeof(float) * (size_t)n_ck * Hv * D * D);
-    const size_t o_ut = off;    off = up(off + sizeof(float) * (size_t)Ttot * Hv * D);
-    const size_t o_ab = off;    off = up(off + sizeof(float) * (size_t)n_ch * Hv * 2 * kda::kChunk * kda::kChunk);
-    const size_t o_dqk = off;   if (r > 1) off = up(off + sizeof(float) * (size_t)Ttot * Hv * 2 * D);
-    const size_t o_par = off;   off = up(off + sizeof(float) * (size_t)units * kda::kParStride);
+    // scratch layout: the status word, the context of kda_fwd, the forward's o and final state
+    kda::CtxCounts cc;
+    cc.N = N; cc.Ttot = Ttot; cc.Hqk = Hqk; cc.Hv = Hv; cc.n_ck = n_ck; cc.n_ch = n_ch;
+    const kda::CtxLayout L = kda::context_layout(cc);
+    size_t off = kStatusBytes;
+    const size_t o_ctx = off;   off = up(off + L.total);
     const size_t o_o = off;     off = up(off + sizeof(kda_bf16) * (size_t)Ttot * Hv * D);
     const size_t o_hT = off;    off = up(off + sizeof(float) * (size_t)N * Hv * D * D);
-    const size_t o_status = off; off = up(off + 16);
     if (off > kNoAllocScratchBytes)
       return nfail(KDA_ERR_WORKSPACE_TOO_SMALL,
                    "problem needs %zu bytes of scratch; kda_bwd_noalloc has %zu (use kda_fwd + kda_bwd)",
@@ -186,26 +216,20 @@ extern "C" kda_status kda_bwd_noalloc(
     }
 
     int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    if (major != 10 || minor != 3) return nfail(KDA_ERR_UNSUPPORTED, "kernels are built for sm_103a");
+    kda_status st = current_sm103(&dev);
+    if (st != KDA_OK) return st;
     void* base = nullptr;
-    kda_status st = scratch_for_device(dev, &base);
+    st = scratch_for_device(dev, &base);
     if (st != KDA_OK) return st;
     char* sc = static_cast<char*>(base);
+    char* cx = sc + o_ctx;
+    int32_t* status = reinterpret_cast<int32_t*>(sc);
 
-    int64_t* cu = reinterpret_cast<int64_t*>(sc + o_cu);
-    const int64_t* cu_src = cu_seqlens_dev;
-    if (!cu_seqlens_dev) {
-      kda_noalloc_fixed_cu_kernel<<<(unsigned)((B + 1 + 255) / 256), 256, 0, stream>>>(cu, B, T);
-      cu_src = cu;
-    }
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
     kda_noalloc_plan_kernel<<<(unsigned)((units + 255) / 256), 256, 0, stream>>>(
-        cu_src, N, Hv, kda::kCkTokens, reinterpret_cast<int32_t*>(sc + o_order),
-        reinterpret_cast<kda::SeqInfo*>(sc + o_seq));
+        cu_seqlens_dev, B, T, N, Hv, n_ck, n_ch, reinterpret_cast<int32_t*>(cx + L.order),
+        reinterpret_cast<kda::SeqInfo*>(cx + L.seq), status);
     if ((e = cudaGetLastError()) != cudaSuccess) return nfail(KDA_ERR_CUDA, "plan launch: %s", cudaGetErrorString(e));
 
     kda::Problem P{};
@@ -217,12 +241,12 @@ extern "C" kda_status kda_bwd_noalloc(
     P.A_log = A_log;
     P.dt_bias = dt_bias;
     P.h0 = h0;
-    P.order = reinterpret_cast<const int32_t*>(sc + o_order);
-    P.seq = reinterpret_cast<const kda::SeqInfo*>(sc + o_seq);
-    P.ckpt = reinterpret_cast<float*>(sc + o_ck);
-    P.status = reinterpret_cast<int32_t*>(sc + o_status);
-    P.utape = reinterpret_cast<float*>(sc + o_ut);
-    P.abtape = reinterpret_cast<float*>(sc + o_ab);
+    P.order = reinterpret_cast<const int32_t*>(cx + L.order);
+    P.seq = reinterpret_cast<const kda::SeqInfo*>(cx + L.seq);
+    P.ckpt = reinterpret_cast<float*>(cx + L.ckpt);
+    P.status = status;
+    P.utape = reinterpret_cast<float*>(cx + L.utape);
+    P.abtape = reinterpret_cast<float*>(cx + L.abtape);
     P.N = N;
     P.Hqk = Hqk;
     P.Hv = Hv;
@@ -241,11 +265,32 @@ extern "C" kda_status kda_bwd_noalloc(
     a.dg = reinterpret_cast<__nv_bfloat16*>(dg);
     a.dbeta = reinterpret_cast<__nv_bfloat16*>(dbeta);
     a.dh0 = dh0;
-    a.dqk_part = reinterpret_cast<float*>(sc + o_dqk);
-    a.par_part = reinterpret_cast<float*>(sc + o_par);
+    a.dqk_part = reinterpret_cast<float*>(cx + L.dqk);
+    a.par_part = reinterpret_cast<float*>(cx + L.par);
     if ((e = kda::launch_backward(P, a, units, Ttot, dA_log, ddt_bias, stream)) != cudaSuccess)
       return nfail(KDA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return KDA_OK;
   });
 }
 
+extern "C" kda_status kda_noalloc_status(struct CUstream_st* stream_) {
+  return kda::guarded([&]() -> kda_status {
+    kda::set_last_error("");
+    int dev = -1;
+    kda_status st = current_sm103(&dev);
+    if (st != KDA_OK) return st;
+    void* base = nullptr;
+    if ((st = scratch_for_device(dev, &base)) != KDA_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    int32_t word = 0;
+    e = cudaMemcpy(&word, base, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return nfail(KDA_ERR_CUDA, "status readback: %s", cudaGetErrorString(e));
+    if (word & 4)
+      return nfail(KDA_ERR_INVALID_ARGUMENT, "the device cu_seqlens disagreed with its host mirror (status %d)", word);
+    if (word & 1) return nfail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (status %d)", word);
+    if (word != 0) return nfail(KDA_ERR_CUDA, "unexpected device status %d", word);
+    return KDA_OK;
+  });
+}

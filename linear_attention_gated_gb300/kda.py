@@ -31,7 +31,8 @@ _STATUS = {
 EXPORTED = ("kda_ctx_workspace_bytes", "kda_fwd", "kda_bwd", "kda_ctx_status", "kda_ctx_destroy",
             "kda_status_string", "kda_last_error_message", "kda_chunk_tokens",
             "kda_checkpoint_tokens", "kda_bwd_noalloc", "kda_decode", "kda_prefill",
-            "kda_selftest_device_timeout", "kda_step_arena_bytes", "kda_step_host")
+            "kda_selftest_device_timeout", "kda_step_arena_bytes", "kda_step_host",
+            "kda_bwd_standalone_workspace_bytes", "kda_bwd_standalone", "kda_noalloc_status")
 
 
 class KdaError(RuntimeError):
@@ -74,6 +75,13 @@ def load_library(path: str = LIB_PATH):
     lib.kda_last_error_message.restype = ctypes.c_char_p
     lib.kda_bwd_noalloc.argtypes = [P] * 8 + [P, P, I, I, I, I, I, I, F, F] + [P] * 10 + [P]
     lib.kda_bwd_noalloc.restype = ctypes.c_int
+    lib.kda_noalloc_status.argtypes = [P]
+    lib.kda_noalloc_status.restype = ctypes.c_int
+    lib.kda_bwd_standalone_workspace_bytes.argtypes = [I, I, I, I, P, I, ctypes.POINTER(S)]
+    lib.kda_bwd_standalone_workspace_bytes.restype = ctypes.c_int
+    lib.kda_bwd_standalone.argtypes = ([P] * 8 + [P, P, I, I, I, I, I, I, F, F] + [P] * 10
+                                       + [P, S, ctypes.POINTER(P), P])
+    lib.kda_bwd_standalone.restype = ctypes.c_int
     lib.kda_decode.argtypes = [P] * 8 + [ctypes.c_int32, P, P, I, I, I, I, I, F, F, ctypes.c_int32,
                                          ctypes.c_int32, P, P]
     lib.kda_decode.restype = ctypes.c_int
@@ -165,16 +173,12 @@ class KdaContext:
             pass
 
 
-def kda_fwd(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens=None, scale=None,
-            lower_bound=-5.0, out=None, final_state_out=None, context_out=None, *,
-            cu_seqlens_cpu=None):
-    """Training forward (flashinfer.kda_training.recurrent_kda_training_forward, parameters; the
-    recurrence of flashinfer.kda_backward.recurrent_kda_backward, description). Returns
-    (o BF16 [B,T,Hv,128], final_state FP32 [N,Hv,128,128], ctx); ctx holds the state checkpoints
-    and tapes the backward consumes (flashinfer.kda_training, module description)."""
-    lib = load_library()
-    if q.dim() != 4 or v.dim() != 4:
-        raise ValueError("q, k, v, g must be [B, T, H, 128]")
+def _check_forward_inputs(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens, cu_seqlens_cpu):
+    """Dtype, shape, contiguity and device checks of the forward's inputs (the C ABI
+    repeats the shape rules on the host). Returns (B, T, Hqk, Hv, D, N)."""
+    for name, t in (("q", q), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError(f"{name} must be a [B, T, H, 128] tensor")
     B, T, Hqk, D = q.shape
     Hv = v.shape[2]
     bf, f32 = torch.bfloat16, torch.float32
@@ -183,10 +187,16 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens=None, sc
     _want(A_log, "A_log", f32, (Hv,)); _want(dt_bias, "dt_bias", f32, (Hv, D))
     if q.device.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
+    for name, t in (("k", k), ("v", v), ("g", g), ("beta", beta), ("A_log", A_log), ("dt_bias", dt_bias),
+                    ("initial_state", initial_state)):
+        if t.device != q.device:
+            raise ValueError(f"{name} must be on {q.device}")
     if cu_seqlens is not None:
         if cu_seqlens_cpu is None:
             raise ValueError("packed input requires cu_seqlens_cpu, a trusted CPU mirror of cu_seqlens")
         _want(cu_seqlens, "cu_seqlens", torch.int64)
+        if cu_seqlens.dim() != 1 or cu_seqlens.device != q.device:
+            raise ValueError(f"cu_seqlens must be a 1-D tensor on {q.device}")
         _want(cu_seqlens_cpu, "cu_seqlens_cpu", torch.int64, cu_seqlens.shape)
         if cu_seqlens_cpu.device.type != "cpu":
             raise ValueError("cu_seqlens_cpu must be a CPU tensor")
@@ -196,6 +206,20 @@ def kda_fwd(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens=None, sc
             raise ValueError("cu_seqlens_cpu must be omitted for fixed-length input")
         N = B
     _want(initial_state, "initial_state", f32, (N, Hv, D, D))
+    return B, T, Hqk, Hv, D, N
+
+
+def kda_fwd(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens=None, scale=None,
+            lower_bound=-5.0, out=None, final_state_out=None, context_out=None, *,
+            cu_seqlens_cpu=None):
+    """Training forward (flashinfer.kda_training.recurrent_kda_training_forward, parameters; the
+    recurrence of flashinfer.kda_backward.recurrent_kda_backward, description). Returns
+    (o BF16 [B,T,Hv,128], final_state FP32 [N,Hv,128,128], ctx); ctx holds the state checkpoints
+    and tapes the backward consumes (flashinfer.kda_training, module description)."""
+    lib = load_library()
+    B, T, Hqk, Hv, D, N = _check_forward_inputs(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens,
+                                                cu_seqlens_cpu)
+    bf, f32 = torch.bfloat16, torch.float32
     dev = q.device
     o = out if out is not None else torch.empty((B, T, Hv, D), dtype=bf, device=dev)
     hT = final_state_out if final_state_out is not None else torch.empty((N, Hv, D, D), dtype=f32, device=dev)
@@ -263,6 +287,26 @@ def kda_bwd(ctx: KdaContext, do, dfinal_state, out=None):
     return tuple(out)
 
 
+def _grad_buffers(out, shapes, dev):
+    dtypes = (torch.bfloat16,) * 5 + (torch.float32,) * 3
+    if out is None:
+        out = tuple(torch.empty(s_, dtype=dt, device=dev) for s_, dt in zip(shapes, dtypes))
+    if len(out) != 8:
+        raise ValueError("out must hold eight gradient tensors in return order")
+    for t, name, s_, dt in zip(out, GRAD_NAMES, shapes, dtypes):
+        _want(t, name, dt, s_)
+        if t.device != dev:
+            raise ValueError(f"{name} must be on {dev}")
+    return tuple(out)
+
+
+def _check_adjoints(do, dfinal_state, B, T, Hv, D, N, dev):
+    _want(do, "do", torch.bfloat16, (B, T, Hv, D))
+    _want(dfinal_state, "dfinal_state", torch.float32, (N, Hv, D, D))
+    if do.device != dev or dfinal_state.device != dev:
+        raise ValueError(f"do and dfinal_state must be on {dev}")
+
+
 def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_state,
                     cu_seqlens=None, scale=None, lower_bound=-5.0, out=None, *, cu_seqlens_cpu=None):
     """Standalone backward that allocates no device memory in the library (for
@@ -270,31 +314,105 @@ def kda_bwd_noalloc(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_
     libkda.so). The pages have no counterpart for this entry point; it computes
     what recurrent_kda_training_forward followed by _backward computes
     (flashinfer.kda_training). Returns the eight gradients of kda_bwd. ``out`` (eight tensors in
-    return order) lets the caller own every output buffer as well."""
+    return order) lets the caller own every output buffer as well. ``noalloc_status()`` reads
+    back the call's device status word."""
     lib = load_library()
-    B, T, Hqk, D = q.shape
-    Hv = v.shape[2]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    if cu_seqlens is not None and cu_seqlens_cpu is None:
-        raise ValueError("packed input requires cu_seqlens_cpu, a trusted CPU mirror of cu_seqlens")
+    B, T, Hqk, Hv, D, N = _check_forward_inputs(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens,
+                                                cu_seqlens_cpu)
     dev = q.device
+    _check_adjoints(do, dfinal_state, B, T, Hv, D, N, dev)
     shapes = ((B, T, Hqk, D), (B, T, Hqk, D), (B, T, Hv, D), (B, T, Hv, D), (B, T, Hv), (Hv,), (Hv, D),
               (N, Hv, D, D))
-    dtypes = (torch.bfloat16,) * 5 + (torch.float32,) * 3
-    if out is None:
-        out = tuple(torch.empty(s_, dtype=dt, device=dev) for s_, dt in zip(shapes, dtypes))
-    for t, name, s_, dt in zip(out, GRAD_NAMES, shapes, dtypes):
-        _want(t, name, dt, s_)
-    stream = torch.cuda.current_stream(dev)
-    rc = lib.kda_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
-                             _ptr(initial_state), _ptr(cu_seqlens),
-                             _ptr(cu_seqlens_cpu) if cu_seqlens_cpu is not None else None,
-                             N if cu_seqlens is not None else 0, B, T, Hqk, Hv, D,
-                             float("nan") if scale is None else float(scale), float(lower_bound),
-                             _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out],
-                             ctypes.c_void_p(stream.cuda_stream))
+    out = _grad_buffers(out, shapes, dev)
+    with torch.cuda.device(dev):
+        rc = lib.kda_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                                 _ptr(initial_state), _ptr(cu_seqlens),
+                                 _ptr(cu_seqlens_cpu) if cu_seqlens_cpu is not None else None,
+                                 N if cu_seqlens is not None else 0, B, T, Hqk, Hv, D,
+                                 float("nan") if scale is None else float(scale), float(lower_bound),
+                                 _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out], _stream_handle(dev))
     _check(rc)
-    return tuple(out)
+    return out
+
+
+def noalloc_status(device=None):
+    """Synchronise the current stream of ``device`` and read back the status word of the
+    last kda_bwd_noalloc call there; raises KdaError on a device-side error."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(load_library().kda_noalloc_status(_stream_handle(dev)))
+
+
+class RecurrentKDABackwardWorkspace:
+    """Reusable scratch of ``recurrent_kda_backward`` (flashinfer.kda_backward.recurrent_kda_backward,
+    parameter ``workspace``): one device buffer of kda_bwd_standalone_workspace_bytes and the
+    handle bound to it. The first call that uses it (eager) uploads the launch plan, built from
+    the host copy of cu_seqlens, which the workspace keeps; later calls with the same shapes,
+    device and stream only launch kernels, so they can be captured into a CUDA graph."""
+
+    def __init__(self, B, T, Hqk, Hv, cu_seqlens_cpu=None, device=None):
+        lib = load_library()
+        self.dev = torch.device(device if device is not None else "cuda")
+        self.cu_cpu = None if cu_seqlens_cpu is None else cu_seqlens_cpu.to(torch.int64).contiguous().cpu()
+        n = ctypes.c_size_t(0)
+        _check(lib.kda_bwd_standalone_workspace_bytes(
+            B, T, Hqk, Hv, _ptr(self.cu_cpu), self.cu_cpu.numel() - 1 if self.cu_cpu is not None else 0,
+            ctypes.byref(n)))
+        self.buffer = torch.empty(int(n.value), dtype=torch.uint8, device=self.dev)
+        self.key = (B, T, Hqk, Hv, None if self.cu_cpu is None else tuple(self.cu_cpu.tolist()))
+        self.handle = ctypes.c_void_p(None)
+
+    def status(self):
+        _check(load_library().kda_ctx_status(self.handle))
+
+    def __del__(self):
+        try:
+            if self.handle and self.handle.value:
+                load_library().kda_ctx_destroy(self.handle)
+                self.handle = ctypes.c_void_p(None)
+        except Exception:
+            pass
+
+
+def recurrent_kda_backward(q, k, v, g, beta, A_log, dt_bias, initial_state, do, dfinal_state, cu_seqlens=None,
+                           scale=None, lower_bound=-5.0, workspace=None, out=None, *, cu_seqlens_cpu=None):
+    """All gradients of the recurrent KDA training recurrence from the forward's inputs, the
+    initial state and the adjoints (flashinfer.kda_backward.recurrent_kda_backward: signature,
+    description, parameters ``workspace`` and ``out``). Returns (dq, dk, dv, dg, dbeta, dA_log,
+    ddt_bias, dinitial_state). ``workspace`` (RecurrentKDABackwardWorkspace) and ``out`` (eight
+    tensors in return order) make every buffer caller-owned; with both, a call after the first
+    one only launches kernels (CUDA-graph capturable). Packed input: the host copy of
+    cu_seqlens comes from ``cu_seqlens_cpu``, else from the workspace, else from a copy of the
+    device tensor (which waits for the device)."""
+    lib = load_library()
+    if cu_seqlens is not None and cu_seqlens_cpu is None:
+        if workspace is not None and workspace.cu_cpu is not None:
+            cu_seqlens_cpu = workspace.cu_cpu
+        else:
+            cu_seqlens_cpu = cu_seqlens.cpu()
+    B, T, Hqk, Hv, D, N = _check_forward_inputs(q, k, v, g, beta, A_log, dt_bias, initial_state, cu_seqlens,
+                                                cu_seqlens_cpu)
+    dev = q.device
+    _check_adjoints(do, dfinal_state, B, T, Hv, D, N, dev)
+    shapes = ((B, T, Hqk, D), (B, T, Hqk, D), (B, T, Hv, D), (B, T, Hv, D), (B, T, Hv), (Hv,), (Hv, D),
+              (N, Hv, D, D))
+    out = _grad_buffers(out, shapes, dev)
+    if workspace is None:
+        workspace = RecurrentKDABackwardWorkspace(B, T, Hqk, Hv, cu_seqlens_cpu, device=dev)
+    key = (B, T, Hqk, Hv, None if cu_seqlens_cpu is None else tuple(cu_seqlens_cpu.tolist()))
+    if workspace.key != key or workspace.dev != dev:
+        raise KdaError(4, "the workspace was made for other shapes or another device")
+    ws = workspace.buffer
+    with torch.cuda.device(dev):
+        rc = lib.kda_bwd_standalone(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A_log), _ptr(dt_bias),
+                                    _ptr(initial_state), _ptr(cu_seqlens),
+                                    _ptr(cu_seqlens_cpu) if cu_seqlens_cpu is not None else None,
+                                    N if cu_seqlens is not None else 0, B, T, Hqk, Hv, D,
+                                    float("nan") if scale is None else float(scale), float(lower_bound),
+                                    _ptr(do), _ptr(dfinal_state), *[_ptr(t) for t in out], _ptr(ws), ws.numel(),
+                                    ctypes.byref(workspace.handle), _stream_handle(dev))
+    _check(rc)
+    return out
 
 
 def _want_gate_params(A_log, dt_bias, Hv, K, use_gate_in_kernel):

@@ -213,3 +213,48 @@ def test_header_is_plain_c_and_cxx(tmp_path, lang, std):
     r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror"] + (["-pedantic"] if lang == "c" else [])
                        + ["-I", inc, "-fsyntax-only", "-x", lang, str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_standalone_workspace_bytes_covers_context(lib):
+    out = ctypes.c_size_t()
+    assert lib.kda_bwd_standalone_workspace_bytes(2, 1024, 32, 32, None, 0, ctypes.byref(out)) == 0
+    rc, ctx = ws_bytes(lib, 2, 1024, 32, 32)
+    # the context workspace plus room for o (BF16 [2, 1024, 32, 128]) and the final state
+    assert out.value >= ctx + 2 * 2 * 1024 * 32 * 128 + 4 * 2 * 32 * 128 * 128
+    assert out.value % 256 == 0
+    assert lib.kda_bwd_standalone_workspace_bytes(1, 64, 3, 4, None, 0, ctypes.byref(out)) == 1
+
+
+def _standalone(lib, ws_bytes_delta=0, **override):
+    """kda_bwd_standalone with fake, well-separated, aligned device addresses."""
+    P = ctypes.c_void_p
+    base = 1 << 40
+    names = ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "h0", "do", "dhT", "dq", "dk", "dv", "dg",
+             "dbeta", "dA_log", "ddt_bias", "dh0", "ws"]
+    a = {n: base + i * (1 << 34) for i, n in enumerate(names)}
+    a.update(override)
+    need = ctypes.c_size_t()
+    assert lib.kda_bwd_standalone_workspace_bytes(1, 64, 2, 2, None, 0, ctypes.byref(need)) == 0
+    handle = P(None)
+    rc = lib.kda_bwd_standalone(*[P(a[n]) for n in names[:8]], None, None, 0, 1, 64, 2, 2, 128,
+                                float("nan"), -5.0, *[P(a[n]) for n in names[8:18]], P(a["ws"]),
+                                need.value + ws_bytes_delta, ctypes.byref(handle), None)
+    return rc, lib.kda_last_error_message().decode()
+
+
+def test_standalone_rejects_small_workspace(lib):
+    rc, msg = _standalone(lib, ws_bytes_delta=-256)
+    assert rc == 7 and "workspace" in msg
+
+
+def test_standalone_rejects_gradient_or_adjoint_in_workspace(lib):
+    ws = (1 << 40) + 18 * (1 << 34)
+    rc, msg = _standalone(lib, dk=ws + 4096)
+    assert rc == 3 and "dk" in msg
+    rc, msg = _standalone(lib, do=ws)
+    assert rc == 3 and "do" in msg
+
+
+def test_standalone_reaches_device_check_when_arguments_are_valid(lib):
+    rc, msg = _standalone(lib)
+    assert rc in (2, 5), msg
