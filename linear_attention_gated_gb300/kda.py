@@ -352,7 +352,10 @@ class RecurrentKDABackwardWorkspace:
 
     def __init__(self, B, T, Hqk, Hv, cu_seqlens_cpu=None, device=None):
         lib = load_library()
-        self.dev = torch.device(device if device is not None else "cuda")
+        dev = torch.device(device if device is not None else "cuda")
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.dev = dev
         self.cu_cpu = None if cu_seqlens_cpu is None else cu_seqlens_cpu.to(torch.int64).contiguous().cpu()
         n = ctypes.c_size_t(0)
         _check(lib.kda_bwd_standalone_workspace_bytes(
