@@ -23,7 +23,10 @@
 // operand), as well as the 16x16 A and B (an M = 64 product next to the first
 // contraction) and the output's B W term (next to the second); the next
 // sub-chunk's prologue runs while the second group is in flight. Token tiles
-// are prefetched into registers one sub-chunk ahead.
+// are prefetched into registers one sub-chunk ahead. Between the two groups,
+// the two independent passes run side by side on the two warp halves: warps
+// 0-3 solve for W (one state row per thread) while warps 4-7 store the state
+// checkpoint and decay the state, all 128 columns of a row per thread.
 // Operands written to shared memory are rounded to TF32; the state read as the
 // A operand is truncated to TF32 by the tensor core (it only feeds the sub-chunk's
 // Y and O); the state update uses split TF32 (x = hi + lo, three products) so
@@ -336,52 +339,12 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         }
       }
     }
-    // ---- state checkpoint and decay S <- S0 diag(gamma_C) in tensor memory
-    {
-      const bool ck = !kPf && (c % ck_every) == 0;
-      float* dst = kPf ? nullptr : P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
-      // prefill: BF16 checkpoint (value-first) of the state before this sub-chunk
-      const bool pck = kPf && pf.ck != nullptr && (c % pf.ck_every_chunks) == 0;
-      __nv_bfloat16* pdst = pck ? pf.ck + ((pf.ck_starts[n] + c / pf.ck_every_chunks) * P.Hv + h) * kDim * kDim +
-                                      (int64_t)sv * kDim + 64 * ch
-                                : nullptr;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        const int col = 64 * ch + 16 * q;
-        float x[16];
-        tc::tmem_ld16(tl + kColS + col, x);
-        if (pck) {
-          store_bf16x8(pdst + 16 * q, x);
-          store_bf16x8(pdst + 16 * q + 8, x + 8);
-        }
-        if (ck) {
-          // 4x4 blocks transposed across each lane quad: lane (quad base + j)
-          // then holds the four values of key col + 4 m + j
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            float y[4] = {x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]};
-            tc::quad_transpose(y, lane);
-            *reinterpret_cast<float4*>(dst + ckpt_index(sv & ~3, col + 4 * m + (lane & 3))) =
-                make_float4(y[0], y[1], y[2], y[3]);
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + col + 4 * m);
-          x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
-        }
-        tc::tmem_st16(tl + kColS + col, x);
-      }
-    }
-    if (__syncthreads_or(!ok)) { aborted = true; break; }  // A and B in shared memory
-    // ---- W by forward substitution: both warps of a state row solve for W; each then
-    // writes the u tape of half of the tokens and one TF32 part of W (the output's B W term
-    // is added by the tensor core with the state update)
-    {
+    if (warp < 4) {
+      // ---- warps 0-3: once A and B are in shared memory (warps 0 and 1 above), W by forward
+      // substitution for state row sv; the u tape of all 16 tokens; W's two TF32 parts
+      asm volatile("bar.sync 2, 128;" ::: "memory");
       float yp[16];
       tc::tmem_ld16(tl + kColYO, yp);
-      // right-looking substitution: once w_j is known it is removed from every
-      // later row, so the dependent chain is one FMA per token
       float w[kChunk], acc[kChunk];
 #pragma unroll
       for (int t = 0; t < kChunk; ++t) acc[t] = sm.Vs[t * kLds + sv] - yp[t];
@@ -398,34 +361,57 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             if (4 * q4 + e > j) acc[4 * q4 + e] = fmaf(-ar[e], w[j], acc[4 * q4 + e]);
         }
       }
-      // this warp's half of the tokens (compile-time): u tape and one TF32 part of W
-      auto emit = [&](auto chc) {
-        constexpr int c_h = decltype(chc)::value;
-        float xw[kChunk];
+      if constexpr (!kPf) {
 #pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const int t = 8 * c_h + tt;
-          if (!kPf && t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
+        for (int t = 0; t < kChunk; ++t)
+          if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
+      }
+      float xh[kChunk], xl[kChunk];
+#pragma unroll
+      for (int t = 0; t < kChunk; ++t) {
+        xh[t] = tc::round_tf32(w[t]);
+        xl[t] = tc::round_tf32(w[t] - xh[t]);
+      }
+      tc::tmem_st16(tl + kColW, xh);  // the tensor-memory A operand of the update
+      tc::tmem_st16(tl + kColW + 16, xl);
+    } else {
+      // ---- warps 4-7: state checkpoint and decay S <- S0 diag(gamma_C) of row sv, all columns
+      const bool ck = !kPf && (c % ck_every) == 0;
+      float* dst = kPf ? nullptr : P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
+      const bool pck = kPf && pf.ck != nullptr && (c % pf.ck_every_chunks) == 0;
+      __nv_bfloat16* pdst = pck ? pf.ck + ((pf.ck_starts[n] + c / pf.ck_every_chunks) * P.Hv + h) * kDim * kDim +
+                                      (int64_t)sv * kDim
+                                : nullptr;
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        const int col = 16 * q;
+        float x[16];
+        tc::tmem_ld16(tl + kColS + col, x);
+        if (pck) {
+          store_bf16x8(pdst + 16 * q, x);
+          store_bf16x8(pdst + 16 * q + 8, x + 8);
         }
+        if (ck) {
 #pragma unroll
-        for (int t4 = 0; t4 < 4; ++t4) {
-          float x[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float hi = tc::round_tf32(w[4 * t4 + e]);
-            x[e] = c_h == 0 ? hi : tc::round_tf32(w[4 * t4 + e] - hi);
+          for (int m = 0; m < 4; ++m) {
+            float y[4] = {x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]};
+            tc::quad_transpose(y, lane);
+            *reinterpret_cast<float4*>(dst + ckpt_index(sv & ~3, col + 4 * m + (lane & 3))) =
+                make_float4(y[0], y[1], y[2], y[3]);
           }
-          xw[4 * t4] = x[0]; xw[4 * t4 + 1] = x[1]; xw[4 * t4 + 2] = x[2]; xw[4 * t4 + 3] = x[3];
         }
-        tc::tmem_st16(tl + kColW + 16 * c_h, xw);  // the tensor-memory A operand of the update
-      };
-      if (ch == 0) emit(std::integral_constant<int, 0>{});
-      else emit(std::integral_constant<int, 1>{});
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + col + 4 * m);
+          x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
+        }
+        tc::tmem_st16(tl + kColS + col, x);
+      }
     }
     tc::tmem_wait_st();
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    if (__syncthreads_or(!ok)) { aborted = true; break; }
     // ---- tensor cores: S += W^T (k^ gamma_C / gamma) in split TF32 (hi hi + lo hi + hi lo), and
     // the output's W^T B^T added to S0 (q^ gamma)^T (W split, B in TF32)
     if (warp == 0) {
