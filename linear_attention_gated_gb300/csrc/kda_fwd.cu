@@ -26,7 +26,10 @@
 // are prefetched into registers one sub-chunk ahead. Between the two groups,
 // the two independent passes run side by side on the two warp halves: warps
 // 0-3 solve for W (one state row per thread) while warps 4-7 store the state
-// checkpoint and decay the state, all 128 columns of a row per thread.
+// checkpoint and decay the state. Value rows are placed in TMEM lanes so that
+// a 16-lane (.16x128b) load gives a thread four consecutive value rows of a
+// key column, which is one 16-byte group of the transposed checkpoint: the
+// checkpoint needs no exchange between lanes.
 // Operands written to shared memory are rounded to TF32; the state read as the
 // A operand is truncated to TF32 by the tensor core (it only feeds the sub-chunk's
 // Y and O); the state update uses split TF32 (x = hi + lo, three products) so
@@ -103,7 +106,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     }
   }
 
-  const int sv = 32 * (warp & 3) + lane;  // state row (TMEM lane) of this thread
+  const int sv = 32 * (warp & 3) + 4 * (lane & 7) + (lane >> 3);  // state row held in this thread's TMEM lane
   const int ch = warp >> 2;               // column half [64 ch, 64 ch + 64)
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) tc::mbar_init(tc::smem_u32(&sm.mbar), 1);
@@ -230,10 +233,10 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
 
   prefetch(0);
   prologue(0);
+  __syncthreads();  // the first prologue is complete; later ones end at the loop's last barrier
   for (int64_t c = 0; c < nchunks; ++c) {
     const int64_t tc0 = si.t0 + c * kChunk;
     const int nt = (int)((si.len - c * kChunk) < kChunk ? (si.len - c * kChunk) : kChunk);
-    __syncthreads();  // prologue of this sub-chunk complete; the previous update's MMA has finished
     // ---- operand tiles: token t, key quads q4 and q4 + 16
     {
       const int t = tid & 15;
@@ -375,37 +378,52 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       tc::tmem_st16(tl + kColW, xh);  // the tensor-memory A operand of the update
       tc::tmem_st16(tl + kColW + 16, xl);
     } else {
-      // ---- warps 4-7: state checkpoint and decay S <- S0 diag(gamma_C) of row sv, all columns
-      const bool ck = !kPf && (c % ck_every) == 0;
-      float* dst = kPf ? nullptr : P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim;
-      const bool pck = kPf && pf.ck != nullptr && (c % pf.ck_every_chunks) == 0;
-      __nv_bfloat16* pdst = pck ? pf.ck + ((pf.ck_starts[n] + c / pf.ck_every_chunks) * P.Hv + h) * kDim * kDim +
-                                      (int64_t)sv * kDim
-                                : nullptr;
+      // ---- warps 4-7: state checkpoint and decay S <- S0 diag(gamma_C), all columns
+      if constexpr (!kPf) {
+        // TMEM lanes 32 w + 8 j + a hold value rows 32 w + 4 a + j (j = 0..3), so the two .16x128b
+        // loads of a 16-column slice give this thread value rows 32 w + 4 (lane / 4) + 0..3 of the
+        // four key columns 4 i + lane % 4: one 16-byte group of the checkpoint layout each
+        float* dst = P.ckpt + ((si.ck_base + c / ck_every) * P.Hv + h) * kDim * kDim +
+                     ckpt_index(32 * (warp & 3) + 4 * (lane >> 2), lane & 3);
+        const bool ck = (c % ck_every) == 0;
 #pragma unroll 1
-      for (int q = 0; q < 8; ++q) {
-        const int col = 16 * q;
-        float x[16];
-        tc::tmem_ld16(tl + kColS + col, x);
-        if (pck) {
-          store_bf16x8(pdst + 16 * q, x);
-          store_bf16x8(pdst + 16 * q + 8, x + 8);
+        for (int q = 0; q < 8; ++q) {
+          const int col = 16 * q;
+          float x0[8], x1[8];
+          tc::tmem_ld16x128_nowait(tl + kColS + col, x0);
+          tc::tmem_ld16x128_nowait(tl + (16u << 16) + kColS + col, x1);
+          tc::tmem_wait_ld8x2(x0, x1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (ck)
+              *reinterpret_cast<float4*>(dst + 4 * (col + 4 * i)) = make_float4(x0[2 * i], x0[2 * i + 1], x1[2 * i], x1[2 * i + 1]);
+            const float gk = sm.gC[col + 4 * i + (lane & 3)];
+            x0[2 * i] *= gk; x0[2 * i + 1] *= gk; x1[2 * i] *= gk; x1[2 * i + 1] *= gk;
+          }
+          tc::tmem_st16x128(tl + kColS + col, x0);
+          tc::tmem_st16x128(tl + (16u << 16) + kColS + col, x1);
         }
-        if (ck) {
+      } else {
+        const bool pck = pf.ck != nullptr && (c % pf.ck_every_chunks) == 0;
+        __nv_bfloat16* pdst = pck ? pf.ck + ((pf.ck_starts[n] + c / pf.ck_every_chunks) * P.Hv + h) * kDim * kDim +
+                                        (int64_t)sv * kDim
+                                  : nullptr;
+#pragma unroll 1
+        for (int q = 0; q < 8; ++q) {
+          const int col = 16 * q;
+          float x[16];
+          tc::tmem_ld16(tl + kColS + col, x);
+          if (pck) {
+            store_bf16x8(pdst + 16 * q, x);
+            store_bf16x8(pdst + 16 * q + 8, x + 8);
+          }
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            float y[4] = {x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]};
-            tc::quad_transpose(y, lane);
-            *reinterpret_cast<float4*>(dst + ckpt_index(sv & ~3, col + 4 * m + (lane & 3))) =
-                make_float4(y[0], y[1], y[2], y[3]);
+            const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + col + 4 * m);
+            x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
           }
+          tc::tmem_st16(tl + kColS + col, x);
         }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 g4 = *reinterpret_cast<const float4*>(sm.gC + col + 4 * m);
-          x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
-        }
-        tc::tmem_st16(tl + kColS + col, x);
       }
     }
     tc::tmem_wait_st();

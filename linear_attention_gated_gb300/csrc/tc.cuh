@@ -225,21 +225,27 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 4x4 transpose among the four lanes of an aligned lane quad: on entry lane
-// (quad base + j) holds row j of the block, on exit it holds column j.
-__device__ __forceinline__ void quad_transpose(float x[4], int lane) {
-  const bool odd = lane & 1;
-  float a = odd ? x[0] : x[1];
-  float b = odd ? x[2] : x[3];
-  a = __shfl_xor_sync(0xffffffffu, a, 1);
-  b = __shfl_xor_sync(0xffffffffu, b, 1);
-  if (odd) { x[0] = a; x[2] = b; } else { x[1] = a; x[3] = b; }
-  const bool hi = lane & 2;
-  float c = hi ? x[0] : x[2];
-  float d = hi ? x[1] : x[3];
-  c = __shfl_xor_sync(0xffffffffu, c, 2);
-  d = __shfl_xor_sync(0xffffffffu, d, 2);
-  if (hi) { x[0] = c; x[1] = d; } else { x[2] = c; x[3] = d; }
+// Shape .16x128b, four repeats along the columns (16 columns of 16 lanes): register
+// 2 i + j of lane l holds lane (taddr lane) + 8 j + l / 4, column (taddr column) + 4 i + l % 4.
+__device__ __forceinline__ void tmem_ld16x128_nowait(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.ld.sync.aligned.16x128b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld8x2(float* a, float* b) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(a);
+  uint32_t* s = reinterpret_cast<uint32_t*>(b);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7])
+               :: "memory");
+}
+__device__ __forceinline__ void tmem_st16x128(uint32_t taddr, const float* v) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])));
 }
 
 }  // namespace tc
