@@ -3,9 +3,10 @@
 //
 // One CTA owns one (sequence, value head) unit and walks its tokens in
 // sub-chunks of kChunk = 16, keeping the 128x128 FP32 value-first state in
-// tensor memory (lane = value row), where it is also the accumulator of the
-// state update; two CTAs fit on one SM. Within a sub-chunk starting from state S0, with Gam_i the
-// cumulative log-decay of tokens 1..i (per key dim) and gamma_i = exp(Gam_i):
+// tensor memory (one value row per lane), where it is also the accumulator of
+// the state update; two CTAs fit on one SM. Within a sub-chunk starting from
+// state S0, with Gam_i the cumulative log-decay of tokens 1..i (per key dim)
+// and gamma_i = exp(Gam_i):
 //   A_ij = k^_i . (k^_j gamma_i / gamma_j)   (j < i)      B_ij likewise with q^_i (j <= i)
 //   Y    = V - (k^ gamma) S0^T
 //   W    solves (I + diag(beta) A) W = diag(beta) Y      (rows: beta_i u_i)
@@ -27,19 +28,20 @@
 // the two independent passes run side by side on the two warp halves: warps
 // 0-3 solve for W (one state row per thread) while warps 4-7 store the state
 // checkpoint, decay the state and build the (k^ gamma_C / gamma)^T operand of
-// the second group (needed by no earlier step). Value rows are placed in TMEM lanes so that
-// a 16-lane (.16x128b) load gives a thread four consecutive value rows of a
-// key column, which is one 16-byte group of the transposed checkpoint: the
-// checkpoint needs no exchange between lanes.
+// the second group (needed by no earlier step). Value rows are placed in TMEM
+// lanes so that a 16-lane (.16x128b) load gives a thread four consecutive
+// value rows of a key column, which is one 16-byte group of the transposed
+// checkpoint: the checkpoint needs no exchange between lanes.
 // Operands written to shared memory are rounded to TF32; the state read as the
-// A operand is truncated to TF32 by the tensor core (it only feeds the sub-chunk's
-// Y and O); the state update uses split TF32 (x = hi + lo, three products) so
-// that the carried FP32 state keeps FP32-level accuracy. Accumulation, the triangular solve, the output and the
-// state stay FP32. Each token's u = v - S' k^ and each sub-chunk's A and B
-// are saved for the backward. The gate, L2 norm
-// and sigmoid of each token are computed on chip (the fused prologue). The
-// state at the start of every checkpoint interval is stored for the backward
-// (transposed, in the layout the backward's tensor-core products read).
+// A operand is truncated to TF32 by the tensor core (it only feeds the
+// sub-chunk's Y and O); the state update uses split TF32 (x = hi + lo, three
+// products) so that the carried FP32 state keeps FP32-level accuracy.
+// Accumulation, the triangular solve, the output and the state stay FP32.
+// Each token's u = v - S' k^ and each sub-chunk's A and B are saved for the
+// backward. The gate, L2 norm and sigmoid of each token are computed on chip
+// (the fused prologue). The state at the start of every checkpoint interval is
+// stored for the backward (transposed, in the layout the backward's
+// tensor-core products read).
 #include <type_traits>
 
 #include "kda_common.cuh"
@@ -51,10 +53,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTileF = kChunk * kLds;
 constexpr uint32_t kTmemCols = 256;  // two CTAs per SM share the 512 columns
-constexpr uint32_t kColS = 0;        // FP32 state S (lane = value row v, column = key k)
+constexpr uint32_t kColS = 0;        // FP32 state S (one value row per lane, see sv below; column = key k)
 constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns; the last 16 then also take + W^T B^T
 constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T (M = 64): A in lanes 0..15, B in lanes 32..47, 16 columns
-constexpr uint32_t kColW = 176;      // W^T (lane = value row v, column = token): TF32 hi in 16 columns, lo in the next 16
+constexpr uint32_t kColW = 176;      // W^T (value rows as in S, column = token): TF32 hi in 16 columns, lo in the next 16
 
 struct FwdSmem {
   // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128). As the A operand of the A/B
