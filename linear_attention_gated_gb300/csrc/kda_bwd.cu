@@ -95,7 +95,7 @@ struct BwdSmem {
   float Ktp[kTileF];                      // k^, then k^ gamma (FP32)
   float Kip[kTileF];                      // k^ / gamma (FP32)
   float Up[kTileF];                       // u from the forward (cp.async staging)
-  float DUp[kTileF];                      // dV
+  float DUp[kTileF];                      // E (dV = diag(beta) E)
   __nv_bfloat16 Sq[kChunk * kDim];        // q, k, g, do of the sub-chunk (cp.async staging)
   __nv_bfloat16 Sk[kChunk * kDim];
   __nv_bfloat16 Sg[kChunk * kDim];
@@ -108,11 +108,10 @@ struct BwdSmem {
   float M2T[kChunk][kChunk];
   float bs[kChunk];
   float braw[kChunk];
-  float dba[kChunk];
+  float dba[kChunk];                      // dbeta before the sigmoid derivative
   float gC[kDim];
   float rho0[2][kDim];                    // halves of sum_v Gd * S0
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
-  float dbp[4][kChunk];                   // per-warp partial dbeta
   unsigned long long mbar[6];
   const float* ck_next[2];                // checkpoint of sub-chunk c - 1, for the MMA warp (slot (c - 1) & 1)
   uint32_t tmem_base;
@@ -529,20 +528,18 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       } else {
         ok = ok && tc::mbar_wait(mbD, ph);
         tc::fence_after();
-        // ---- P5: per value column (warps 0-3): dW, E, dV, dbeta partials
+        // ---- P5: per value column (warps 0-3): dW, E, dV
         const int vv = kl;
-        float acc[kChunk], pbv[kChunk];
+        float acc[kChunk], ev[kChunk];
         tc::tmem_ld16(tl + kColDW, acc);  // dW (rows v)
         // E solves (I + A^T diag(beta)) E = dW, last row first (right-looking)
-        float bsv[kChunk], upv[kChunk];
+        float bsv[kChunk];
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-          bsv[i] = sm.bs[i];
-          upv[i] = sm.Up[i * kLds + vv];
-        }
+        for (int i = 0; i < kChunk; ++i) bsv[i] = sm.bs[i];
 #pragma unroll
         for (int i = kChunk - 1; i >= 0; --i) {
           const float ei = acc[i];
+          ev[i] = ei;
           const float du = bsv[i] * ei;
           acc[i] = du;  // keep dV in place
           float arow[kChunk];
@@ -553,37 +550,11 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
           }
 #pragma unroll
           for (int m = 0; m < i; ++m) acc[m] = fmaf(-arow[m], du, acc[m]);
-          pbv[i] = ei * upv[i];
-        }
-        // dbeta partial sums over the warp's 32 value rows: halving butterfly
-        // (16 shuffles); lane l ends with the sum for token 8 b4 + 4 b3 + 2 b2 + b1
-        {
-          float y8[8], y4[4], y2[2];
-          const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float send = b4 ? pbv[j] : pbv[j + 8], keep = b4 ? pbv[j + 8] : pbv[j];
-            y8[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float send = b3 ? y8[j] : y8[j + 4], keep = b3 ? y8[j + 4] : y8[j];
-            y4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-          }
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const float send = b2 ? y4[j] : y4[j + 2], keep = b2 ? y4[j + 2] : y4[j];
-            y2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-          }
-          const float send = b1 ? y2[0] : y2[1], keep = b1 ? y2[1] : y2[0];
-          float y1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-          y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-          if ((lane & 1) == 0) sm.dbp[warp][(b4 ? 8 : 0) + (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0)] = y1;
         }
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
           if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(acc[i]);
-          sm.DUp[i * kLds + vv] = acc[i];
+          sm.DUp[i * kLds + vv] = ev[i];  // E; dV = diag(beta) E
         }
 #pragma unroll
         for (int a4 = 0; a4 < 4; ++a4) {
@@ -599,30 +570,35 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
       tc::fence_before();
       csync();
-      // dV rows of the S0^T dV^T operand (token ot, quads oq and oq + 16)
+      // dV rows (beta E) of the S0^T dV^T operand (token ot, quads oq and oq + 16)
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
         const int k0 = 4 * (oq + 16 * rep);
         const float4 d4 = *reinterpret_cast<const float4*>(sm.DUp + ot * kLds + k0);
+        const float bt = sm.bs[ot];
         *reinterpret_cast<float4*>(sm.dOU + tc::kmaj(16 + ot, k0, kDim)) =
-            make_float4(tc::round_tf32(d4.x), tc::round_tf32(d4.y), tc::round_tf32(d4.z), tc::round_tf32(d4.w));
+            make_float4(tc::round_tf32(bt * d4.x), tc::round_tf32(bt * d4.y), tc::round_tf32(bt * d4.z),
+                        tc::round_tf32(bt * d4.w));
       }
       tc::fence_async_smem();
       tc::fence_before();
       // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T;
       // every compute thread arrives once its own operand tiles are written (no CTA barrier)
       tc::mbar_arrive(rdy2);
-      if (tid < kChunk) sm.dba[tid] = sm.dbp[0][tid] + sm.dbp[1][tid] + sm.dbp[2][tid] + sm.dbp[3][tid];
-      {  // dV W^T in FP32, one entry (i, j) per thread
-        const int i = tid >> 4, j = tid & 15;
+      {  // dV W^T in FP32 as diag(beta) (E U^T) diag(beta), one entry (i, j) per thread; a warp
+         // takes a 4 (i) x 8 (j) block, so its float4 loads touch 4 rows of E and 8 rows of u
+         // (no bank conflicts); the diagonal of E U^T is dbeta
+        const int i = 4 * (warp >> 1) + (lane >> 3), j = 8 * (warp & 1) + (lane & 7);
         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int vv = 0; vv < kDim; vv += 4)
           fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
                *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
-        const float acc = hsum4(a4);
-        sm.M2[i][j] = acc * sm.bs[j];
-        sm.M2T[j][i] = acc * sm.bs[j];
+        const float acc = hsum4(a4);  // sum_v E_i U_j
+        if (i == j) sm.dba[i] = acc;  // dbeta_i = E_i . U_i (before the sigmoid derivative)
+        const float m2 = acc * sm.bs[i] * sm.bs[j];
+        sm.M2[i][j] = m2;
+        sm.M2T[j][i] = m2;
       }
       ok = ok && tc::mbar_wait(mb1, ph);
       ok = ok && tc::mbar_wait(mb2, ph);
