@@ -329,7 +329,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     }
     if (warp < 4) {
       // ---- warps 0-3: once A and B are in shared memory (warps 0 and 1 above), W by forward
-      // substitution for state row sv; the u tape of all 16 tokens; W's two TF32 parts
+      // substitution for state row sv; u of all 16 tokens into shared memory; W's two TF32 parts
       asm volatile("bar.sync 2, 128;" ::: "memory");
       float yp[16];
       tc::tmem_ld16(tl + kColYO, yp);
@@ -350,9 +350,10 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         }
       }
       if constexpr (!kPf) {
+        // u_t for the backward, staged in the first group's KQ tile (free until the next tile build)
+        float* us = reinterpret_cast<float*>(sm.KQ);
 #pragma unroll
-        for (int t = 0; t < kChunk; ++t)
-          if (t < nt) P.utape[((tc0 + t) * P.Hv + h) * kDim + sv] = acc[t];  // u_t for the backward
+        for (int t = 0; t < kChunk; ++t) us[t * kLds + sv] = acc[t];
       }
       float xh[kChunk], xl[kChunk];
 #pragma unroll
@@ -472,6 +473,14 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       for (int tt = 0; tt < 8; ++tt) {
         const int t = 8 * ch + tt;
         if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o8[tt]);
+      }
+    }
+    if constexpr (!kPf) {  // the u tape: token ti, value rows c8 .. c8 + 7
+      const float* us = reinterpret_cast<const float*>(sm.KQ);
+      if (ti < nt) {
+        float* dst = P.utape + ((tc0 + ti) * P.Hv + h) * kDim + c8;
+        *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(us + ti * kLds + c8);
+        *reinterpret_cast<float4*>(dst + 4) = *reinterpret_cast<const float4*>(us + ti * kLds + c8 + 4);
       }
     }
     if (__syncthreads_or(!ok)) { aborted = true; break; }
