@@ -26,9 +26,9 @@
 // sub-chunk's prologue runs while the second group is in flight. Token tiles
 // are prefetched into registers one sub-chunk ahead. Between the two groups,
 // the two independent passes run side by side on the two warp halves: warps
-// 0-3 solve for W (one state row per thread) while warps 4-7 store the state
-// checkpoint, decay the state and build the (k^ gamma_C / gamma)^T operand of
-// the second group (needed by no earlier step). Value rows are placed in TMEM
+// 0-3 solve for W (one state row per thread) and then build the (k^ gamma_C /
+// gamma)^T operand of the second group (needed by no earlier step) while warps
+// 4-7 store the state checkpoint and decay the state. Value rows are placed in TMEM
 // lanes so that a 16-lane (.16x128b) load gives a thread four consecutive
 // value rows of a key column, which is one 16-byte group of the transposed
 // checkpoint: the checkpoint needs no exchange between lanes.
@@ -329,7 +329,8 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     }
     if (warp < 4) {
       // ---- warps 0-3: once A and B are in shared memory (warps 0 and 1 above), W by forward
-      // substitution for state row sv; u of all 16 tokens into shared memory; W's two TF32 parts
+      // substitution for state row sv; u of all 16 tokens into shared memory; W's two TF32 parts;
+      // then the second group's (k^ gamma_C / gamma)^T operand
       asm volatile("bar.sync 2, 128;" ::: "memory");
       float yp[16];
       tc::tmem_ld16(tl + kColYO, yp);
@@ -363,9 +364,26 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       }
       tc::tmem_st16(tl + kColW, xh);  // the tensor-memory A operand of the update
       tc::tmem_st16(tl + kColW + 16, xl);
+      {  // (k^ gamma_C / gamma)^T as rows k (K = token) in TF32 hi + lo, for the second group: key k,
+         // all 16 tokens, each float4 store covering 4 tokens
+        const int k = tid;
+        const float gck = sm.gC[k];
+#pragma unroll 2
+        for (int t4 = 0; t4 < kChunk; t4 += 4) {
+          float hi[4], lo[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int t = t4 + j;
+            const float kb = sm.Pk[t * kLds + k] * (gck * __fdividef(1.0f, sm.Pa[t * kLds + k]));
+            hi[j] = tc::round_tf32(kb);
+            lo[j] = tc::round_tf32(kb - hi[j]);
+          }
+          *reinterpret_cast<float4*>(sm.KbT[0] + tc::kmaj(k, t4, kChunk)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<float4*>(sm.KbT[1] + tc::kmaj(k, t4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
     } else {
-      // ---- warps 4-7: state checkpoint and decay S <- S0 diag(gamma_C), all columns; then the
-      // second group's (k^ gamma_C / gamma)^T operand
+      // ---- warps 4-7: state checkpoint and decay S <- S0 diag(gamma_C), all columns
       if constexpr (!kPf) {
         // TMEM lanes 32 w + 8 j + a hold value rows 32 w + 4 a + j (j = 0..3), so the two .16x128b
         // loads of a 16-column slice give this thread value rows 32 w + 4 (lane / 4) + 0..3 of the
@@ -410,24 +428,6 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             x[4 * m] *= g4.x; x[4 * m + 1] *= g4.y; x[4 * m + 2] *= g4.z; x[4 * m + 3] *= g4.w;
           }
           tc::tmem_st16(tl + kColS + col, x);
-        }
-      }
-      {  // (k^ gamma_C / gamma)^T as rows k (K = token) in TF32 hi + lo, for the second group: key k,
-         // all 16 tokens, each float4 store covering 4 tokens
-        const int k = tid - 128;
-        const float gck = sm.gC[k];
-#pragma unroll 2
-        for (int t4 = 0; t4 < kChunk; t4 += 4) {
-          float hi[4], lo[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int t = t4 + j;
-            const float kb = sm.Pk[t * kLds + k] * (gck * __fdividef(1.0f, sm.Pa[t * kLds + k]));
-            hi[j] = tc::round_tf32(kb);
-            lo[j] = tc::round_tf32(kb - hi[j]);
-          }
-          *reinterpret_cast<float4*>(sm.KbT[0] + tc::kmaj(k, t4, kChunk)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<float4*>(sm.KbT[1] + tc::kmaj(k, t4, kChunk)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
