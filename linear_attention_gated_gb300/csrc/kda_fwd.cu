@@ -61,7 +61,8 @@ constexpr uint32_t kColW = 176;      // W^T (value rows as in S, column = token)
 struct FwdSmem {
   // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128). As the A operand of the A/B
   // product (M = 64) it is read as 64 rows: rows 32..63 fall on the tile below and only fill TMEM
-  // lanes that are never read.
+  // lanes that are never read. Once the first group has completed it holds, until the next tile
+  // build, the sub-chunk's u (16 rows of kLds floats) and B^T in FP32 (16 x 16) for the tapes.
   unsigned char KQ[32 * kDim * 4];
   unsigned char KiT[kChunk * kDim * 4];    // k^ / gamma rows t, TF32 (K-major, K = 128)
   unsigned char Bt[kChunk * kChunk * 4];   // B rows t, TF32 (K-major, K = 16): O += W^T B^T
@@ -293,11 +294,11 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     if (warp < 2) {
       // A (D rows 0..15: warp 0's lanes 0..15, strictly lower) and B (D rows 16..31: warp 1's
       // lanes 0..15, lower) from tensor memory (an M = 64 product places rows 16 w .. 16 w + 15
-      // in lanes 32 w .. 32 w + 15); for the backward the tape holds A row-major and B
-      // transposed (its columns are read there)
+      // in lanes 32 w .. 32 w + 15); the backward's tape, written by all threads after the
+      // second group, holds A row-major (from AsT) and B transposed (its columns are read
+      // there; from the FP32 copy that warp 1 leaves in the KQ tile)
       float d16[16];
       tc::tmem_ld16(tl + kColAB, d16);
-      float* tape = kPf ? nullptr : P.abtape + ((si.ch_base + c) * P.Hv + h) * 512;
       if (lane < kChunk) {
         const int i = lane;
         if (warp == 0) {
@@ -306,17 +307,11 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             d16[j] = j < i ? d16[j] : 0.f;
             sm.AsT[j][i] = d16[j];
           }
-          if constexpr (!kPf) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              *reinterpret_cast<float4*>(tape + i * 16 + 4 * q4) =
-                  make_float4(d16[4 * q4], d16[4 * q4 + 1], d16[4 * q4 + 2], d16[4 * q4 + 3]);
-          }
         } else {
 #pragma unroll
           for (int j = 0; j < kChunk; ++j) {
             d16[j] = j <= i ? d16[j] : 0.f;
-            if constexpr (!kPf) tape[256 + j * 16 + i] = d16[j];
+            if constexpr (!kPf) reinterpret_cast<float*>(sm.KQ)[kChunk * kLds + j * 16 + i] = d16[j];  // B^T, FP32
           }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -474,6 +469,11 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
         const int t = 8 * ch + tt;
         if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o8[tt]);
       }
+    }
+    if constexpr (!kPf) {  // the A/B tape: A row-major (from AsT), B transposed
+      float* tape = P.abtape + ((si.ch_base + c) * P.Hv + h) * 512;
+      tape[tid] = sm.AsT[tid & 15][tid >> 4];
+      tape[256 + tid] = reinterpret_cast<const float*>(sm.KQ)[kChunk * kLds + tid];
     }
     if constexpr (!kPf) {  // the u tape: token ti, value rows c8 .. c8 + 7
       const float* us = reinterpret_cast<const float*>(sm.KQ);
