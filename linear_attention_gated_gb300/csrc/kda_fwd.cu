@@ -461,13 +461,25 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     if (ok) ok = tc::mbar_wait_warp(mbar, parity);
     parity ^= 1;
     tc::fence_after();
-    {  // the output of this warp's half of the tokens: o = scale (S0 (q^ gamma)^T + W^T B^T)
-      float o8[8];
-      tc::tmem_ld8(tl + kColYO + 16 + 8 * ch, o8);
+    {  // the output of this warp's half of the tokens: o = scale (S0 (q^ gamma)^T + W^T B^T); two
+       // 16-lane loads give this thread value rows 32 w + 4 (lane / 4) + 0..3 of tokens
+       // 8 ch + 4 i + lane % 4 (i = 0, 1): one 8-byte store per token
+      float x0[4], x1[4];
+      tc::tmem_ld16x128x2_nowait(tl + kColYO + 16 + 8 * ch, x0);
+      tc::tmem_ld16x128x2_nowait(tl + (16u << 16) + kColYO + 16 + 8 * ch, x1);
+      tc::tmem_wait_ld4x2(x0, x1);
+      const int v0 = 32 * (warp & 3) + 4 * (lane >> 2);
 #pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        const int t = 8 * ch + tt;
-        if (t < nt) out.o[((tc0 + t) * P.Hv + h) * kDim + sv] = __float2bfloat16_rn(P.scale * o8[tt]);
+      for (int i = 0; i < 2; ++i) {
+        const int t = 8 * ch + 4 * i + (lane & 3);
+        if (t < nt) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(P.scale * x0[2 * i], P.scale * x0[2 * i + 1]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(P.scale * x1[2 * i], P.scale * x1[2 * i + 1]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(out.o + ((tc0 + t) * P.Hv + h) * kDim + v0) = pk;
+        }
       }
     }
     if constexpr (!kPf) {  // the A/B tape: A row-major (from AsT), B transposed

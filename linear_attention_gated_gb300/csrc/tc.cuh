@@ -241,6 +241,21 @@ __device__ __forceinline__ void tmem_wait_ld8x2(float* a, float* b) {
                  "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7])
                :: "memory");
 }
+// Shape .16x128b, two repeats (8 columns of 16 lanes): register 2 i + j of lane l holds lane
+// (taddr lane) + 8 j + l / 4, column (taddr column) + 4 i + l % 4.
+__device__ __forceinline__ void tmem_ld16x128x2_nowait(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.ld.sync.aligned.16x128b.x2.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld4x2(float* a, float* b) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(a);
+  uint32_t* s = reinterpret_cast<uint32_t*>(b);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3])
+               :: "memory");
+}
 __device__ __forceinline__ void tmem_st16x128(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
                ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
