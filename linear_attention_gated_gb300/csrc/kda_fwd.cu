@@ -69,6 +69,7 @@ struct FwdSmem {
   unsigned char KbT[2][kDim * kChunk * 4]; // (k^ gamma_C / gamma)^T, rows k, TF32 hi / lo (K = 16)
   float Pq[kTileF];                        // q^
   float Pk[kTileF];                        // k^
+  float Kif[kTileF];                       // k^ / gamma (FP32), from the tile build
   float Pa[kTileF];                        // log decay, then gamma
   float Vs[kTileF];                        // v
   float AsT[kChunk][kChunk];               // A transposed: AsT[j][t] = A[t][j]
@@ -266,6 +267,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             make_float4(tc::round_tf32(qt[0]), tc::round_tf32(qt[1]), tc::round_tf32(qt[2]), tc::round_tf32(qt[3]));
         *reinterpret_cast<float4*>(sm.KiT + tc::kmaj(t, k0, kDim)) =
             make_float4(tc::round_tf32(ki[0]), tc::round_tf32(ki[1]), tc::round_tf32(ki[2]), tc::round_tf32(ki[3]));
+        *reinterpret_cast<float4*>(sm.Kif + t * kLds + k0) = make_float4(ki[0], ki[1], ki[2], ki[3]);
       }
     }
     tc::fence_async_smem();
@@ -369,7 +371,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int t = t4 + j;
-            const float kb = sm.Pk[t * kLds + k] * (gck * __fdividef(1.0f, sm.Pa[t * kLds + k]));
+            const float kb = sm.Kif[t * kLds + k] * gck;
             hi[j] = tc::round_tf32(kb);
             lo[j] = tc::round_tf32(kb - hi[j]);
           }
