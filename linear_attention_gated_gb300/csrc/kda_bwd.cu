@@ -553,8 +553,20 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
         }
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-          if (i < nt) a.dv[((tc0 + i) * P.Hv + h) * kDim + vv] = __float2bfloat16_rn(acc[i]);
           sm.DUp[i * kLds + vv] = ev[i];  // E; dV = diag(beta) E
+        }
+#pragma unroll
+        for (int t4 = 0; t4 < kChunk; t4 += 4) {  // dv: lane (quad base + j) writes token t4 + j
+          float y[4] = {acc[t4], acc[t4 + 1], acc[t4 + 2], acc[t4 + 3]};
+          tc::quad_transpose(y, lane);
+          const int t = t4 + (lane & 3);
+          if (t < nt) {
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(y[0], y[1]), p1 = __floats2bfloat162_rn(y[2], y[3]);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&p0);
+            pk.y = *reinterpret_cast<uint32_t*>(&p1);
+            *reinterpret_cast<uint2*>(a.dv + ((tc0 + t) * P.Hv + h) * kDim + (vv & ~3)) = pk;
+          }
         }
 #pragma unroll
         for (int a4 = 0; a4 < 4; ++a4) {

@@ -263,5 +263,22 @@ __device__ __forceinline__ void tmem_st16x128(uint32_t taddr, const float* v) {
                  "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])));
 }
 
+// 4x4 transpose among the four lanes of an aligned lane quad: on entry lane (quad base + j) holds
+// row j of the block, on exit it holds column j (four shuffles; the whole warp takes part).
+__device__ __forceinline__ void quad_transpose(float x[4], int lane) {
+  const bool odd = lane & 1;
+  float a = odd ? x[0] : x[1];
+  float b = odd ? x[2] : x[3];
+  a = __shfl_xor_sync(0xffffffffu, a, 1);
+  b = __shfl_xor_sync(0xffffffffu, b, 1);
+  if (odd) { x[0] = a; x[2] = b; } else { x[1] = a; x[3] = b; }
+  const bool hi = lane & 2;
+  float c = hi ? x[0] : x[2];
+  float d = hi ? x[1] : x[3];
+  c = __shfl_xor_sync(0xffffffffu, c, 2);
+  d = __shfl_xor_sync(0xffffffffu, d, 2);
+  if (hi) { x[0] = c; x[1] = d; } else { x[2] = c; x[3] = d; }
+}
+
 }  // namespace tc
 }  // namespace kda
