@@ -57,12 +57,13 @@ constexpr uint32_t kColS = 0;        // FP32 state S (one value row per lane, se
 constexpr uint32_t kColYO = 128;     // S0 [k^g; q^g]^T : 32 columns; the last 16 then also take + W^T B^T
 constexpr uint32_t kColAB = 160;     // [k^g; q^g] (k^/g)^T (M = 64): A in lanes 0..15, B in lanes 32..47, 16 columns
 constexpr uint32_t kColW = 176;      // W^T (value rows as in S, column = token): TF32 hi in 16 columns, lo in the next 16
+constexpr uint32_t kColU = 208;      // u (value rows as in S, column = token), for the tape
 
 struct FwdSmem {
   // rows 0..15 k^ gamma, rows 16..31 q^ gamma (K-major, K = 128). As the A operand of the A/B
   // product (M = 64) it is read as 64 rows: rows 32..63 fall on the tile below and only fill TMEM
   // lanes that are never read. Once the first group has completed it holds, until the next tile
-  // build, the sub-chunk's u (16 rows of kLds floats) and B^T in FP32 (16 x 16) for the tapes.
+  // build, the sub-chunk's B^T in FP32 (16 x 16, after 16 x kLds floats) for the tape.
   unsigned char KQ[32 * kDim * 4];
   unsigned char KiT[kChunk * kDim * 4];    // k^ / gamma rows t, TF32 (K-major, K = 128)
   unsigned char Bt[kChunk * kChunk * 4];   // B rows t, TF32 (K-major, K = 16): O += W^T B^T
@@ -326,7 +327,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     }
     if (warp < 4) {
       // ---- warps 0-3: once A and B are in shared memory (warps 0 and 1 above), W by forward
-      // substitution for state row sv; u of all 16 tokens into shared memory; W's two TF32 parts;
+      // substitution for state row sv; u of all 16 tokens into tensor memory; W's two TF32 parts;
       // then the second group's (k^ gamma_C / gamma)^T operand
       asm volatile("bar.sync 2, 128;" ::: "memory");
       float yp[16];
@@ -347,12 +348,7 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
             if (4 * q4 + e > j) acc[4 * q4 + e] = fmaf(-ar[e], w[j], acc[4 * q4 + e]);
         }
       }
-      if constexpr (!kPf) {
-        // u_t for the backward, staged in the first group's KQ tile (free until the next tile build)
-        float* us = reinterpret_cast<float*>(sm.KQ);
-#pragma unroll
-        for (int t = 0; t < kChunk; ++t) us[t * kLds + sv] = acc[t];
-      }
+      if constexpr (!kPf) tc::tmem_st16(tl + kColU, acc);  // u_t for the backward's tape
       float xh[kChunk], xl[kChunk];
 #pragma unroll
       for (int t = 0; t < kChunk; ++t) {
@@ -489,12 +485,18 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
       tape[tid] = sm.AsT[tid & 15][tid >> 4];
       tape[256 + tid] = reinterpret_cast<const float*>(sm.KQ)[kChunk * kLds + tid];
     }
-    if constexpr (!kPf) {  // the u tape: token ti, value rows c8 .. c8 + 7
-      const float* us = reinterpret_cast<const float*>(sm.KQ);
-      if (ti < nt) {
-        float* dst = P.utape + ((tc0 + ti) * P.Hv + h) * kDim + c8;
-        *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(us + ti * kLds + c8);
-        *reinterpret_cast<float4*>(dst + 4) = *reinterpret_cast<const float4*>(us + ti * kLds + c8 + 4);
+    if constexpr (!kPf) {  // the u tape: value rows 32 w + 4 (lane / 4) + 0..3 of tokens 8 ch + 4 i + lane % 4
+      float u0[4], u1[4];
+      tc::tmem_ld16x128x2_nowait(tl + kColU + 8 * ch, u0);
+      tc::tmem_ld16x128x2_nowait(tl + (16u << 16) + kColU + 8 * ch, u1);
+      tc::tmem_wait_ld4x2(u0, u1);
+      const int v0 = 32 * (warp & 3) + 4 * (lane >> 2);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = 8 * ch + 4 * i + (lane & 3);
+        if (t < nt)
+          *reinterpret_cast<float4*>(P.utape + ((tc0 + t) * P.Hv + h) * kDim + v0) =
+              make_float4(u0[2 * i], u0[2 * i + 1], u1[2 * i], u1[2 * i + 1]);
       }
     }
     if (__syncthreads_or(!ok)) { aborted = true; break; }
