@@ -28,7 +28,9 @@
 // the two independent passes run side by side on the two warp halves: warps
 // 0-3 solve for W (one state row per thread) and then build the (k^ gamma_C /
 // gamma)^T operand of the second group (needed by no earlier step) while warps
-// 4-7 store the state checkpoint and decay the state. Value rows are placed in TMEM
+// 4-7 store the state checkpoint and decay the state. The 16x16 A and B are read
+// out of TMEM before the solve by warps 0, 1 (columns 0-7) and 4, 5 (columns
+// 8-15, the same lane quarters; prefill: warps 0, 1 alone). Value rows are placed in TMEM
 // lanes so that a 16-lane (.16x128b) load gives a thread four consecutive
 // value rows of a key column, which is one 16-byte group of the transposed
 // checkpoint: the checkpoint needs no exchange between lanes.
@@ -294,42 +296,45 @@ kda_fwd_kernel(const Problem P, const FwdOut out, const PrefillArgs pf) {
     if (ok) ok = tc::mbar_wait_warp(mbar, parity);
     parity ^= 1;
     tc::fence_after();
-    if (warp < 2) {
-      // A (D rows 0..15: warp 0's lanes 0..15, strictly lower) and B (D rows 16..31: warp 1's
-      // lanes 0..15, lower) from tensor memory (an M = 64 product places rows 16 w .. 16 w + 15
-      // in lanes 32 w .. 32 w + 15); the backward's tape, written by all threads after the
-      // second group, holds A row-major (from AsT) and B transposed (its columns are read
-      // there; from the FP32 copy that warp 1 leaves in the KQ tile)
-      float d16[16];
-      tc::tmem_ld16(tl + kColAB, d16);
+    // A (D rows 0..15: lanes 0..15 of lane quarter 0, strictly lower) and B (D rows 16..31: lanes
+    // 0..15 of quarter 1, lower) from tensor memory (an M = 64 product places rows 16 w .. 16 w + 15
+    // in lanes 32 w .. 32 w + 15). Training: warps 0 / 1 take columns 0..7 and warps 4 / 5 columns
+    // 8..15 (warps 4-7 reach this point well ahead of their own pass's end); prefill: warps 0 / 1
+    // take all 16 (measured faster there, with no tape copy to make). The backward's tape, written
+    // by all threads after the second group, holds A row-major (from AsT) and B transposed (its
+    // columns are read there; from the FP32 copy left in the KQ tile)
+    constexpr int kRb = kPf ? 16 : 8;  // columns per readback thread
+    if ((warp & 3) < 2 && (!kPf || warp < 4)) {
+      const int j0 = 8 * (warp >> 2);
+      float d8[kRb];
+      if constexpr (kRb == 16) tc::tmem_ld16(tl + kColAB, d8);
+      else tc::tmem_ld8(tl + kColAB + j0, d8);
       if (lane < kChunk) {
         const int i = lane;
-        if (warp == 0) {
+        if ((warp & 3) == 0) {
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) {
-            d16[j] = j < i ? d16[j] : 0.f;
-            sm.AsT[j][i] = d16[j];
-          }
+          for (int jj = 0; jj < kRb; ++jj) sm.AsT[j0 + jj][i] = j0 + jj < i ? d8[jj] : 0.f;
         } else {
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) {
-            d16[j] = j <= i ? d16[j] : 0.f;
-            if constexpr (!kPf) reinterpret_cast<float*>(sm.KQ)[kChunk * kLds + j * 16 + i] = d16[j];  // B^T, FP32
+          for (int jj = 0; jj < kRb; ++jj) {
+            d8[jj] = j0 + jj <= i ? d8[jj] : 0.f;
+            if constexpr (!kPf) reinterpret_cast<float*>(sm.KQ)[kChunk * kLds + (j0 + jj) * 16 + i] = d8[jj];  // B^T
           }
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            *reinterpret_cast<float4*>(sm.Bt + tc::kmaj(i, 4 * q4, kChunk)) =
-                make_float4(tc::round_tf32(d16[4 * q4]), tc::round_tf32(d16[4 * q4 + 1]), tc::round_tf32(d16[4 * q4 + 2]),
-                            tc::round_tf32(d16[4 * q4 + 3]));
+          for (int q4 = 0; q4 < kRb / 4; ++q4) {
+            *reinterpret_cast<float4*>(sm.Bt + tc::kmaj(i, j0 + 4 * q4, kChunk)) =
+                make_float4(tc::round_tf32(d8[4 * q4]), tc::round_tf32(d8[4 * q4 + 1]), tc::round_tf32(d8[4 * q4 + 2]),
+                            tc::round_tf32(d8[4 * q4 + 3]));
           }
         }
       }
+      if (warp >= 4) asm volatile("bar.arrive 2, 192;" ::: "memory");  // warps 0-3 wait on it below
     }
     if (warp < 4) {
-      // ---- warps 0-3: once A and B are in shared memory (warps 0 and 1 above), W by forward
+      // ---- warps 0-3: once A and B are in shared memory (warps 0, 1, 4, 5 above), W by forward
       // substitution for state row sv; u of all 16 tokens into tensor memory; W's two TF32 parts;
       // then the second group's (k^ gamma_C / gamma)^T operand
-      asm volatile("bar.sync 2, 128;" ::: "memory");
+      asm volatile("bar.sync 2, %0;" ::"n"(kPf ? 128 : 192) : "memory");  // warps 0-3 (and 4, 5 in training)
       float yp[16];
       tc::tmem_ld16(tl + kColYO, yp);
       float w[kChunk], acc[kChunk];
