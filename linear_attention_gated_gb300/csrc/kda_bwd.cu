@@ -597,16 +597,49 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T;
       // every compute thread arrives once its own operand tiles are written (no CTA barrier)
       tc::mbar_arrive(rdy2);
-      {  // dV W^T in FP32 as diag(beta) (E U^T) diag(beta), one entry (i, j) per thread; a warp
-         // takes a 4 (i) x 8 (j) block, so its float4 loads touch 4 rows of E and 8 rows of u
-         // (no bank conflicts); the diagonal of E U^T is dbeta
-        const int i = 4 * (warp >> 1) + (lane >> 3), j = 8 * (warp & 1) + (lane & 7);
-        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int vv = 0; vv < kDim; vv += 4)
-          fma4(a4, *reinterpret_cast<const float4*>(sm.DUp + i * kLds + vv),
-               *reinterpret_cast<const float4*>(sm.Up + j * kLds + vv));
-        const float acc = hsum4(a4);  // sum_v E_i U_j
+      {  // dV W^T in FP32 as diag(beta) (E U^T) diag(beta): a warp takes a 4 (i) x 8 (j) block of
+         // entries, a lane a 2 x 4 block over an eighth o of the value columns (float4 groups
+         // 4 o + 32 m), so that each 16-byte load feeds 16 or 32 FMAs instead of 4 (the loop is bound
+         // by shared-memory wavefronts); an 8-lane phase reads 128 contiguous bytes of one row. A
+         // reduce-scatter over the eight lanes of a block (three shuffle rounds) leaves entry o in
+         // lane o; the diagonal of E U^T is dbeta. Only the strict lower triangle of M2 is read
+         // (by the combination), so 12 of the 32 blocks, wholly above the diagonal, load nothing
+        constexpr int BI = 2, BJ = 4, KS = BI * BJ;
+        const int o = lane % KS, g = lane / KS;
+        const int i0 = 4 * (warp >> 1) + BI * (g / (8 / BJ)), j0 = 8 * (warp & 1) + BJ * (g % (8 / BJ));
+        const float* e0 = sm.DUp + i0 * kLds + 4 * o;
+        const float* u0 = sm.Up + j0 * kLds + 4 * o;
+        float ac[KS];
+#pragma unroll
+        for (int e = 0; e < KS; ++e) ac[e] = 0.f;
+        // blocks wholly above the diagonal (i0 + 1 < j0) are not needed: their lanes keep zeros
+        const int mend = i0 + BI - 1 >= j0 ? 32 / KS : 0;
+#pragma unroll 2
+        for (int m = 0; m < mend; ++m) {
+          float4 a[BI], x[BJ];
+#pragma unroll
+          for (int ii = 0; ii < BI; ++ii) a[ii] = *reinterpret_cast<const float4*>(e0 + ii * kLds + 4 * KS * m);
+#pragma unroll
+          for (int jj = 0; jj < BJ; ++jj) x[jj] = *reinterpret_cast<const float4*>(u0 + jj * kLds + 4 * KS * m);
+#pragma unroll
+          for (int ii = 0; ii < BI; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < BJ; ++jj) {
+              float& r = ac[BJ * ii + jj];
+              r = fmaf(a[ii].w, x[jj].w, fmaf(a[ii].z, x[jj].z, fmaf(a[ii].y, x[jj].y, fmaf(a[ii].x, x[jj].x, r))));
+            }
+        }
+#pragma unroll
+        for (int w = KS / 2; w >= 1; w >>= 1) {
+          const bool up = o & w;
+#pragma unroll
+          for (int r = 0; r < w; ++r) {
+            const float mine = up ? ac[w + r] : ac[r], oth = up ? ac[r] : ac[w + r];
+            ac[r] = mine + __shfl_xor_sync(0xffffffffu, oth, w);
+          }
+        }
+        const float acc = ac[0];  // sum_v E_i U_j
+        const int i = i0 + o / BJ, j = j0 + o % BJ;
         if (i == j) sm.dba[i] = acc;  // dbeta_i = E_i . U_i (before the sigmoid derivative)
         const float m2 = acc * sm.bs[i] * sm.bs[j];
         sm.M2[i][j] = m2;
