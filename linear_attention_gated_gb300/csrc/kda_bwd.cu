@@ -39,8 +39,13 @@
 // to TF32 in place after sum_v Gd * S0 has been taken from it in FP32. Gd is
 // read by the tensor core at TF32 (truncated); Gd^T W^T adds the product of
 // Gd^T's truncated-away low part, so it is split TF32 on both sides. dO W^T
-// (dO exact in TF32, W split) also runs on the tensor core. The
-// forward's FP32 A and B of each sub-chunk are reused. The next sub-chunk's
+// (dO exact in TF32, W split) also runs on the tensor core. The first group
+// (dW first, then Gd^T W^T and dO W^T) runs while warps 0-3 solve for E; the
+// dO half of the adjoint update follows it once warps 4-7 have stored the
+// (scale q^ gamma, -k^ gamma) tile; the second group, once dV is in place, is
+// S0^T [dO; dV]^T as one N = 32 product (the staged checkpoint is read once)
+// and the dV half of the update. The forward's FP32 A and B of each sub-chunk
+// are reused. The next sub-chunk's
 // token tiles, u and A/B are prefetched with cp.async into buffers freed
 // earlier in the current sub-chunk; its state checkpoint (64 KiB, contiguous)
 // arrives by four bulk copies that the MMA warp issues once the second group
@@ -72,7 +77,7 @@ constexpr uint32_t kColGT = 128;  // G^T, the same adjoint transposed (lanes k, 
 constexpr uint32_t kColGL = 256;  // Gd^T minus its TF32 truncation (the part the tensor core drops)
 constexpr uint32_t kColDW = 384;  // Gd (k^ / gamma)^T : lanes v, 16 columns
 constexpr uint32_t kColQ = 400;   // S0^T dO^T : lanes k, 16 columns
-constexpr uint32_t kColR = 416;   // S0^T dV^T : lanes k, 16 columns
+constexpr uint32_t kColR = 416;   // S0^T dV^T : lanes k, 16 columns (right after Q: one N = 32 product)
 constexpr uint32_t kColWG = 432;  // Gd^T [W_hi; W_lo]^T : lanes k, 32 columns
 constexpr uint32_t kColM1 = 464;  // dO [W_hi; W_lo]^T : lanes 0..15 (token i), 32 columns
 
@@ -112,7 +117,7 @@ struct BwdSmem {
   float gC[kDim];
   float rho0[2][kDim];                    // halves of sum_v Gd * S0
   float rho2[2][kDim];                    // halves of sum_i (k^/g)_i (W Gd)_i
-  unsigned long long mbar[6];
+  unsigned long long mbar[7];
   const float* ck_next[2];                // checkpoint of sub-chunk c - 1, for the MMA warp (slot (c - 1) & 1)
   uint32_t tmem_base;
 };
@@ -147,7 +152,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem_base), kTmemCols);
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 6; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), i == 3 || i == 4 ? kThreads : 1);
+    for (int i = 0; i < 7; ++i) tc::mbar_init(tc::smem_u32(&sm.mbar[i]), i == 3 || i == 4 ? kThreads : i == 6 ? 128 : 1);
   }
   tc::fence_before();
   __syncthreads();
@@ -159,6 +164,7 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
   // compute -> MMA warp: each of the 256 compute threads arrives once its operand tiles are stored
   const uint32_t rdy1 = tc::smem_u32(&sm.mbar[3]), rdy2 = tc::smem_u32(&sm.mbar[4]);
   const uint32_t mbS = tc::smem_u32(&sm.mbar[5]);  // a sub-chunk's checkpoint has landed in S0s
+  const uint32_t rdyQ = tc::smem_u32(&sm.mbar[6]);  // warps 4-7 -> MMA warp: the QKT tile is stored
   uint32_t ph = 0;  // every barrier completes once per sub-chunk
   bool ok = true;
   bool aborted = false;
@@ -212,16 +218,16 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       // sub-chunk, so that ptxas forms each step's descriptor with one add next to its MMA
       // instead of hoisting every (tile, step) descriptor out of the loop into registers.
       const uint64_t kKi = tc::kdesc(tc::smem_u32(sm.Ki), 0, kDim), kS0 = tc::sdesc(tc::smem_u32(sm.S0s), 2048u, 128u);
-      const uint64_t kDou = tc::kdesc(tc::smem_u32(sm.dOU), 0, kDim), kDv = tc::kdesc(tc::smem_u32(sm.dOU) + 2 * 4096, 0, kDim);
+      const uint64_t kDou = tc::kdesc(tc::smem_u32(sm.dOU), 0, kDim);
       const uint64_t kWt = tc::kdesc(tc::smem_u32(sm.Wt[0]), 0, kDim), kDouv = tc::kdesc(tc::smem_u32(sm.dOUv), 0, 32);
       const uint64_t kBs0 = tc::kdesc(tc::smem_u32(sm.Bsc[0]), 0, kChunk), kBs1 = tc::kdesc(tc::smem_u32(sm.Bsc[1]), 0, kChunk);
       const uint64_t kQkt = tc::kdesc(tc::smem_u32(sm.QKT), 0, 32), kDul = tc::kdesc(tc::smem_u32(sm.dUlo), 0, kChunk);
       for (int64_t c = nchunks - 1; c >= 0; --c) {
         if (!tc::mbar_wait(rdy1, mph)) break;
         tc::fence_after();
-        uint64_t dKi = kKi, dS0 = kS0, dDou = kDou, dDv = kDv, dWt = kWt, dDouv = kDouv, dBs0 = kBs0, dBs1 = kBs1,
+        uint64_t dKi = kKi, dS0 = kS0, dDou = kDou, dWt = kWt, dDouv = kDouv, dBs0 = kBs0, dBs1 = kBs1,
                  dQkt = kQkt, dDul = kDul;
-        asm volatile("" : "+l"(dKi), "+l"(dS0), "+l"(dDou), "+l"(dDv), "+l"(dWt));
+        asm volatile("" : "+l"(dKi), "+l"(dS0), "+l"(dDou), "+l"(dWt));
         asm volatile("" : "+l"(dDouv), "+l"(dBs0), "+l"(dBs1), "+l"(dQkt), "+l"(dDul));
         {
           const uint32_t i16 = tc::idesc_tf32(128, 16), i32 = tc::idesc_tf32(128, 32);
@@ -236,10 +242,8 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
             tc::mma_ss(tbase + kColDW, dDouv + 16u * st, dBs1 + 16u * st, i16, 1);
           tc::mma_commit(mbD);
 #pragma unroll
-          for (int st = 0; st < kDim / 8; ++st) {
-            tc::mma_ss(tbase + kColQ, dS0 + 256u * st, dDou + 16u * st, i16, st > 0);
+          for (int st = 0; st < kDim / 8; ++st)
             tc::mma_ts(tbase + kColWG, tbase + kColGT + 8 * st, dWt + 16u * st, i32, st > 0);
-          }
 #pragma unroll
           for (int st = 0; st < kDim / 8; ++st)  // the low part of Gd^T with [W_hi; W_lo]
             tc::mma_ts(tbase + kColWG, tbase + kColGL + 8 * st, dWt + 16u * st, i32, 1);
@@ -251,15 +255,27 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
             tc::mma_ss(tbase + kColM1, dDou + 16u * st, dWt + 16u * st, tc::idesc_tf32(64, 32), st > 0);
           tc::mma_commit(mb1);
         }
+        // the dO half of the adjoint update, once QKT is stored and the first group (which reads G
+        // and G^T) has completed; the second group's commit covers it
+        if (!tc::mbar_wait(rdyQ, mph) || !tc::mbar_wait(mb1, mph)) break;
+        tc::fence_after();
+        {
+          const uint32_t i128 = tc::idesc_tf32(128, 128);
+#pragma unroll
+          for (int st = 0; st < 2; ++st) {
+            tc::mma_ss(tbase + kColGT, dQkt + 16u * st, dDouv + 16u * st, i128, 1);
+            tc::mma_ss(tbase + kColG, dDouv + 16u * st, dQkt + 16u * st, i128, 1);
+          }
+        }
         if (!tc::mbar_wait(rdy2, mph)) break;
         tc::fence_after();
         {
-          const uint32_t i16 = tc::idesc_tf32(128, 16), i128 = tc::idesc_tf32(128, 128);
+          const uint32_t i32 = tc::idesc_tf32(128, 32), i128 = tc::idesc_tf32(128, 128);
 #pragma unroll
-          for (int st = 0; st < kDim / 8; ++st)  // S0^T dV^T (dV: rows 16..31 of dOU)
-            tc::mma_ss(tbase + kColR, dS0 + 256u * st, dDv + 16u * st, i16, st > 0);
+          for (int st = 0; st < kDim / 8; ++st)  // S0^T [dO; dV]^T (dOU rows 0..31) into the Q and R columns
+            tc::mma_ss(tbase + kColQ, dS0 + 256u * st, dDou + 16u * st, i32, st > 0);
 #pragma unroll
-          for (int st = 0; st < 4; ++st) {
+          for (int st = 2; st < 4; ++st) {  // the dV half (the dO half was issued after the first group)
             tc::mma_ss(tbase + kColGT, dQkt + 16u * st, dDouv + 16u * st, i128, 1);
             tc::mma_ss(tbase + kColG, dDouv + 16u * st, dQkt + 16u * st, i128, 1);
           }
@@ -485,12 +501,13 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       tc::fence_async_smem();
       tc::fence_before();
       // ---- MMA group 1 (issued by the MMA warp): dW = Gd (k^/g)^T + scale dO^T B first (the dV
-      // chain needs it), then S0^T dO^T, Gd^T W^T and dO W^T; every compute thread arrives once its
-      // own operand tiles are written (no CTA barrier)
+      // chain needs it), then Gd^T W^T and dO W^T; every compute thread arrives once its own operand
+      // tiles are written (no CTA barrier)
       tc::mbar_arrive(rdy1);
       if (warp >= 4) {
         ok = ok && tc::mbar_wait(rdy1, ph);  // QKT below reads every thread's q^g and k^g rows
-        {  // QKT, rows k: columns 0..15 scale q^g, 16..31 -k^g (the adjoint updates of the second group)
+        {  // QKT, rows k: columns 0..15 scale q^g, 16..31 -k^g (the adjoint updates); once it is stored,
+           // the MMA warp issues the dO half of the update after the first group
           const int k = tid - 128;
 #pragma unroll
           for (int t4 = 0; t4 < kChunk; t4 += 4) {
@@ -503,6 +520,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
             *reinterpret_cast<float4*>(sm.QKT + tc::kmaj(k, t4, 32)) = make_float4(qv[0], qv[1], qv[2], qv[3]);
             *reinterpret_cast<float4*>(sm.QKT + tc::kmaj(k, 16 + t4, 32)) = make_float4(kv[0], kv[1], kv[2], kv[3]);
           }
+          tc::fence_async_smem();
+          tc::fence_before();
+          tc::mbar_arrive(rdyQ);
         }
         // dO W^T = dO (W_hi + W_lo)^T from tensor memory (dO is exact in TF32)
         ok = ok && tc::mbar_wait(mb1, ph);
@@ -594,8 +614,9 @@ kda_bwd_kernel(const Problem P, const BwdArgs a) {
       }
       tc::fence_async_smem();
       tc::fence_before();
-      // ---- MMA group 2 (issued by the MMA warp): S0^T dV^T and the adjoint update of G and G^T;
-      // every compute thread arrives once its own operand tiles are written (no CTA barrier)
+      // ---- MMA group 2 (issued by the MMA warp): S0^T [dO; dV]^T and the dV half of the adjoint
+      // update of G and G^T; every compute thread arrives once its own operand tiles are written (no
+      // CTA barrier)
       tc::mbar_arrive(rdy2);
       {  // dV W^T in FP32 as diag(beta) (E U^T) diag(beta): a warp takes a 4 (i) x 8 (j) block of
          // entries, a lane a 2 x 4 block over an eighth o of the value columns (float4 groups
